@@ -1,0 +1,92 @@
+"""Seeded synthetic inputs for the GLA prefill forward pass.
+
+This module only draws random numbers and names workloads. It holds none of the
+method's arithmetic, and it is the one module that both the CUDA path's tests/bench
+and the oracle consume.
+
+Recipe (the same for every workload; the pages measure on random shapes, not on a
+dataset — "Linear Attention 在 GPU 上到底慢在哪", section 实验设计):
+
+* ``torch.Generator('cpu').manual_seed(seed)``; draw order q, k, v, u, then h0, each a
+  float32 ``randn`` of its full shape.
+* q, k, v ~ N(0, 1), shapes [B, T, H, Dk] / [B, T, H, Dv].
+* log-gate g = logsigmoid(u) / 16 with u ~ N(0, 1), one value per token, head and key
+  dimension, kept in float32.
+* h0 = 0.02 * N(0, 1) (standard deviation 0.02) where a workload carries a state in.
+* scale = Dk ** -0.5.
+* bf16 workloads round q, k, v to bf16 after drawing; g and h0 stay float32.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, replace
+
+import torch
+import torch.nn.functional as F
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    T: int
+    H: int
+    Dk: int = 128
+    Dv: int = 128
+    io: str = "bf16"          # dtype of q, k, v, o: "bf16" or "f32"
+    seed: int = 0
+    with_h0: bool = False     # draw a nonzero initial state
+    want_hT: bool = False     # the workload returns the final state
+
+    @property
+    def tokens(self) -> int:
+        return self.B * self.T
+
+    def with_(self, **kw) -> "Workload":
+        return replace(self, **kw)
+
+
+# The five parity workloads (sizes from the pages' test grid and latency table).
+WORKLOADS = {
+    "f32_B1_H2_T512": Workload("f32_B1_H2_T512", B=1, T=512, H=2, io="f32", seed=0),
+    "bf16_B1_H16_T4096": Workload("bf16_B1_H16_T4096", B=1, T=4096, H=16, seed=1),
+    "bf16_B1_H16_T16384": Workload("bf16_B1_H16_T16384", B=1, T=16384, H=16, seed=2),
+    "bf16_B4_H16_T16384": Workload("bf16_B4_H16_T16384", B=4, T=16384, H=16, seed=2),
+    "bf16_B16_H16_T4096": Workload("bf16_B16_H16_T4096", B=16, T=4096, H=16, seed=3),
+    "bf16_B1_H16_T131072_h0": Workload("bf16_B1_H16_T131072_h0", B=1, T=131072, H=16, seed=4,
+                                       with_h0=True, want_hT=True),
+}
+
+# The workload the throughput metric is quoted on (B=1, H=16, T=16K, D=128, bf16).
+BENCH_WORKLOAD = "bf16_B1_H16_T16384"
+
+
+def make_inputs(w: Workload, device: str | torch.device = "cpu") -> dict:
+    """Draw the inputs of workload ``w`` on the CPU generator and move them to ``device``.
+
+    Returns a dict with q, k, v (bf16 or float32), g (float32), h0 (float32 or None)
+    and scale (python float).
+    """
+    gen = torch.Generator("cpu").manual_seed(w.seed)
+    io = torch.bfloat16 if w.io == "bf16" else torch.float32
+
+    def draw(*shape):
+        return torch.randn(*shape, generator=gen, dtype=torch.float32)
+
+    q = draw(w.B, w.T, w.H, w.Dk).to(io)
+    k = draw(w.B, w.T, w.H, w.Dk).to(io)
+    v = draw(w.B, w.T, w.H, w.Dv).to(io)
+    g = F.logsigmoid(draw(w.B, w.T, w.H, w.Dk)) / 16.0
+    h0 = draw(w.B, w.H, w.Dk, w.Dv) * 0.02 if w.with_h0 else None
+    out = dict(q=q, k=k, v=v, g=g, h0=h0, scale=float(w.Dk) ** -0.5)
+    if str(device) != "cpu":
+        for key in ("q", "k", "v", "g", "h0"):
+            if out[key] is not None:
+                out[key] = out[key].to(device)
+    return out
+
+
+def small(name: str, B: int, T: int, H: int, io: str = "bf16", seed: int = 0,
+          with_h0: bool = False, Dk: int = 128, Dv: int = 128) -> Workload:
+    """An ad-hoc workload with the same distributions (tests use these for edge cases)."""
+    return Workload(name, B=B, T=T, H=H, Dk=Dk, Dv=Dv, io=io, seed=seed, with_h0=with_h0,
+                    want_hT=True)
