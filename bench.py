@@ -1,0 +1,425 @@
+#!/usr/bin/env python3
+"""Throughput bench for the GLA prefill forward (one JSON line on rank 0).
+
+    python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+
+A step is one gla_fwd call over the whole workload (B=1, H=16, T=16384, Dk=Dv=128,
+bf16 q/k/v/o, fp32 log-gates), inputs resident in HBM. L2 is flushed (a 256 MiB
+device write) before every step, outside the timed events. Each step is timed with
+CUDA events on the launching stream; value = tokens (B*T, summed over ranks) / the
+max over ranks of the summed step times.
+
+Under torchrun (N > 1) every rank runs its own copy of the workload on its own GPU
+(weak scaling, no collective on the data path; the (batch, head) problems are
+independent). The reference arm (--impl reference) times the fp64 CPU oracle on a
+bounded sample of the same workload, on rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GLA prefill fwd tokens/s (B·T, H=16 D=128 bf16) and % of HBM/tensor roofline"
+UNIT = "tokens/s"
+FLUSH_BYTES = 256 << 20
+KERNEL_SOURCES = {
+    "tc": ["chunkwise_recurrent_prefill_gb300/csrc/gla_tc.cu"],
+    "exact": ["chunkwise_recurrent_prefill_gb300/csrc/gla_exact.cu"],
+}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=None)
+    ap.add_argument("--path", default="auto", choices=["auto", "tc", "exact"])
+    ap.add_argument("--seq-splits", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU work of the oracle baseline sample")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ workload arithmetic
+
+def algorithmic_bytes(w) -> int:
+    """Bytes a forward must move at least: q, k, v read, o written (io dtype), g read
+    (fp32), plus h0 read / hT written when the workload carries them."""
+    es = 2 if w.io == "bf16" else 4
+    per_token_head = 2 * w.Dk * es + w.Dv * es + w.Dv * es + w.Dk * 4
+    n = w.B * w.T * w.H * per_token_head
+    state = w.B * w.H * w.Dk * w.Dv * 4
+    return n + (state if w.with_h0 else 0) + (state if w.want_hT else 0)
+
+
+def algorithmic_flops(w, C: int = 64) -> int:
+    """Chunkwise flops (causal half of the in-chunk products): per token and head
+    4*Dk*Dv (state contribution and q.S) + (C+1)*(Dk+Dv) (q.k^T and P.v)."""
+    return w.B * w.T * w.H * (4 * w.Dk * w.Dv + (C + 1) * (w.Dk + w.Dv))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def source_sha(path_kind: str) -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES.get(path_kind, []):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def committed_traffic(kernel_kind: str, workload: str):
+    """Per-launch DRAM bytes from the committed ncu summary, or None if the kernel source
+    changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        entries = json.load(f)
+    sha = source_sha(kernel_kind)
+    for e in entries:
+        if e.get("kernel_kind") == kernel_kind and e.get("workload") == workload \
+                and e.get("source_sha256") == sha:
+            return int(e["dram_bytes_per_launch"])
+    return None
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.samples = []
+        self.proc = None
+        self.t_lo = self.t_hi = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def mark(self, lo, hi):
+        self.t_lo, self.t_hi = lo, hi
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for t, line in self.samples:
+            if self.t_lo is not None and not (self.t_lo <= t <= self.t_hi):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[0]), smax=float(parts[1]), hw=parts[4],
+                                 hwt=parts[5], swt=parts[6], swp=parts[7]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples in timed region"]}
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows),
+                "sm_max_mhz": max(r["smax"] for r in rows), "reasons": sorted(reasons),
+                "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ arms
+
+def cpu_oracle_sample(w, x_cpu, target_s: float, max_heads=None):
+    """Time the fp64 C oracle on a bounded sample of the workload: the first T_s tokens of
+    every (batch, head) (all heads, batch 0..B-1), T_s sized for ~target_s of work."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    q = x_cpu["q"].float().numpy()
+    k = x_cpu["k"].float().numpy()
+    v = x_cpu["v"].float().numpy()
+    g = x_cpu["g"].numpy()
+    h0 = None if x_cpu["h0"] is None else x_cpu["h0"].numpy()
+    cal_T = min(w.T, 256)
+    t0 = time.perf_counter()
+    oracle.recurrent(q[:, :cal_T], k[:, :cal_T], v[:, :cal_T], g[:, :cal_T], x_cpu["scale"], h0)
+    rate = (w.B * cal_T) / max(time.perf_counter() - t0, 1e-6)   # tokens/s (all heads)
+    T_s = int(min(w.T, max(64, (target_s * rate) / w.B)))
+    t0 = time.perf_counter()
+    oracle.recurrent(np.ascontiguousarray(q[:, :T_s]), np.ascontiguousarray(k[:, :T_s]),
+                     np.ascontiguousarray(v[:, :T_s]), np.ascontiguousarray(g[:, :T_s]),
+                     x_cpu["scale"], h0)
+    dt = time.perf_counter() - t0
+    return {"value": (w.B * T_s) / dt, "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"first {T_s} of {w.T} tokens of all {w.B}x{w.H} (batch, head) pairs, "
+                      f"fp64 C recurrence, {dt:.2f} s"}
+
+
+def run_reference(args, w, rank, world):
+    """--impl reference: the fp64 CPU oracle as the reference arm (rank 0 only)."""
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    from chunkwise_recurrent_prefill_gb300.workloads import make_inputs
+    oracle.build()
+    x = make_inputs(w)
+    q = x["q"].float().numpy()
+    k = x["k"].float().numpy()
+    v = x["v"].float().numpy()
+    g = x["g"].numpy()
+    h0 = None if x["h0"] is None else x["h0"].numpy()
+    # size each step so that warmup + steps take ~150 s of CPU time in total
+    cal_T = min(w.T, 128)
+    t0 = time.perf_counter()
+    oracle.recurrent(q[:, :cal_T], k[:, :cal_T], v[:, :cal_T], g[:, :cal_T], x["scale"], h0)
+    rate = (w.B * cal_T) / max(time.perf_counter() - t0, 1e-6)
+    per_step_s = 150.0 / max(1, args.steps + args.warmup)
+    T_s = int(min(w.T, max(1, per_step_s * rate / w.B)))
+    sl = [np.ascontiguousarray(a[:, :T_s]) for a in (q, k, v, g)]
+    for _ in range(args.warmup):
+        oracle.recurrent(*sl, x["scale"], h0)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.recurrent(*sl, x["scale"], h0)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = args.steps * w.B * T_s / total
+    sample = (f"each step: first {T_s} of {w.T} tokens of all {w.B}x{w.H} (batch, head) "
+              f"pairs, fp64 C recurrence on host cores")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(w, "oracle"),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def workload_config(w, path):
+    l2 = ("n/a (host CPU)" if path == "oracle"
+          else "flushed by a 256 MiB device write before every timed step")
+    return {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "Dk": w.Dk, "Dv": w.Dv,
+            "io": w.io, "gate": "fp32 log-gate logsigmoid(u)/16", "path": path,
+            "h0": w.with_h0, "hT": w.want_hT, "l2": l2}
+
+
+def run_ours(args, w, rank, world, dist):
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from chunkwise_recurrent_prefill_gb300 import gla
+    from chunkwise_recurrent_prefill_gb300.workloads import make_inputs
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    x_cpu = make_inputs(w)
+    x = {k_: (v_.to(dev) if hasattr(v_, "to") else v_) for k_, v_ in x_cpu.items()}
+    o = torch.empty((w.B, w.T, w.H, w.Dv), dtype=x["q"].dtype, device=dev)
+    hT = torch.empty((w.B, w.H, w.Dk, w.Dv), dtype=torch.float32, device=dev) \
+        if w.want_hT else None
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        gla.gla_fwd(x["q"], x["k"], x["v"], x["g"], x["scale"], x["h0"], o=o, hT=hT,
+                    path=args.path, seq_splits=args.seq_splits, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert gla.last_device_status() == 0, "device error during warm-up"
+
+    gid = str(torch.cuda.get_device_properties(dev).uuid)
+    sampler = ClockSampler(gid if gid.startswith("GPU-") else "GPU-" + gid)
+    sampler.start()
+    time.sleep(0.3)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = gla.launch_counter()
+    t_lo = time.time()
+    for i in range(args.steps):
+        flush.zero_()
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    t_hi = time.time()
+    if dist:
+        dist.barrier()
+    launches = gla.launch_counter() - launches0
+    time.sleep(0.2)
+    sampler.mark(t_lo, t_hi)
+    sampler.stop()
+    assert gla.last_device_status() == 0, "device error during the timed region"
+    ms = [a.elapsed_time(b) for a, b in evs]
+    total_s = sum(ms) / 1e3
+    if dist:
+        t = torch.tensor([total_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_s = float(t.item())
+    tokens = w.B * w.T
+    value = world * tokens * args.steps / total_s
+    ms_sorted = sorted(ms)
+    per_launch_s = total_s / args.steps
+
+    # roofline of the dominant (only) kernel of the call
+    hbm_gbs, bf16_tflops, peak_src = load_peaks()
+    abytes = algorithmic_bytes(w)
+    aflops = algorithmic_flops(w)
+    achieved = abytes / per_launch_s / 1e9
+    kind = gla.path_for(w.B, w.T, w.H, w.Dk, w.Dv, w.io, args.path)
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                "frac": achieved / hbm_gbs, "traffic": committed_traffic(kind, w.name),
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst)",
+                "algorithmic_bytes_per_launch": abytes,
+                "tensor_frac": (aflops / per_launch_s / 1e12) / bf16_tflops,
+                "kernel": kind}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, w, x_cpu, dev, stream, gla, world, dist)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_oracle_sample(w, x_cpu, args.cpu_seconds)
+
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * per_launch_s,
+            "ms_p50": ms_sorted[len(ms) // 2], "ms_p95": ms_sorted[int(0.95 * (len(ms) - 1))],
+            "ms_p99": ms_sorted[int(0.99 * (len(ms) - 1))],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) q/k/v, logsigmoid(N(0,1))/16 gates)",
+            "config": workload_config(w, kind), "clocks": sampler.summary(),
+            "gpu_launches": launches, "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu,
+        }), flush=True)
+
+
+def run_e2e(args, w, x_cpu, dev, stream, gla, world, dist):
+    """End to end through the public API: pinned host inputs -> device, forward, output
+    (and final state) -> pinned host, all inside the timed events, every step."""
+    import torch
+    steps = max(3, min(args.steps, 50))
+    host = {k_: (v_.pin_memory() if hasattr(v_, "pin_memory") else v_) for k_, v_ in x_cpu.items()}
+    dbuf = {k_: (torch.empty_like(v_, device=dev) if hasattr(v_, "to") else v_)
+            for k_, v_ in x_cpu.items()}
+    o = torch.empty((w.B, w.T, w.H, w.Dv), dtype=x_cpu["q"].dtype, device=dev)
+    hT = torch.empty((w.B, w.H, w.Dk, w.Dv), dtype=torch.float32, device=dev) \
+        if w.want_hT else None
+    o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hT_host = torch.empty(hT.shape, dtype=hT.dtype).pin_memory() if hT is not None else None
+    h2d = sum(t.numel() * t.element_size() for k_, t in host.items()
+              if k_ in ("q", "k", "v", "g", "h0") and t is not None)
+    d2h = o.numel() * o.element_size() + (hT.numel() * 4 if hT is not None else 0)
+
+    def step():
+        for k_ in ("q", "k", "v", "g", "h0"):
+            if host[k_] is not None:
+                dbuf[k_].copy_(host[k_], non_blocking=True)
+        gla.gla_fwd(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["g"], x_cpu["scale"], dbuf["h0"],
+                    o=o, hT=hT, path=args.path, seq_splits=args.seq_splits, stream=stream)
+        o_host.copy_(o, non_blocking=True)
+        if hT is not None:
+            hT_host.copy_(hT, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    total_s = a.elapsed_time(b) / 1e3
+    if dist:
+        t = torch.tensor([total_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_s = float(t.item())
+    return {"value": world * w.B * w.T * steps / total_s, "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+def main():
+    args = parse_args()
+    from chunkwise_recurrent_prefill_gb300.workloads import BENCH_WORKLOAD, WORKLOADS
+    w = WORKLOADS[args.workload or BENCH_WORKLOAD]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, w, rank, world)
+        return
+    import torch
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        local = int(os.environ.get("LOCAL_RANK", "0"))
+        torch.cuda.set_device(local)
+        tdist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        dist = tdist
+    else:
+        torch.cuda.set_device(0)
+    try:
+        run_ours(args, w, rank, world, dist)
+    finally:
+        if dist:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,290 @@
+// C ABI of libgla.so: argument validation, path selection, workspace, status.
+// See include/gla.h for the contract of every entry point.
+#include <atomic>
+#include <mutex>
+#include <stdint.h>
+#include <string.h>
+
+#include "gla.h"
+#include "gla_internal.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// Error word raised by kernels (bounded waits that ran out); one per device.
+__device__ unsigned int g_dev_err;
+
+struct DeviceState {
+    bool probed = false;
+    bool sm103 = false;
+    int num_sms = 0;
+    unsigned int *err_word = nullptr;
+    void *ws = nullptr;
+    size_t ws_bytes = 0;
+};
+
+std::mutex g_mu;
+std::atomic<uint64_t> g_launches{0};
+DeviceState g_dev[kMaxDevices];
+
+// Probe the current device once: architecture, SM count, error word address.
+gla_status current_device(DeviceState **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return GLA_ERR_LAUNCH;
+    }
+    DeviceState &st = g_dev[dev];
+    if (!st.probed) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return GLA_ERR_LAUNCH;
+        }
+        st.sm103 = (major == 10 && minor == 3);
+        st.num_sms = sms;
+        if (st.sm103) {
+            void *p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_dev_err) != cudaSuccess) {
+                cudaGetLastError();
+                return GLA_ERR_LAUNCH;
+            }
+            st.err_word = static_cast<unsigned int *>(p);
+        }
+        st.probed = true;
+    }
+    *out = &st;
+    return st.sm103 ? GLA_OK : GLA_ERR_UNSUPPORTED_DEVICE;
+}
+
+bool misaligned(const void *p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u); }
+
+bool overlap(const void *a, size_t na, const void *b, size_t nb) {
+    if (!a || !b || na == 0 || nb == 0) return false;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+// Multiply non-negative sizes, flagging overflow past 2^62.
+bool mul_ok(int64_t a, int64_t b, int64_t *r) {
+    if (a < 0 || b < 0) return false;
+    if (a != 0 && b > (int64_t(1) << 62) / a) return false;
+    *r = a * b;
+    return true;
+}
+
+struct Sizes {
+    int64_t nqk, nv, nstate;  // element counts
+};
+
+gla_status validate_shape(int64_t B, int64_t T, int64_t H, int64_t Dk, int64_t Dv, int io,
+                          Sizes *sz) {
+    if (io != GLA_IO_BF16 && io != GLA_IO_F32) return GLA_ERR_BAD_OPTION;
+    if (B < 0 || T < 0 || H < 0) return GLA_ERR_BAD_SHAPE;
+    if (Dk <= 0 || Dv <= 0) return GLA_ERR_UNSUPPORTED_DIM;
+    int64_t bth, bh;
+    if (!mul_ok(B, T, &bth) || !mul_ok(bth, H, &bth) || !mul_ok(B, H, &bh))
+        return GLA_ERR_BAD_SHAPE;
+    if (!mul_ok(bth, Dk, &sz->nqk) || !mul_ok(bth, Dv, &sz->nv) ||
+        !mul_ok(bh, Dk * Dv, &sz->nstate) || bh > (int64_t(1) << 31) - 1)
+        return GLA_ERR_BAD_SHAPE;
+    return GLA_OK;
+}
+
+gla_status validate(const void *q, const void *k, const void *v, const float *g,
+                    const float *h0, const void *o, const float *hT, int64_t B, int64_t T,
+                    int64_t H, int64_t Dk, int64_t Dv, int io, Sizes *sz) {
+    gla_status rc = validate_shape(B, T, H, Dk, Dv, io, sz);
+    if (rc != GLA_OK) return rc;
+    const bool empty = (sz->nqk == 0);
+    if (!empty && (!q || !k || !v || !g || !o)) return GLA_ERR_NULL_ARG;
+    if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(g) || misaligned(h0) ||
+        misaligned(o) || misaligned(hT))
+        return GLA_ERR_MISALIGNED;
+    const size_t es = io == GLA_IO_BF16 ? 2 : 4;
+    const size_t bqk = (size_t)sz->nqk * es, bv = (size_t)sz->nv * es;
+    const size_t bg = (size_t)sz->nqk * 4, bs = (size_t)sz->nstate * 4;
+    const void *ins[5] = {q, k, v, g, h0};
+    const size_t nins[5] = {bqk, bqk, bv, bg, bs};
+    for (int i = 0; i < 5; ++i) {
+        if (overlap(o, bv, ins[i], nins[i]) || overlap(hT, bs, ins[i], nins[i]))
+            return GLA_ERR_ALIAS;
+    }
+    if (overlap(o, bv, hT, bs)) return GLA_ERR_ALIAS;
+    return GLA_OK;
+}
+
+// The library-owned workspace of the current device, grown on demand.
+gla_status library_workspace(DeviceState *st, size_t need, void **out) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (st->ws_bytes < need) {
+        if (st->ws) {
+            cudaFree(st->ws);  // synchronises the device: no call still uses the old one
+            st->ws = nullptr;
+            st->ws_bytes = 0;
+        }
+        void *p = nullptr;
+        if (cudaMalloc(&p, need) != cudaSuccess) {
+            cudaGetLastError();
+            return GLA_ERR_WORKSPACE;
+        }
+        st->ws = p;
+        st->ws_bytes = need;
+    }
+    *out = st->ws;
+    return GLA_OK;
+}
+
+int resolve_path(const gla_options *opt, const gla::Problem &p) {
+    const int path = opt ? opt->path : GLA_PATH_AUTO;
+    if (path != GLA_PATH_AUTO) return path;
+    return (p.io == GLA_IO_BF16 && gla::tc_supported(p)) ? GLA_PATH_TC : GLA_PATH_EXACT;
+}
+
+}  // namespace
+
+namespace gla {
+void count_launches(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+}  // namespace gla
+
+extern "C" {
+
+uint64_t gla_launch_counter(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int gla_version(void) { return 100; }
+
+const char *gla_status_string(gla_status s) {
+    switch (s) {
+        case GLA_OK: return "GLA_OK";
+        case GLA_ERR_NULL_ARG: return "GLA_ERR_NULL_ARG";
+        case GLA_ERR_BAD_SHAPE: return "GLA_ERR_BAD_SHAPE";
+        case GLA_ERR_UNSUPPORTED_DIM: return "GLA_ERR_UNSUPPORTED_DIM";
+        case GLA_ERR_MISALIGNED: return "GLA_ERR_MISALIGNED";
+        case GLA_ERR_ALIAS: return "GLA_ERR_ALIAS";
+        case GLA_ERR_LAUNCH: return "GLA_ERR_LAUNCH";
+        case GLA_ERR_DEVICE_TIMEOUT: return "GLA_ERR_DEVICE_TIMEOUT";
+        case GLA_ERR_UNSUPPORTED_DEVICE: return "GLA_ERR_UNSUPPORTED_DEVICE";
+        case GLA_ERR_WORKSPACE: return "GLA_ERR_WORKSPACE";
+        case GLA_ERR_BAD_OPTION: return "GLA_ERR_BAD_OPTION";
+    }
+    return "GLA_ERR_UNKNOWN";
+}
+
+int gla_path_for(int64_t B, int64_t T, int64_t H, int64_t Dk, int64_t Dv, int io,
+                 const gla_options *opt) {
+    Sizes sz;
+    if (validate_shape(B, T, H, Dk, Dv, io, &sz) != GLA_OK) return -1;
+    gla::Problem p{};
+    p.B = B; p.T = T; p.H = H; p.Dk = Dk; p.Dv = Dv; p.io = io;
+    const int path = resolve_path(opt, p);
+    if (path == GLA_PATH_EXACT) return gla::exact_supported(Dk, Dv) ? path : -1;
+    if (path == GLA_PATH_TC) return (io == GLA_IO_BF16 && gla::tc_supported(p)) ? path : -1;
+    return -1;
+}
+
+size_t gla_fwd_workspace_size(int64_t B, int64_t T, int64_t H, int64_t Dk, int64_t Dv, int io,
+                              const gla_options *opt) {
+    Sizes sz;
+    if (validate_shape(B, T, H, Dk, Dv, io, &sz) != GLA_OK) return 0;
+    gla::Problem p{};
+    p.B = B; p.T = T; p.H = H; p.Dk = Dk; p.Dv = Dv; p.io = io;
+    if (resolve_path(opt, p) != GLA_PATH_TC || !gla::tc_supported(p)) return 0;
+    int splits = opt ? opt->seq_splits : 0;
+    if (splits <= 0) {
+        DeviceState *st = nullptr;
+        const int sms = current_device(&st) == GLA_OK ? st->num_sms : 152;
+        splits = gla::tc_auto_splits(p, sms);
+    }
+    return gla::tc_workspace_bytes(p, splits);
+}
+
+gla_status gla_fwd_ex(const void *q, const void *k, const void *v, const float *g_log,
+                      float scale, const float *h0, void *o, float *hT, int64_t B, int64_t T,
+                      int64_t H, int64_t Dk, int64_t Dv, int io, const gla_options *opt,
+                      gla_stream_t stream) {
+    Sizes sz;
+    gla_status rc = validate(q, k, v, g_log, h0, o, hT, B, T, H, Dk, Dv, io, &sz);
+    if (rc != GLA_OK) return rc;
+    gla::Problem p{q, k, v, g_log, scale, h0, o, hT, B, T, H, Dk, Dv, io};
+    const int path = resolve_path(opt, p);
+    if (path != GLA_PATH_EXACT && path != GLA_PATH_TC) return GLA_ERR_BAD_OPTION;
+    if (opt && opt->seq_splits < 0) return GLA_ERR_BAD_OPTION;
+    if (path == GLA_PATH_EXACT && !gla::exact_supported(Dk, Dv)) return GLA_ERR_UNSUPPORTED_DIM;
+    if (path == GLA_PATH_TC && (io != GLA_IO_BF16 || !gla::tc_supported(p)))
+        return GLA_ERR_UNSUPPORTED_DIM;
+    if (opt && opt->workspace && misaligned(opt->workspace)) return GLA_ERR_WORKSPACE;
+
+    DeviceState *st = nullptr;
+    rc = current_device(&st);
+    if (rc != GLA_OK) return rc;
+    if (B * H == 0) return GLA_OK;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (path == GLA_PATH_EXACT) {
+        e = gla::launch_exact(p, st->err_word, s);
+    } else {
+        int splits = (opt && opt->seq_splits > 0) ? opt->seq_splits
+                                                  : gla::tc_auto_splits(p, st->num_sms);
+        const size_t need = gla::tc_workspace_bytes(p, splits);
+        void *ws = nullptr;
+        if (need > 0) {
+            if (opt && opt->workspace) {
+                if (opt->workspace_bytes < need) return GLA_ERR_WORKSPACE;
+                ws = opt->workspace;
+            } else {
+                rc = library_workspace(st, need, &ws);
+                if (rc != GLA_OK) return rc;
+            }
+        }
+        e = gla::launch_tc(p, splits, ws, need, st->err_word, s);
+    }
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return GLA_ERR_LAUNCH;
+    }
+    return GLA_OK;
+}
+
+gla_status gla_fwd(const void *q, const void *k, const void *v, const float *g_log, float scale,
+                   const float *h0, void *o, float *hT, int64_t B, int64_t T, int64_t H,
+                   int64_t Dk, int64_t Dv, gla_stream_t stream) {
+    return gla_fwd_ex(q, k, v, g_log, scale, h0, o, hT, B, T, H, Dk, Dv, GLA_IO_BF16, nullptr,
+                      stream);
+}
+
+gla_status gla_fwd_f32(const float *q, const float *k, const float *v, const float *g_log,
+                       float scale, const float *h0, float *o, float *hT, int64_t B, int64_t T,
+                       int64_t H, int64_t Dk, int64_t Dv, gla_stream_t stream) {
+    return gla_fwd_ex(q, k, v, g_log, scale, h0, o, hT, B, T, H, Dk, Dv, GLA_IO_F32, nullptr,
+                      stream);
+}
+
+gla_status gla_last_device_status(gla_stream_t stream) {
+    DeviceState *st = nullptr;
+    gla_status rc = current_device(&st);
+    if (rc != GLA_OK) return rc;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return GLA_ERR_LAUNCH;
+    }
+    unsigned int word = 0;
+    if (cudaMemcpy(&word, st->err_word, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return GLA_ERR_LAUNCH;
+    }
+    if (word != 0) {
+        const unsigned int zero = 0;
+        if (cudaMemcpy(st->err_word, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) {
+            cudaGetLastError();
+            return GLA_ERR_LAUNCH;
+        }
+        return GLA_ERR_DEVICE_TIMEOUT;
+    }
+    return GLA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,42 @@
+// Host-side declarations shared by the translation units of libgla.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stddef.h>
+
+namespace gla {
+
+// One forward problem, already validated by the C ABI layer.
+struct Problem {
+    const void *q, *k, *v;   // [B,T,H,Dk] / [B,T,H,Dv], bf16 or fp32 (io)
+    const float *g;          // [B,T,H,Dk] log-gates
+    float scale;
+    const float *h0;         // [B,H,Dk,Dv] or nullptr
+    void *o;                 // [B,T,H,Dv]
+    float *hT;               // [B,H,Dk,Dv] or nullptr
+    int64_t B, T, H, Dk, Dv;
+    int io;                  // GLA_IO_BF16 / GLA_IO_F32
+};
+
+// Bits of the device error word kernels may raise (never trap).
+enum : unsigned int {
+    kDevErrTimeout = 1u,     // a bounded mbarrier / flag wait ran out
+    kDevErrInternal = 2u,    // an internal consistency check failed
+};
+
+// Host-side count of kernel launches issued by the library (gla_launch_counter).
+void count_launches(unsigned n);
+
+// Exact fp32 CUDA-core chunkwise kernel (any io, Dk/Dv in {64,128}).
+bool exact_supported(int64_t Dk, int64_t Dv);
+cudaError_t launch_exact(const Problem &p, unsigned int *dev_err, cudaStream_t s);
+
+// tcgen05 path (bf16 io, Dk = Dv = 128).
+bool tc_supported(const Problem &p);
+int tc_auto_splits(const Problem &p, int num_sms);
+size_t tc_workspace_bytes(const Problem &p, int splits);
+cudaError_t launch_tc(const Problem &p, int splits, void *ws, size_t ws_bytes,
+                      unsigned int *dev_err, cudaStream_t s);
+
+}  // namespace gla

@@ -1,0 +1,175 @@
+"""Python binding of libgla.so (argument marshalling only).
+
+Every step of the forward pass runs inside the library's CUDA kernels; this module
+checks tensor dtypes/shapes/devices, allocates outputs with torch (device memory is
+plumbing here) and passes raw pointers and the current CUDA stream to the C ABI
+declared in ``include/gla.h``. There is no CPU or PyTorch fallback: if the library is
+missing or the device is not sm_103, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libgla.so")
+
+GLA_OK = 0
+STATUS = {
+    0: "GLA_OK", 1: "GLA_ERR_NULL_ARG", 2: "GLA_ERR_BAD_SHAPE", 3: "GLA_ERR_UNSUPPORTED_DIM",
+    4: "GLA_ERR_MISALIGNED", 5: "GLA_ERR_ALIAS", 6: "GLA_ERR_LAUNCH",
+    7: "GLA_ERR_DEVICE_TIMEOUT", 8: "GLA_ERR_UNSUPPORTED_DEVICE", 9: "GLA_ERR_WORKSPACE",
+    10: "GLA_ERR_BAD_OPTION",
+}
+PATHS = {"auto": 0, "exact": 1, "tc": 2}
+IO_BF16, IO_F32 = 0, 1
+
+
+class GLAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+
+
+class _Options(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int), ("seq_splits", ctypes.c_int),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libgla.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(path):
+                raise RuntimeError(f"libgla.so is not built ({path}); run __graft_entry__.build()")
+            lib = ctypes.CDLL(path)
+            vp, i64, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float
+            sig = [vp, vp, vp, vp, f32, vp, vp, vp, i64, i64, i64, i64, i64]
+            lib.gla_fwd.argtypes = sig + [vp]
+            lib.gla_fwd_f32.argtypes = sig + [vp]
+            lib.gla_fwd_ex.argtypes = sig + [ctypes.c_int, ctypes.POINTER(_Options), vp]
+            for f in (lib.gla_fwd, lib.gla_fwd_f32, lib.gla_fwd_ex):
+                f.restype = ctypes.c_int
+            lib.gla_fwd_workspace_size.argtypes = [i64, i64, i64, i64, i64, ctypes.c_int,
+                                                   ctypes.POINTER(_Options)]
+            lib.gla_fwd_workspace_size.restype = ctypes.c_size_t
+            lib.gla_last_device_status.argtypes = [vp]
+            lib.gla_last_device_status.restype = ctypes.c_int
+            lib.gla_status_string.argtypes = [ctypes.c_int]
+            lib.gla_status_string.restype = ctypes.c_char_p
+            lib.gla_path_for.argtypes = [i64, i64, i64, i64, i64, ctypes.c_int,
+                                         ctypes.POINTER(_Options)]
+            lib.gla_path_for.restype = ctypes.c_int
+            lib.gla_launch_counter.argtypes = []
+            lib.gla_launch_counter.restype = ctypes.c_uint64
+            lib.gla_version.argtypes = []
+            lib.gla_version.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(t, name, dtype, shape, device):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.device != device:
+        raise ValueError(f"{name}: on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def options(path: str = "auto", seq_splits: int = 0, workspace: torch.Tensor | None = None):
+    opt = _Options()
+    opt.path = PATHS[path]
+    opt.seq_splits = int(seq_splits)
+    opt.workspace = None if workspace is None else workspace.data_ptr()
+    opt.workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return opt
+
+
+def workspace_size(B, T, H, Dk=128, Dv=128, io="bf16", path="auto", seq_splits=0) -> int:
+    opt = options(path, seq_splits)
+    return int(load_library().gla_fwd_workspace_size(B, T, H, Dk, Dv,
+                                                      IO_BF16 if io == "bf16" else IO_F32,
+                                                      ctypes.byref(opt)))
+
+
+def path_for(B, T, H, Dk=128, Dv=128, io="bf16", path="auto") -> str | None:
+    """Name of the path gla_fwd would run ("exact" / "tc"), or None if unsupported."""
+    opt = options(path)
+    r = int(load_library().gla_path_for(B, T, H, Dk, Dv, IO_BF16 if io == "bf16" else IO_F32,
+                                        ctypes.byref(opt)))
+    return {1: "exact", 2: "tc"}.get(r)
+
+
+def gla_fwd(q, k, v, g, scale: float, h0=None, *, o=None, hT=None, return_state: bool = False,
+            path: str = "auto", seq_splits: int = 0, workspace=None, stream=None):
+    """GLA prefill forward through ``gla_fwd_ex``.
+
+    q, k: [B,T,H,Dk]; v: [B,T,H,Dv] (all bf16, or all float32); g: [B,T,H,Dk] float32
+    log-gates; h0: [B,H,Dk,Dv] float32 or None. Outputs o (same dtype as q) and, when
+    ``return_state`` or ``hT`` is given, the float32 final state. Returns (o, hT|None).
+    Asynchronous on ``stream`` (default: torch's current stream).
+    """
+    lib = load_library()
+    if q.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("q/k/v must be bfloat16 or float32")
+    B, T, H, Dk = q.shape
+    Dv = v.shape[-1]
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("tensors must be on a CUDA device")
+    _check(q, "q", q.dtype, (B, T, H, Dk), dev)
+    _check(k, "k", q.dtype, (B, T, H, Dk), dev)
+    _check(v, "v", q.dtype, (B, T, H, Dv), dev)
+    _check(g, "g", torch.float32, (B, T, H, Dk), dev)
+    if h0 is not None:
+        _check(h0, "h0", torch.float32, (B, H, Dk, Dv), dev)
+    if o is None:
+        o = torch.empty((B, T, H, Dv), dtype=q.dtype, device=dev)
+    else:
+        _check(o, "o", q.dtype, (B, T, H, Dv), dev)
+    if hT is None and return_state:
+        hT = torch.empty((B, H, Dk, Dv), dtype=torch.float32, device=dev)
+    elif hT is not None:
+        _check(hT, "hT", torch.float32, (B, H, Dk, Dv), dev)
+    opt = options(path, seq_splits, workspace)
+    io = IO_BF16 if q.dtype == torch.bfloat16 else IO_F32
+    with torch.cuda.device(dev):
+        rc = lib.gla_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(g), ctypes.c_float(scale), _ptr(h0),
+                            _ptr(o), _ptr(hT), B, T, H, Dk, Dv, io, ctypes.byref(opt),
+                            _stream_handle(stream))
+    if rc != GLA_OK:
+        raise GLAError(rc, "gla_fwd_ex")
+    return o, hT
+
+
+def launch_counter() -> int:
+    """Kernel launches the library has issued in this process."""
+    return int(load_library().gla_launch_counter())
+
+
+def last_device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error status."""
+    return int(load_library().gla_last_device_status(_stream_handle(stream)))

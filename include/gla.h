@@ -1,0 +1,143 @@
+/*
+ * gla.h — C ABI of libgla.so, the GB300 (sm_103a) gated-linear-attention prefill forward.
+ *
+ * What every entry point computes, per batch b and head h independently
+ * ("Linear Attention 在 GPU 上到底慢在哪", section 学长的反馈: the state update
+ * h <- h.g + k^T v with a D x D state; "线性注意力GPU算子库的定义与技术解析",
+ * section 四: the state is updated with token t before o[t] is read):
+ *
+ *     S_0 = h0 (zero when h0 == NULL)
+ *     S_t = diag(exp(g_t)) . S_{t-1} + k_t^T v_t          t = 0 .. T-1
+ *     o_t = scale . q_t . S_t
+ *     hT  = S_T                                            (written when hT != NULL)
+ *
+ * g_t is the log-gate (a Dk vector per token and head; expected <= 0, any finite value
+ * is accepted and computed as given). The GPU evaluates this in the chunkwise form of
+ * "线性注意力GPU算子库的定义与技术解析", section 四 (chunks of 64 tokens, in-chunk
+ * cumulative log-gate, decay-masked in-chunk attention, a state scan across chunks,
+ * matrix products for the in-chunk work). The result equals the recurrence up to
+ * floating-point rounding.
+ *
+ * Layouts (all contiguous, row-major, element strides implied by the shape):
+ *     q, k, g_log : [B, T, H, Dk]
+ *     v, o        : [B, T, H, Dv]
+ *     h0, hT      : [B, H, Dk, Dv]   float32
+ * Supported head dims: Dk = Dv = 128 on the tensor-core path; the exact CUDA-core path
+ * also takes Dk, Dv in {64, 128}. Any T >= 0 (a partial last chunk is handled).
+ *
+ * Ownership and memory: every tensor pointer is a DEVICE pointer owned by the caller
+ * and must be 16-byte aligned. o and hT must not overlap any input. The library never
+ * frees caller memory.
+ *
+ * Execution: every call is asynchronous and ordered on `stream` (NULL = the legacy
+ * default stream). No call synchronises the host, except gla_last_device_status().
+ *
+ * Errors: every entry point returns a gla_status and never aborts, traps or throws.
+ * Argument errors are detected on the host before any launch; nothing is written then.
+ */
+#ifndef GLA_H_
+#define GLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same underlying type as cudaStream_t / CUstream, so either may be passed. */
+typedef struct CUstream_st *gla_stream_t;
+
+typedef enum {
+    GLA_OK = 0,
+    GLA_ERR_NULL_ARG = 1,          /* a required pointer is NULL                      */
+    GLA_ERR_BAD_SHAPE = 2,         /* negative or overflowing B, T, H                 */
+    GLA_ERR_UNSUPPORTED_DIM = 3,   /* Dk / Dv not supported by the requested path     */
+    GLA_ERR_MISALIGNED = 4,        /* a pointer is not 16-byte aligned                */
+    GLA_ERR_ALIAS = 5,             /* an output overlaps an input                     */
+    GLA_ERR_LAUNCH = 6,            /* a CUDA call or kernel launch failed             */
+    GLA_ERR_DEVICE_TIMEOUT = 7,    /* a kernel gave up waiting on a pipeline barrier  */
+    GLA_ERR_UNSUPPORTED_DEVICE = 8,/* the current device is not sm_103                */
+    GLA_ERR_WORKSPACE = 9,         /* caller workspace too small or misaligned        */
+    GLA_ERR_BAD_OPTION = 10        /* an option value is out of range                 */
+} gla_status;
+
+/* Which arithmetic path runs. */
+typedef enum {
+    GLA_PATH_AUTO = 0,   /* tensor-core path for bf16 I/O, exact path for fp32 I/O    */
+    GLA_PATH_EXACT = 1,  /* fp32 CUDA-core chunkwise kernel (exact in-chunk decays)   */
+    GLA_PATH_TC = 2      /* tcgen05 / TMEM / TMA kernel, bf16 operands, fp32 state     */
+} gla_path;
+
+typedef enum { GLA_IO_BF16 = 0, GLA_IO_F32 = 1 } gla_io;
+
+typedef struct {
+    int path;               /* gla_path                                                */
+    int seq_splits;         /* tensor-core path: sequence segments per head; 0 = auto  */
+    void *workspace;        /* device scratch owned by the caller; NULL = the library
+                               keeps one per device (allocated on first need, grown
+                               when a larger problem arrives)                          */
+    size_t workspace_bytes; /* size of `workspace` in bytes                            */
+} gla_options;
+
+/*
+ * gla_fwd — bf16 q, k, v, o; fp32 g_log, h0, hT; fp32 state and accumulation.
+ * Arguments: q, k, v, g_log (inputs), scale (output multiplier, typically Dk^-0.5),
+ * h0 (initial state or NULL), o (output), hT (final state or NULL), shape B, T, H, Dk,
+ * Dv, and the stream. Runs the tensor-core path.
+ */
+gla_status gla_fwd(const void *q, const void *k, const void *v, const float *g_log,
+                   float scale, const float *h0, void *o, float *hT,
+                   int64_t B, int64_t T, int64_t H, int64_t Dk, int64_t Dv,
+                   gla_stream_t stream);
+
+/* gla_fwd_f32 — same contract with fp32 q, k, v, o; runs the exact CUDA-core path. */
+gla_status gla_fwd_f32(const float *q, const float *k, const float *v, const float *g_log,
+                       float scale, const float *h0, float *o, float *hT,
+                       int64_t B, int64_t T, int64_t H, int64_t Dk, int64_t Dv,
+                       gla_stream_t stream);
+
+/*
+ * gla_fwd_ex — the general entry: io selects bf16 or fp32 q/k/v/o, opt (may be NULL)
+ * selects the path, the sequence split and the workspace. The tensor-core path needs
+ * bf16 I/O and Dk = Dv = 128.
+ */
+gla_status gla_fwd_ex(const void *q, const void *k, const void *v, const float *g_log,
+                      float scale, const float *h0, void *o, float *hT,
+                      int64_t B, int64_t T, int64_t H, int64_t Dk, int64_t Dv,
+                      int io, const gla_options *opt, gla_stream_t stream);
+
+/* Bytes of device workspace gla_fwd_ex needs for this shape and options (0 if none).
+ * Returns 0 as well for arguments it would reject. */
+size_t gla_fwd_workspace_size(int64_t B, int64_t T, int64_t H, int64_t Dk, int64_t Dv,
+                              int io, const gla_options *opt);
+
+/* The path gla_fwd_ex would run for this shape, io and options: GLA_PATH_EXACT or
+ * GLA_PATH_TC, or -1 when it would reject them. Makes no CUDA call. */
+int gla_path_for(int64_t B, int64_t T, int64_t H, int64_t Dk, int64_t Dv, int io,
+                 const gla_options *opt);
+
+/*
+ * gla_last_device_status — synchronises `stream`, then reads and clears the library's
+ * device error word on the current device. Returns GLA_OK, GLA_ERR_DEVICE_TIMEOUT when
+ * a kernel abandoned a bounded pipeline wait (its outputs are then undefined, the
+ * context stays usable), or GLA_ERR_LAUNCH when the synchronisation itself failed.
+ */
+gla_status gla_last_device_status(gla_stream_t stream);
+
+/* Human-readable name of a status (static storage; never NULL). */
+const char *gla_status_string(gla_status s);
+
+/* Number of kernel launches this library has issued in this process (all devices),
+ * counted on the host at each successful launch. Lets a caller verify how many of
+ * the library's kernels ran inside a timed region. */
+uint64_t gla_launch_counter(void);
+
+/* Library ABI version: major * 10000 + minor * 100 + patch. */
+int gla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GLA_H_ */

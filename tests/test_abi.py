@@ -1,0 +1,98 @@
+"""The C ABI library loads, exports every symbol include/gla.h declares, and rejects bad
+arguments on the host (no GPU needed: validation returns before any CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from chunkwise_recurrent_prefill_gb300 import build_ext
+    from chunkwise_recurrent_prefill_gb300.gla import load_library
+    build_ext.build()
+    return load_library()
+
+
+def _declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(gla_[a-z0-9_]+)\s*\(", src))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _declared_functions()
+    assert {"gla_fwd", "gla_fwd_f32", "gla_fwd_ex", "gla_last_device_status"} <= declared
+    for name in declared:
+        assert hasattr(lib, name), f"libgla.so does not export {name}"
+
+
+def test_version_and_status_strings(lib):
+    assert lib.gla_version() >= 100
+    for code, name in [(0, b"GLA_OK"), (3, b"GLA_ERR_UNSUPPORTED_DIM"), (7, b"GLA_ERR_DEVICE_TIMEOUT")]:
+        assert lib.gla_status_string(code) == name
+    assert lib.gla_status_string(999) == b"GLA_ERR_UNKNOWN"
+
+
+def _call(lib, q=0x10000, k=0x20000, v=0x30000, g=0x40000, h0=None, o=0x50000, hT=None,
+          B=1, T=64, H=2, Dk=128, Dv=128, io=0, opt=None):
+    from chunkwise_recurrent_prefill_gb300.gla import _Options
+    p = lambda x: None if x is None else ctypes.c_void_p(x)  # noqa: E731
+    opt_p = ctypes.byref(opt) if opt is not None else ctypes.POINTER(_Options)()
+    return lib.gla_fwd_ex(p(q), p(k), p(v), p(g), ctypes.c_float(1.0), p(h0), p(o), p(hT),
+                          B, T, H, Dk, Dv, io, opt_p, None)
+
+
+# fake device addresses far apart so that no range overlaps unless a test wants it
+A = dict(q=0x1000000000, k=0x2000000000, v=0x3000000000, g=0x4000000000, o=0x5000000000)
+
+
+def test_null_pointer(lib):
+    assert _call(lib, **{**A, "q": None}) == 1
+    assert _call(lib, **{**A, "o": None}) == 1
+
+
+def test_bad_shape(lib):
+    assert _call(lib, **A, B=-1) == 2
+    assert _call(lib, **A, T=-5) == 2
+    assert _call(lib, **A, B=1 << 40, T=1 << 40) == 2
+
+
+def test_misaligned(lib):
+    assert _call(lib, **{**A, "k": A["k"] + 2}) == 4
+    assert _call(lib, **A, hT=0x6000000008) == 4
+
+
+def test_alias(lib):
+    assert _call(lib, **{**A, "o": A["q"] + 64}) == 5          # o overlaps q
+    assert _call(lib, **A, h0=0x6000000000, hT=0x6000000000) == 5
+    assert _call(lib, **A, hT=A["o"] + 1024) == 5              # hT inside o
+
+
+def test_bad_io_and_options(lib):
+    from chunkwise_recurrent_prefill_gb300.gla import options
+    assert _call(lib, **A, io=7) == 10
+    assert _call(lib, **A, opt=options("auto", -3)) == 10
+
+
+def test_unsupported_dims(lib):
+    from chunkwise_recurrent_prefill_gb300.gla import options
+    assert _call(lib, **A, Dk=96, opt=options("exact")) == 3
+    assert _call(lib, **A, Dk=0) == 3
+    assert _call(lib, **A, io=1, opt=options("tc")) == 3       # tensor cores need bf16 I/O
+    assert _call(lib, **A, Dk=64, Dv=64, opt=options("tc")) == 3
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    from chunkwise_recurrent_prefill_gb300 import gla_fwd
+    x = torch.zeros(1, 4, 1, 128)
+    with pytest.raises(ValueError):
+        gla_fwd(x, x, x, x, 1.0)
