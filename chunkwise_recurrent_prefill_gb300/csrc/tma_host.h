@@ -1,0 +1,48 @@
+// Host-side construction of TMA tensor maps (driver entry point fetched through the
+// runtime, so the library does not link libcuda directly).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gla {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+inline EncodeTiledFn encode_tiled_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        else
+            cudaGetLastError();
+    }
+    return fn;
+}
+
+// Map of a [B, T, H, D] tensor (D innermost) with a box of (box_d, 1, box_t, 1).
+// Out-of-range rows (t >= T) read as zero.
+inline bool make_bthd_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt,
+                          uint32_t elem_bytes, int64_t B, int64_t T, int64_t H, int64_t D,
+                          uint32_t box_d, uint32_t box_t, CUtensorMapSwizzle swz) {
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn) return false;
+    cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
+    cuuint64_t strides[3] = {(cuuint64_t)(D * elem_bytes), (cuuint64_t)(H * D * elem_bytes),
+                             (cuuint64_t)(T * H * D * elem_bytes)};
+    cuuint32_t box[4] = {box_d, 1, box_t, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(m, dt, 4, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace gla

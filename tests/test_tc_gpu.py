@@ -1,0 +1,151 @@
+"""GPU parity of the tensor-core path (tcgen05/TMEM/TMA) against the fp64 oracle.
+
+bf16 tolerances: max|d| <= 1.5e-2 max|ref|, sum|d| / sum|ref| <= 5e-3, for o and hT.
+"""
+import numpy as np
+import pytest
+import torch
+
+from parity import assert_close
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _run(x, path="tc", seq_splits=0):
+    from chunkwise_recurrent_prefill_gb300 import gla_fwd, last_device_status
+    o, hT = gla_fwd(x["q"], x["k"], x["v"], x["g"], x["scale"], x["h0"], return_state=True,
+                    path=path, seq_splits=seq_splits)
+    torch.cuda.synchronize()
+    assert last_device_status() == 0
+    return o, hT
+
+
+def _oracle(x):
+    import oracle
+    cpu = lambda t: None if t is None else t.cpu()  # noqa: E731
+    return oracle.recurrent(cpu(x["q"]), cpu(x["k"]), cpu(x["v"]), cpu(x["g"]), x["scale"],
+                            cpu(x["h0"]))
+
+
+def _inputs(B, T, H, seed=0, with_h0=True):
+    from chunkwise_recurrent_prefill_gb300.workloads import make_inputs, small
+    return make_inputs(small("tc", B=B, T=T, H=H, io="bf16", seed=seed, with_h0=with_h0), DEV)
+
+
+def _check(x, seq_splits=0):
+    o, hT = _run(x, seq_splits=seq_splits)
+    o_ref, h_ref = _oracle(x)
+    a = assert_close(o.float().cpu().numpy(), o_ref, "bf16", f"o(splits={seq_splits})")
+    b = assert_close(hT.cpu().numpy(), h_ref, "bf16", f"hT(splits={seq_splits})")
+    return a, b
+
+
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 200, 512, 1000])
+@pytest.mark.parametrize("splits", [1, 2, 3, 7])
+def test_tc_small_ragged(T, splits):
+    _check(_inputs(B=2, T=T, H=2, seed=T + splits), seq_splits=splits)
+
+
+def test_tc_no_h0():
+    _check(_inputs(B=1, T=333, H=3, seed=8, with_h0=False), seq_splits=2)
+
+
+def test_tc_split_invariance():
+    """Different sequence splits give the same numbers up to bf16 operand rounding."""
+    x = _inputs(B=1, T=2048, H=4, seed=21)
+    o1, h1 = _run(x, seq_splits=1)
+    for s in (2, 5, 16):
+        o2, h2 = _run(x, seq_splits=s)
+        d = (o1.float() - o2.float()).abs().max().item() / o1.float().abs().max().item()
+        assert d < 1e-2, (s, d)
+        dh = (h1 - h2).abs().max().item() / h1.abs().max().item()
+        assert dh < 1e-2, (s, dh)
+
+
+@pytest.mark.parametrize("name", ["bf16_B1_H16_T4096", "bf16_B1_H16_T16384",
+                                  "bf16_B4_H16_T16384", "bf16_B16_H16_T4096",
+                                  "bf16_B1_H16_T131072_h0"])
+def test_tc_parity_workload(name):
+    """Every output of the full-size parity workloads, element by element, in the launch
+    configuration the bench times (automatic sequence split)."""
+    from chunkwise_recurrent_prefill_gb300.workloads import WORKLOADS, make_inputs
+    w = WORKLOADS[name]
+    x = make_inputs(w, DEV)
+    o, hT = _run(x)
+    o_ref, h_ref = _oracle(x)
+    assert_close(o.float().cpu().numpy(), o_ref, "bf16", f"{name} o")
+    assert_close(hT.cpu().numpy(), h_ref, "bf16", f"{name} hT")
+
+
+def _extreme(x, kind):
+    g = x["g"]
+    if kind == "forget":
+        x["g"] = torch.full_like(g, -1e4)
+    elif kind == "no_decay":
+        x["g"] = torch.zeros_like(g)
+    elif kind == "tiny":
+        x["g"] = -1e-8 * torch.ones_like(g)
+    elif kind == "strong":
+        x["g"] = -5.0 * torch.rand_like(g)
+    elif kind == "mixed":
+        x["g"] = torch.where(torch.rand_like(g) < 0.02, torch.full_like(g, -200.0), g)
+    elif kind == "one_chunk_extreme":
+        g[:, 64:128] = -3.0
+        x["g"] = g
+    elif kind == "big_values":
+        for key in ("q", "k", "v"):
+            x[key] = (x[key].float() * 30).to(x[key].dtype)
+    return x
+
+
+@pytest.mark.parametrize("kind", ["forget", "no_decay", "tiny", "strong", "mixed",
+                                  "one_chunk_extreme", "big_values"])
+def test_tc_extreme_gates(kind):
+    x = _extreme(_inputs(B=1, T=300, H=2, seed=3), kind)
+    o, hT = _run(x, seq_splits=2)
+    assert torch.isfinite(o.float()).all() and torch.isfinite(hT).all()
+    o_ref, h_ref = _oracle(x)
+    assert_close(o.float().cpu().numpy(), o_ref, "bf16", f"o[{kind}]")
+    assert_close(hT.cpu().numpy(), h_ref, "bf16", f"hT[{kind}]")
+
+
+def test_tc_nan_propagates():
+    x = _inputs(B=1, T=200, H=1, seed=1, with_h0=False)
+    x["v"][0, 150, 0, 5] = float("nan")
+    o, hT = _run(x, seq_splits=1)
+    o = o.float().cpu()
+    assert torch.isfinite(o[0, :150]).all()
+    assert torch.isnan(o[0, 150:, 0, 5]).all()
+    assert torch.isnan(hT.cpu()[0, 0, :, 5]).all()
+
+
+def test_tc_caller_workspace_and_too_small():
+    from chunkwise_recurrent_prefill_gb300 import GLAError, gla_fwd, workspace_size
+    x = _inputs(B=1, T=1024, H=2, seed=4)
+    need = workspace_size(1, 1024, 2, path="tc", seq_splits=4)
+    assert need > 0
+    ws = torch.empty(need, dtype=torch.uint8, device=DEV)
+    o, hT = gla_fwd(x["q"], x["k"], x["v"], x["g"], x["scale"], x["h0"], return_state=True,
+                    path="tc", seq_splits=4, workspace=ws)
+    torch.cuda.synchronize()
+    o_ref, h_ref = _oracle(x)
+    assert_close(o.float().cpu().numpy(), o_ref, "bf16", "o(ws)")
+    small = torch.empty(need - 16, dtype=torch.uint8, device=DEV)
+    with pytest.raises(GLAError) as e:
+        gla_fwd(x["q"], x["k"], x["v"], x["g"], x["scale"], x["h0"], path="tc", seq_splits=4,
+                workspace=small)
+    assert e.value.status == 9
+
+
+def test_tc_default_path_is_tensor_cores():
+    from chunkwise_recurrent_prefill_gb300.gla import path_for
+    assert path_for(1, 16384, 16) == "tc"
+    assert path_for(1, 512, 2, io="f32") == "exact"
