@@ -55,6 +55,25 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// Per-role timeline tracing, compiled in only with -DGLA_TRACE: clock64() stamps of the
+// first kTraceCtas CTAs into a device buffer [cta][event][chunk] set by the tracer.
+#ifdef GLA_TRACE
+constexpr int kTraceCtas = 4, kTraceEvents = 24, kTraceChunks = 256;
+__device__ long long *g_trace_out;
+__device__ long long *g_trace_state;
+#define GLA_TRACE_AT(buf, ev, lc)                                                              \
+    do {                                                                                       \
+        if ((buf) && blockIdx.x < kTraceCtas && (lc) < kTraceChunks)                           \
+            (buf)[((size_t)blockIdx.x * kTraceEvents + (ev)) * kTraceChunks + (lc)] = clock64(); \
+    } while (0)
+#else
+#define GLA_TRACE_AT(buf, ev, lc) \
+    do {                          \
+    } while (0)
+#endif
+#define TRACE_OUT(ev, lc) GLA_TRACE_AT(g_trace_out, ev, lc)
+#define TRACE_ST(ev, lc) GLA_TRACE_AT(g_trace_state, ev, lc)
+
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
     return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
@@ -165,6 +184,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     tc_fence_after();
     const uint32_t tm = *tslot;
     bool ok = true;
+    if (threadIdx.x == 0) TRACE_OUT(14, 0);
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -176,6 +196,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 if (lc >= 2 && !mbar_wait(&bars[EMPTY + st], (u - 1) & 1)) { ok = false; break; }
                 uint8_t *base = sm + st * om::STAGE;
                 uint64_t *fb = &bars[FULL + st];
+                TRACE_OUT(0, lc);
                 mbar_arrive_expect_tx(fb, 3 * 16384 + 32768);
                 const int t = (cb + lc) * kC;
                 tma_load_4d(base + om::Q, &tq, fb, 0, h, t, bidx);
@@ -204,6 +225,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 const uint32_t u = lc >> 1;
                 if (!mbar_wait(&bars[GDONE + st], u & 1)) { ok = false; break; }
                 if (lc >= 2 && !mbar_wait(&bars[PFREE + st], (u - 1) & 1)) { ok = false; break; }
+                TRACE_OUT(3, lc);
                 tc_fence_after();
                 const uint32_t base = smem_u32(sm + st * om::STAGE);
                 // P = Q~ K~^T  (64 x 64, K = 128)
@@ -214,8 +236,10 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                            smem_desc(base + om::K + off, 16, 1024), idP, kk > 0);
                 }
                 mma_commit(&bars[PFULL + st]);
+                TRACE_OUT(4, lc);
                 // S^T += V^T K^   (128 x 128, K = 64 tokens)
                 if (!mbar_wait(&bars[SREADY], lc & 1)) { ok = false; break; }
+                TRACE_OUT(5, lc);
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
@@ -225,6 +249,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 // O^T = V^T P^T + S^T Q~^T   (128 x 64)
                 if (!mbar_wait(&bars[PBF + st], u & 1)) { ok = false; break; }
                 if (lc >= 2 && !mbar_wait(&bars[OFREE + st], (u - 1) & 1)) { ok = false; break; }
+                TRACE_OUT(6, lc);
                 tc_fence_after();
                 const uint32_t pbase = smem_u32(sm + om::P + st * 8192);
 #pragma unroll
@@ -238,6 +263,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                            idOs, 1);
                 mma_commit(&bars[OFULL + st]);
                 mma_commit(&bars[EMPTY + st]);
+                TRACE_OUT(7, lc);
             }
             // all issued MMAs complete before the CTA tears down its TMEM
             mma_commit(&bars[FIN]);
@@ -256,6 +282,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 const uint32_t u = lc >> 1;
                 bool w = mbar_wait(&bars[GDONE + st], u & 1) && mbar_wait(&bars[PFULL + st], u & 1);
                 if (named_bar_or(2, 128, !w)) { ok = false; break; }
+                if (et == 0) TRACE_OUT(10, lc);
                 tc_fence_after();
                 const bool extreme = xf[st] != 0;
                 float prow[64];
@@ -320,6 +347,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[PBF + st]);
+                if (et == 0) TRACE_OUT(11, lc);
             }
             if (lc >= 1) {
                 const int pc = lc - 1;
@@ -327,6 +355,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 const uint32_t u = pc >> 1;
                 const bool w = mbar_wait(&bars[OFULL + st], u & 1);
                 if (named_bar_or(2, 128, !w)) { ok = false; break; }
+                if (et == 0) TRACE_OUT(12, pc);
                 tc_fence_after();
                 float ov[64];
 #pragma unroll
@@ -347,6 +376,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
 #pragma unroll
                 for (int x = 0; x < 64; ++x)
                     if (t0 + x < a.T) op[x * rs] = __float2bfloat16_rn(a.scale * ov[x]);
+                if (et == 0) TRACE_OUT(13, pc);
             }
         }
         __syncwarp();
@@ -373,6 +403,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             const uint32_t u = lc >> 1;
             if (lc >= 1 && !mbar_wait(&bars[UDONE], (lc - 1) & 1)) { ok = false; break; }
             if (!mbar_wait(&bars[GDONE + st], u & 1)) { ok = false; break; }
+            if (v == 0) TRACE_OUT(8, lc);
             tc_fence_after();
             const float *gam = gam_s + st * 128;
 #pragma unroll 1
@@ -395,6 +426,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[SREADY]);
+            if (v == 0) TRACE_OUT(9, lc);
         }
         if (ok && a.hT && seg == a.splits - 1) {
             if (!mbar_wait(&bars[UDONE], (n - 1) & 1)) {
@@ -427,6 +459,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             const uint32_t u = lc >> 1;
             const bool w = mbar_wait(&bars[FULL + st], u & 1);
             if (named_bar_or(1, 256, !w)) { ok = false; break; }
+            if (gt == 0) TRACE_OUT(1, lc);
             uint8_t *base = sm + st * om::STAGE;
             const float *gs = reinterpret_cast<const float *>(base + om::G);
             float b0[16], b1[16];
@@ -489,6 +522,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[GDONE + st]);
+            if (gt == 0) TRACE_OUT(2, lc);
         }
         __syncwarp();
     }
@@ -496,6 +530,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     if (!ok) atomicOr(a.err, kDevErrTimeout);
     tc_fence_before();
     __syncthreads();
+    if (threadIdx.x == 0) TRACE_OUT(15, 0);
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tm, 512);
@@ -562,6 +597,7 @@ gla_tc_state_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
                 if (lc >= 2 && !mbar_wait(&bars[SEMPTY + st], (u - 1) & 1)) { ok = false; break; }
                 uint8_t *base = sm + st * sm_::STAGE;
                 uint64_t *fb = &bars[SFULL + st];
+                TRACE_ST(0, lc);
                 mbar_arrive_expect_tx(fb, 2 * 16384 + 32768);
                 const int t = (ce - 1 - lc) * kC;      // last chunk first
                 tma_load_4d(base + sm_::K, &tk, fb, 0, h, t, bidx);
@@ -590,6 +626,7 @@ gla_tc_state_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
                            smem_desc(base + sm_::KH + kk * 2048, 8192, 1024), idU,
                            (lc > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(&bars[SEMPTY + st]);
+                TRACE_ST(3, lc);
             }
             mma_commit(&bars[SEDONE]);
             if (!mbar_wait(&bars[SEDONE], 0)) ok = false;
@@ -608,6 +645,7 @@ gla_tc_state_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
             const uint32_t u = lc >> 1;
             const bool w = mbar_wait(&bars[SFULL + st], u & 1);
             if (named_bar_or(1, 256, !w)) { ok = false; break; }
+            if (gt == 0) TRACE_ST(1, lc);
             uint8_t *base = sm + st * sm_::STAGE;
             const float *gs = reinterpret_cast<const float *>(base + sm_::G);
             float b0[16], b1[16];
@@ -650,6 +688,7 @@ gla_tc_state_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[SGDONE + st]);
+            if (gt == 0) TRACE_ST(2, lc);
         }
         if (ok && qq == 0) {
             float *gp = a.gam + ((size_t)bh * (a.splits - 1) + seg) * kD;
