@@ -84,12 +84,16 @@ constexpr uint32_t kColSB = 128;   // S^T bf16 (A operand), 2 x 64 columns
 constexpr uint32_t kColP = 256;    // P fp32 (M=64 layout), 2 x 64 columns
 constexpr uint32_t kColO = 384;    // O^T fp32, 2 x 64 columns
 
-// Shared-memory map of the output kernel (bytes from a 1024-aligned base).
+// Shared-memory map of the output kernel (bytes from a 1024-aligned base). A stage holds
+// the raw q, k, v tiles (128B-swizzled [64 x 64] bf16 boxes, two per tile) and the fp32
+// log-gate rows; the gate warps rewrite q -> Q~ and k -> K~ in place and write K^ over
+// the first half of the gate rows once every gate row has been read.
 namespace om {
-constexpr uint32_t Q = 0, K = 16384, V = 32768, G = 49152, KH = 81920, STAGE = 98304;
+constexpr uint32_t Q = 0, K = 16384, V = 32768, G = 49152, KH = G, STAGE = 81920;
 constexpr uint32_t P = 2 * STAGE;      // 2 x [64 x 64] bf16 P tiles (128B swizzle)
-constexpr uint32_t GAM = P + 16384;    // [2][128] f32 exp(Bc)
-constexpr uint32_t BV = GAM + 1024;    // [2][128] f32 Bc
+constexpr uint32_t OST = P + 16384;    // [64 x 128] bf16 output staging (two boxes)
+constexpr uint32_t GAM = OST + 16384;  // [2][128] f32 exp(Bc)
+constexpr uint32_t BV = GAM + 1024;    // [2][128] f32 Bc (log2 units)
 constexpr uint32_t XCH = BV + 1024;    // [4][128] f32 token-quarter totals
 constexpr uint32_t XF = XCH + 2048;    // [2] u32 "extreme chunk" flags
 constexpr uint32_t SCR = XF + 64;      // [4][64] f32 exact-path scratch
@@ -111,7 +115,6 @@ constexpr int kStateThreads = 320;     // 10 warps
 struct OutArgs {
     const __nv_bfloat16 *q, *k;        // raw inputs (exact route of extreme chunks)
     const float *g;
-    __nv_bfloat16 *o;
     const float *h0;                   // [B,H,Dk,Dv] or null
     float *hT;                         // [B,H,Dk,Dv] or null
     const float *sstart;               // [BH][splits-1][Dk][Dv] start states of segments 1..
@@ -134,11 +137,61 @@ __device__ __forceinline__ void seg_range(int seg, int nchunks, int splits, int 
     ce = (int)((int64_t)(seg + 1) * nchunks / splits);
 }
 
+// Load 64 consecutive TMEM columns of this warp's lane quarter (one wait).
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&out)[64]) {
+    uint32_t r0[16], r1[16], r2[16], r3[16];
+    tmem_ld16(taddr, r0);
+    tmem_ld16(taddr + 16, r1);
+    tmem_ld16(taddr + 32, r2);
+    tmem_ld16(taddr + 48, r3);
+    tmem_wait_ld();
+    reg_fence(r0);
+    reg_fence(r1);
+    reg_fence(r2);
+    reg_fence(r3);
+#pragma unroll
+    for (int x = 0; x < 16; ++x) {
+        out[x] = __uint_as_float(r0[x]);
+        out[16 + x] = __uint_as_float(r1[x]);
+        out[32 + x] = __uint_as_float(r2[x]);
+        out[48 + x] = __uint_as_float(r3[x]);
+    }
+}
+
+// In-chunk cumulative log-gate of one thread's column pair over 16 tokens, in log2 units,
+// shared with the other token quarters through `xch` (named barrier `bar`, 256 threads).
+// On return b0/b1 hold the chunk-inclusive cumulative log2-gates of the thread's tokens.
+__device__ __forceinline__ void gate_cumsum(const float *gs, float *xch, int qq, int d,
+                                            float (&b0)[16], float (&b1)[16], uint32_t bar) {
+    float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+    for (int x = 0; x < 16; ++x) {
+        const float2 gv = *reinterpret_cast<const float2 *>(gs + (16 * qq + x) * kD + d);
+        a0 = fmaf(gv.x, kLog2e, a0);
+        a1 = fmaf(gv.y, kLog2e, a1);
+        b0[x] = a0;
+        b1[x] = a1;
+    }
+    *reinterpret_cast<float2 *>(xch + qq * kD + d) = make_float2(a0, a1);
+    named_bar_sync(bar, 256);
+    float o0 = 0.f, o1 = 0.f;
+    for (int q2 = 0; q2 < qq; ++q2) {
+        const float2 t = *reinterpret_cast<const float2 *>(xch + q2 * kD + d);
+        o0 += t.x;
+        o1 += t.y;
+    }
+#pragma unroll
+    for (int x = 0; x < 16; ++x) {
+        b0[x] += o0;
+        b1[x] += o1;
+    }
+}
+
 // ======================================================================= output kernel
-__global__ void __launch_bounds__(kOutThreads, 1)
+__global__ void __maxnreg__(112)
 gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg,
-                  const OutArgs a) {
+                  const __grid_constant__ CUtensorMap to, const OutArgs a) {
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = align1024(smraw);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + om::BAR);
@@ -177,6 +230,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         tma_prefetch_desc(&tk);
         tma_prefetch_desc(&tv);
         tma_prefetch_desc(&tg);
+        tma_prefetch_desc(&to);
     }
     if (warp == 1) tmem_alloc(tslot, 512);
     tc_fence_before();
@@ -199,13 +253,13 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 TRACE_OUT(0, lc);
                 mbar_arrive_expect_tx(fb, 3 * 16384 + 32768);
                 const int t = (cb + lc) * kC;
+                tma_load_4d(base + om::G, &tg, fb, 0, h, t, bidx);
                 tma_load_4d(base + om::Q, &tq, fb, 0, h, t, bidx);
                 tma_load_4d(base + om::Q + 8192, &tq, fb, 64, h, t, bidx);
                 tma_load_4d(base + om::K, &tk, fb, 0, h, t, bidx);
                 tma_load_4d(base + om::K + 8192, &tk, fb, 64, h, t, bidx);
                 tma_load_4d(base + om::V, &tv, fb, 0, h, t, bidx);
                 tma_load_4d(base + om::V + 8192, &tv, fb, 64, h, t, bidx);
-                tma_load_4d(base + om::G, &tg, fb, 0, h, t, bidx);
                 ++issued[st];
             }
             // never leave with a bulk copy still landing in this CTA's shared memory
@@ -215,20 +269,20 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        // order per chunk c: U(c) [needs S_c ready], P(c+1) [needs gates of c+1], O(c)
         if (lane == 0) {
             const uint32_t idP = idesc_bf16(64, 64, 0, 0);
             const uint32_t idU = idesc_bf16(128, 128, 1, 1);
             const uint32_t idOi = idesc_bf16(128, 64, 1, 0);
             const uint32_t idOs = idesc_bf16(128, 64, 0, 0);
-            for (int lc = 0; lc < n; ++lc) {
+            auto issue_p = [&](int lc) -> bool {
                 const int st = lc & 1;
                 const uint32_t u = lc >> 1;
-                if (!mbar_wait(&bars[GDONE + st], u & 1)) { ok = false; break; }
-                if (lc >= 2 && !mbar_wait(&bars[PFREE + st], (u - 1) & 1)) { ok = false; break; }
+                if (!mbar_wait(&bars[GDONE + st], u & 1)) return false;
+                if (lc >= 2 && !mbar_wait(&bars[PFREE + st], (u - 1) & 1)) return false;
                 TRACE_OUT(3, lc);
                 tc_fence_after();
                 const uint32_t base = smem_u32(sm + st * om::STAGE);
-                // P = Q~ K~^T  (64 x 64, K = 128)
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
@@ -237,6 +291,13 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 }
                 mma_commit(&bars[PFULL + st]);
                 TRACE_OUT(4, lc);
+                return true;
+            };
+            if (n > 0 && !issue_p(0)) ok = false;
+            for (int lc = 0; lc < n && ok; ++lc) {
+                const int st = lc & 1;
+                const uint32_t u = lc >> 1;
+                const uint32_t base = smem_u32(sm + st * om::STAGE);
                 // S^T += V^T K^   (128 x 128, K = 64 tokens)
                 if (!mbar_wait(&bars[SREADY], lc & 1)) { ok = false; break; }
                 TRACE_OUT(5, lc);
@@ -246,6 +307,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     mma_ss(tm + kColS, smem_desc(base + om::V + kk * 2048, 8192, 1024),
                            smem_desc(base + om::KH + kk * 2048, 8192, 1024), idU, 1);
                 mma_commit(&bars[UDONE]);
+                if (lc + 1 < n && !issue_p(lc + 1)) { ok = false; break; }
                 // O^T = V^T P^T + S^T Q~^T   (128 x 64)
                 if (!mbar_wait(&bars[PBF + st], u & 1)) { ok = false; break; }
                 if (lc >= 2 && !mbar_wait(&bars[OFREE + st], (u - 1) & 1)) { ok = false; break; }
@@ -276,6 +338,8 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         const int et = (warp - 4) * 32 + lane;      // 0..127
         const int v = j * 32 + lane;                // O^T lane = value column
         float *scr = reinterpret_cast<float *>(sm + om::SCR);
+        uint8_t *ost = sm + om::OST + (v >> 6) * 8192;
+        const uint32_t vcol = (uint32_t)(v & 63);
         for (int lc = 0; lc <= n && ok; ++lc) {
             if (lc < n) {
                 const int st = lc & 1;
@@ -288,15 +352,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 float prow[64];
                 const int i = 16 * j + lane;        // P row held by this lane (lane < 16)
                 if (!extreme) {
-#pragma unroll
-                    for (int c0 = 0; c0 < 64; c0 += 16) {
-                        uint32_t r[16];
-                        tmem_ld16(tmem_addr(tm, j, kColP + st * 64 + c0), r);
-                        tmem_wait_ld();
-                        reg_fence(r);
-#pragma unroll
-                        for (int x = 0; x < 16; ++x) prow[c0 + x] = __uint_as_float(r[x]);
-                    }
+                    tmem_ld64(tmem_addr(tm, j, kColP + st * 64), prow);
                 } else {
                     // exact route: P_ij = sum_d q_id k_jd exp(b_id - b_jd), j <= i
 #pragma unroll
@@ -358,27 +414,29 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 if (et == 0) TRACE_OUT(12, pc);
                 tc_fence_after();
                 float ov[64];
-#pragma unroll
-                for (int c0 = 0; c0 < 64; c0 += 16) {
-                    uint32_t r[16];
-                    tmem_ld16(tmem_addr(tm, j, kColO + st * 64 + c0), r);
-                    tmem_wait_ld();
-                    reg_fence(r);
-#pragma unroll
-                    for (int x = 0; x < 16; ++x) ov[c0 + x] = __uint_as_float(r[x]);
-                }
+                tmem_ld64(tmem_addr(tm, j, kColO + st * 64), ov);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[OFREE + st]);
-                const int64_t t0 = (int64_t)(cb + pc) * kC;
-                __nv_bfloat16 *op = a.o + (((int64_t)bidx * a.T + t0) * a.H + h) * kD + v;
-                const int64_t rs = (int64_t)a.H * kD;
+                // stage O (bf16, 128B-swizzled boxes) and write it with two bulk tensor stores
+                if (et == 0) bulk_wait_read_all();
+                named_bar_sync(2, 128);
 #pragma unroll
                 for (int x = 0; x < 64; ++x)
-                    if (t0 + x < a.T) op[x * rs] = __float2bfloat16_rn(a.scale * ov[x]);
-                if (et == 0) TRACE_OUT(13, pc);
+                    *reinterpret_cast<__nv_bfloat16 *>(ost + sw128_offset(x, vcol)) =
+                        __float2bfloat16_rn(a.scale * ov[x]);
+                fence_proxy_async_smem();
+                named_bar_sync(2, 128);
+                if (et == 0) {
+                    const int t0 = (cb + pc) * kC;
+                    tma_store_4d(&to, sm + om::OST, 0, h, t0, bidx);
+                    tma_store_4d(&to, sm + om::OST + 8192, 64, h, t0, bidx);
+                    bulk_commit();
+                    TRACE_OUT(13, pc);
+                }
             }
         }
+        if (et == 0) bulk_wait_all();
         __syncwarp();
     } else if (warp >= 8 && warp < 12) {
         // ------------------------------------------------------------ state scan (TMEM)
@@ -407,20 +465,22 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             tc_fence_after();
             const float *gam = gam_s + st * 128;
 #pragma unroll 1
-            for (int d0 = 0; d0 < kD; d0 += 16) {
-                uint32_t r[16];
-                tmem_ld16(tmem_addr(tm, j, kColS + d0), r);
-                tmem_wait_ld();
-                reg_fence(r);
-                uint32_t pk[8];
+            for (int half = 0; half < 2; ++half) {
+                float sv[64];
+                tmem_ld64(tmem_addr(tm, j, kColS + half * 64), sv);
 #pragma unroll
-                for (int x = 0; x < 8; ++x)
-                    pk[x] = pack_bf16(__uint_as_float(r[2 * x]), __uint_as_float(r[2 * x + 1]));
-                tmem_st8(tmem_addr(tm, j, kColSB + st * 64 + d0 / 2), pk);
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t pk[8];
 #pragma unroll
-                for (int x = 0; x < 16; ++x)
-                    r[x] = __float_as_uint(__uint_as_float(r[x]) * gam[d0 + x]);
-                tmem_st16(tmem_addr(tm, j, kColS + d0), r);
+                    for (int x = 0; x < 8; ++x)
+                        pk[x] = pack_bf16(sv[16 * c + 2 * x], sv[16 * c + 2 * x + 1]);
+                    tmem_st8(tmem_addr(tm, j, kColSB + st * 64 + half * 32 + c * 8), pk);
+                    uint32_t r[16];
+#pragma unroll
+                    for (int x = 0; x < 16; ++x)
+                        r[x] = __float_as_uint(sv[16 * c + x] * gam[half * 64 + 16 * c + x]);
+                    tmem_st16(tmem_addr(tm, j, kColS + half * 64 + 16 * c), r);
+                }
             }
             tmem_wait_st();
             tc_fence_before();
@@ -435,13 +495,11 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 tc_fence_after();
                 float *hp = a.hT + (size_t)bh * (kD * kD) + v;
 #pragma unroll 1
-                for (int d0 = 0; d0 < kD; d0 += 16) {
-                    uint32_t r[16];
-                    tmem_ld16(tmem_addr(tm, j, kColS + d0), r);
-                    tmem_wait_ld();
-                    reg_fence(r);
+                for (int half = 0; half < 2; ++half) {
+                    float sv[64];
+                    tmem_ld64(tmem_addr(tm, j, kColS + half * 64), sv);
 #pragma unroll
-                    for (int x = 0; x < 16; ++x) hp[(d0 + x) * kD] = __uint_as_float(r[x]);
+                    for (int x = 0; x < 64; ++x) hp[(half * 64 + x) * kD] = sv[x];
                 }
             }
         }
@@ -454,6 +512,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         const int d = 2 * p;
         const uint32_t boxo = (uint32_t)(p >> 5) * 8192;
         const uint32_t col = (uint32_t)(d & 63);
+        const float lim = kExtreme * kLog2e;
         for (int lc = 0; lc < n; ++lc) {
             const int st = lc & 1;
             const uint32_t u = lc >> 1;
@@ -461,41 +520,21 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             if (named_bar_or(1, 256, !w)) { ok = false; break; }
             if (gt == 0) TRACE_OUT(1, lc);
             uint8_t *base = sm + st * om::STAGE;
-            const float *gs = reinterpret_cast<const float *>(base + om::G);
-            float b0[16], b1[16];
-            float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-            for (int x = 0; x < 16; ++x) {
-                const float2 gv = *reinterpret_cast<const float2 *>(gs + (16 * qq + x) * kD + d);
-                a0 += gv.x;
-                a1 += gv.y;
-                b0[x] = a0;
-                b1[x] = a1;
-            }
-            *reinterpret_cast<float2 *>(xch + qq * kD + d) = make_float2(a0, a1);
-            named_bar_sync(1, 256);
-            float o0 = 0.f, o1 = 0.f;
-            for (int q2 = 0; q2 < qq; ++q2) {
-                const float2 t = *reinterpret_cast<const float2 *>(xch + q2 * kD + d);
-                o0 += t.x;
-                o1 += t.y;
-            }
+            float b0[16], b1[16];   // cumulative log2-gates of this thread's tokens
+            gate_cumsum(reinterpret_cast<const float *>(base + om::G), xch, qq, d, b0, b1, 1);
             float mx = 0.f;
 #pragma unroll
-            for (int x = 0; x < 16; ++x) {
-                b0[x] += o0;
-                b1[x] += o1;
-                mx = fmaxf(mx, fmaxf(fabsf(b0[x]), fabsf(b1[x])));
-            }
-            if (qq == 3) {
+            for (int x = 0; x < 16; ++x) mx = fmaxf(mx, fmaxf(fabsf(b0[x]), fabsf(b1[x])));
+            if (qq == 3) {   // chunk totals -> exp(Bc) for the state warps and K^
                 bv_s[st * 128 + d] = b0[15];
                 bv_s[st * 128 + d + 1] = b1[15];
-                gam_s[st * 128 + d] = ex2(b0[15] * kLog2e);
-                gam_s[st * 128 + d + 1] = ex2(b1[15] * kLog2e);
+                gam_s[st * 128 + d] = ex2(b0[15]);
+                gam_s[st * 128 + d + 1] = ex2(b1[15]);
             }
-            const bool extreme = named_bar_or(1, 256, mx > kExtreme);
-            const float B0 = bv_s[st * 128 + d], B1 = bv_s[st * 128 + d + 1];
+            const bool extreme = named_bar_or(1, 256, mx > lim);
+            // every gate row has been read (the barriers above): K^ may overwrite them
             const float G0 = gam_s[st * 128 + d], G1 = gam_s[st * 128 + d + 1];
+            const float B0 = bv_s[st * 128 + d], B1 = bv_s[st * 128 + d + 1];
             uint8_t *qt = base + om::Q + boxo;
             uint8_t *kt = base + om::K + boxo;
             uint8_t *kh = base + om::KH + boxo;
@@ -504,8 +543,8 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 const uint32_t off = sw128_offset(16 * qq + x, col);
                 const float2 qv = unpack_bf16(*reinterpret_cast<const uint32_t *>(qt + off));
                 const float2 kv = unpack_bf16(*reinterpret_cast<const uint32_t *>(kt + off));
-                const float ep0 = ex2(b0[x] * kLog2e), ep1 = ex2(b1[x] * kLog2e);
-                const float em0 = ex2(-b0[x] * kLog2e), em1 = ex2(-b1[x] * kLog2e);
+                const float ep0 = ex2(b0[x]), ep1 = ex2(b1[x]);
+                const float em0 = ex2(-b0[x]), em1 = ex2(-b1[x]);
                 *reinterpret_cast<uint32_t *>(qt + off) = pack_bf16(qv.x * ep0, qv.y * ep1);
                 *reinterpret_cast<uint32_t *>(kt + off) = pack_bf16(kv.x * em0, kv.y * em1);
                 float kh0, kh1;
@@ -513,8 +552,8 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     kh0 = kv.x * em0 * G0;
                     kh1 = kv.y * em1 * G1;
                 } else {
-                    kh0 = kv.x * ex2((B0 - b0[x]) * kLog2e);
-                    kh1 = kv.y * ex2((B1 - b1[x]) * kLog2e);
+                    kh0 = kv.x * ex2(B0 - b0[x]);
+                    kh1 = kv.y * ex2(B1 - b1[x]);
                 }
                 *reinterpret_cast<uint32_t *>(kh + off) = pack_bf16(kh0, kh1);
             }
@@ -538,16 +577,19 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
 }
 
 // ======================================================================= state kernel
+// Three-stage ring of k, v and gate rows; the suffix-decayed keys K^' overwrite the gate
+// rows of their stage once all of them have been read.
 namespace sm_ {
-constexpr uint32_t K = 0, V = 16384, G = 32768, KH = 65536, STAGE = 81920;
-constexpr uint32_t BV = 2 * STAGE;     // [2][128] f32
-constexpr uint32_t XCH = BV + 1024;    // [4][128] f32
+constexpr int NST = 3;
+constexpr uint32_t K = 0, V = 16384, G = 32768, KH = G, STAGE = 65536;
+constexpr uint32_t BV = NST * STAGE;   // [3][128] f32 chunk totals
+constexpr uint32_t XCH = BV + 1536;    // [4][128] f32
 constexpr uint32_t BAR = XCH + 2048;
-constexpr uint32_t TSLOT = BAR + 64;
+constexpr uint32_t TSLOT = BAR + 80;
 constexpr uint32_t ALLOC = TSLOT + 16 + 1024;
 }  // namespace sm_
 
-enum { SFULL = 0, SEMPTY = 2, SGDONE = 4, SEDONE = 6 };
+enum { SFULL = 0, SEMPTY = 3, SGDONE = 6, SEDONE = 9 };
 
 __global__ void __launch_bounds__(kStateThreads, 1)
 gla_tc_state_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
@@ -566,9 +608,10 @@ gla_tc_state_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
     int cb, ce;
     seg_range(seg, a.nchunks, a.splits, cb, ce);
     const int n = ce - cb;
+    constexpr int NST = sm_::NST;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < NST; ++i) {
             mbar_init(&bars[SFULL + i], 1);
             mbar_init(&bars[SEMPTY + i], 1);
             mbar_init(&bars[SGDONE + i], 8);
@@ -590,24 +633,24 @@ gla_tc_state_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
 
     if (warp == 0) {
         if (lane == 0) {
-            int issued[2] = {0, 0};
+            int issued[NST] = {0, 0, 0};
             for (int lc = 0; lc < n; ++lc) {
-                const int st = lc & 1;
-                const uint32_t u = lc >> 1;
-                if (lc >= 2 && !mbar_wait(&bars[SEMPTY + st], (u - 1) & 1)) { ok = false; break; }
+                const int st = lc % NST;
+                const uint32_t u = lc / NST;
+                if (lc >= NST && !mbar_wait(&bars[SEMPTY + st], (u - 1) & 1)) { ok = false; break; }
                 uint8_t *base = sm + st * sm_::STAGE;
                 uint64_t *fb = &bars[SFULL + st];
                 TRACE_ST(0, lc);
                 mbar_arrive_expect_tx(fb, 2 * 16384 + 32768);
                 const int t = (ce - 1 - lc) * kC;      // last chunk first
+                tma_load_4d(base + sm_::G, &tg, fb, 0, h, t, bidx);
                 tma_load_4d(base + sm_::K, &tk, fb, 0, h, t, bidx);
                 tma_load_4d(base + sm_::K + 8192, &tk, fb, 64, h, t, bidx);
                 tma_load_4d(base + sm_::V, &tv, fb, 0, h, t, bidx);
                 tma_load_4d(base + sm_::V + 8192, &tv, fb, 64, h, t, bidx);
-                tma_load_4d(base + sm_::G, &tg, fb, 0, h, t, bidx);
                 ++issued[st];
             }
-            for (int st = 0; st < 2; ++st)
+            for (int st = 0; st < NST; ++st)
                 if (issued[st] > 0 && !mbar_wait(&bars[SFULL + st], (issued[st] - 1) & 1)) ok = false;
         }
         __syncwarp();
@@ -615,8 +658,8 @@ gla_tc_state_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
         if (lane == 0) {
             const uint32_t idU = idesc_bf16(128, 128, 1, 1);
             for (int lc = 0; lc < n; ++lc) {
-                const int st = lc & 1;
-                const uint32_t u = lc >> 1;
+                const int st = lc % NST;
+                const uint32_t u = lc / NST;
                 if (!mbar_wait(&bars[SGDONE + st], u & 1)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t base = smem_u32(sm + st * sm_::STAGE);
@@ -633,55 +676,36 @@ gla_tc_state_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
         }
         __syncwarp();
     } else {
-        // gate warps 2..9: suffix-decayed keys  k * exp(Bc - b + l), l = sum of later Bc
+        // gate warps 2..9: suffix-decayed keys k * exp(Bc - b + l), l = sum of later Bc
         const int gt = (warp - 2) * 32 + lane;
         const int p = gt & 63, qq = gt >> 6;
         const int d = 2 * p;
         const uint32_t boxo = (uint32_t)(p >> 5) * 8192;
         const uint32_t col = (uint32_t)(d & 63);
-        float l0 = 0.f, l1 = 0.f;
+        float l0 = 0.f, l1 = 0.f;   // log2 of the decay from this chunk's end to the segment end
         for (int lc = 0; lc < n; ++lc) {
-            const int st = lc & 1;
-            const uint32_t u = lc >> 1;
+            const int st = lc % NST;
+            const uint32_t u = lc / NST;
             const bool w = mbar_wait(&bars[SFULL + st], u & 1);
             if (named_bar_or(1, 256, !w)) { ok = false; break; }
             if (gt == 0) TRACE_ST(1, lc);
             uint8_t *base = sm + st * sm_::STAGE;
-            const float *gs = reinterpret_cast<const float *>(base + sm_::G);
             float b0[16], b1[16];
-            float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-            for (int x = 0; x < 16; ++x) {
-                const float2 gv = *reinterpret_cast<const float2 *>(gs + (16 * qq + x) * kD + d);
-                a0 += gv.x;
-                a1 += gv.y;
-                b0[x] = a0;
-                b1[x] = a1;
-            }
-            *reinterpret_cast<float2 *>(xch + qq * kD + d) = make_float2(a0, a1);
-            named_bar_sync(1, 256);
-            float o0 = 0.f, o1 = 0.f;
-            for (int q2 = 0; q2 < qq; ++q2) {
-                const float2 t = *reinterpret_cast<const float2 *>(xch + q2 * kD + d);
-                o0 += t.x;
-                o1 += t.y;
-            }
+            gate_cumsum(reinterpret_cast<const float *>(base + sm_::G), xch, qq, d, b0, b1, 1);
             if (qq == 3) {
-                bv_s[st * 128 + d] = b0[15] + o0;
-                bv_s[st * 128 + d + 1] = b1[15] + o1;
+                bv_s[st * 128 + d] = b0[15];
+                bv_s[st * 128 + d + 1] = b1[15];
             }
             named_bar_sync(1, 256);
-            const float B0 = bv_s[st * 128 + d], B1 = bv_s[st * 128 + d + 1];
-            const float s0 = B0 + l0, s1 = B1 + l1;
+            const float s0 = bv_s[st * 128 + d] + l0, s1 = bv_s[st * 128 + d + 1] + l1;
             const uint8_t *kt = base + sm_::K + boxo;
             uint8_t *kh = base + sm_::KH + boxo;
 #pragma unroll
             for (int x = 0; x < 16; ++x) {
                 const uint32_t off = sw128_offset(16 * qq + x, col);
                 const float2 kv = unpack_bf16(*reinterpret_cast<const uint32_t *>(kt + off));
-                const float f0 = ex2((s0 - (b0[x] + o0)) * kLog2e);
-                const float f1 = ex2((s1 - (b1[x] + o1)) * kLog2e);
-                *reinterpret_cast<uint32_t *>(kh + off) = pack_bf16(kv.x * f0, kv.y * f1);
+                *reinterpret_cast<uint32_t *>(kh + off) =
+                    pack_bf16(kv.x * ex2(s0 - b0[x]), kv.y * ex2(s1 - b1[x]));
             }
             l0 = s0;
             l1 = s1;
@@ -692,8 +716,8 @@ gla_tc_state_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
         }
         if (ok && qq == 0) {
             float *gp = a.gam + ((size_t)bh * (a.splits - 1) + seg) * kD;
-            gp[d] = ex2(l0 * kLog2e);
-            gp[d + 1] = ex2(l1 * kLog2e);
+            gp[d] = ex2(l0);
+            gp[d + 1] = ex2(l1);
         }
         // E^T (lane = v, column = d) -> E[d][v]
         if (ok && warp >= 4 && warp < 8) {
@@ -705,13 +729,11 @@ gla_tc_state_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
                 tc_fence_after();
                 float *ep = a.E + ((size_t)bh * (a.splits - 1) + seg) * (kD * kD) + v;
 #pragma unroll 1
-                for (int d0 = 0; d0 < kD; d0 += 16) {
-                    uint32_t r[16];
-                    tmem_ld16(tmem_addr(tm, j, d0), r);
-                    tmem_wait_ld();
-                    reg_fence(r);
+                for (int half = 0; half < 2; ++half) {
+                    float ev[64];
+                    tmem_ld64(tmem_addr(tm, j, half * 64), ev);
 #pragma unroll
-                    for (int x = 0; x < 16; ++x) ep[(d0 + x) * kD] = __uint_as_float(r[x]);
+                    for (int x = 0; x < 64; ++x) ep[(half * 64 + x) * kD] = ev[x];
                 }
             }
         }
@@ -812,7 +834,7 @@ cudaError_t launch_tc(const Problem &p, int splits, void *ws, size_t ws_bytes,
     const int s = clamp_splits(p, splits);
     cudaError_t e = set_attrs();
     if (e != cudaSuccess) return e;
-    CUtensorMap mq, mk, mv, mg;
+    CUtensorMap mq, mk, mv, mg, mo;
     if (!make_bthd_map(&mq, p.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.B, p.T, p.H, kD, 64, kC,
                        CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_bthd_map(&mk, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.B, p.T, p.H, kD, 64, kC,
@@ -820,7 +842,9 @@ cudaError_t launch_tc(const Problem &p, int splits, void *ws, size_t ws_bytes,
         !make_bthd_map(&mv, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.B, p.T, p.H, kD, 64, kC,
                        CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_bthd_map(&mg, p.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.B, p.T, p.H, kD, kD, kC,
-                       CU_TENSOR_MAP_SWIZZLE_NONE))
+                       CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_bthd_map(&mo, p.o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.B, p.T, p.H, kD, 64, kC,
+                       CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     const int nchunks = (int)((p.T + kC - 1) / kC);
     const int bh = (int)(p.B * p.H);
@@ -838,9 +862,8 @@ cudaError_t launch_tc(const Problem &p, int splits, void *ws, size_t ws_bytes,
         count_launches(2);
     }
     OutArgs oa{static_cast<const __nv_bfloat16 *>(p.q), static_cast<const __nv_bfloat16 *>(p.k),
-               p.g, static_cast<__nv_bfloat16 *>(p.o), p.h0, p.hT, sstart, p.T, (int)p.H,
-               nchunks, s, p.scale, dev_err};
-    gla_tc_out_kernel<<<bh * s, kOutThreads, om::ALLOC, stream>>>(mq, mk, mv, mg, oa);
+               p.g, p.h0, p.hT, sstart, p.T, (int)p.H, nchunks, s, p.scale, dev_err};
+    gla_tc_out_kernel<<<bh * s, kOutThreads, om::ALLOC, stream>>>(mq, mk, mv, mg, mo, oa);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     count_launches(1);
     return cudaSuccess;
