@@ -3,6 +3,7 @@
 #include <atomic>
 #include <mutex>
 #include <stdint.h>
+#include <stdio.h>
 #include <string.h>
 
 #include "gla.h"
@@ -25,6 +26,11 @@ struct DeviceState {
 };
 
 std::mutex g_mu;
+thread_local char g_detail[256] = "";
+
+void set_detail(const char *where, cudaError_t e) {
+    snprintf(g_detail, sizeof(g_detail), "%s: %s (%d)", where, cudaGetErrorString(e), (int)e);
+}
 std::atomic<uint64_t> g_launches{0};
 DeviceState g_dev[kMaxDevices];
 
@@ -127,8 +133,10 @@ gla_status library_workspace(DeviceState *st, size_t need, void **out) {
             st->ws_bytes = 0;
         }
         void *p = nullptr;
-        if (cudaMalloc(&p, need) != cudaSuccess) {
+        const cudaError_t e = cudaMalloc(&p, need);
+        if (e != cudaSuccess) {
             cudaGetLastError();
+            set_detail("workspace cudaMalloc", e);
             return GLA_ERR_WORKSPACE;
         }
         st->ws = p;
@@ -151,6 +159,8 @@ void count_launches(unsigned n) { g_launches.fetch_add(n, std::memory_order_rela
 }  // namespace gla
 
 extern "C" {
+
+const char *gla_last_error_detail(void) { return g_detail; }
 
 uint64_t gla_launch_counter(void) { return g_launches.load(std::memory_order_relaxed); }
 
@@ -244,6 +254,7 @@ gla_status gla_fwd_ex(const void *q, const void *k, const void *v, const float *
     }
     if (e != cudaSuccess) {
         cudaGetLastError();
+        set_detail(path == GLA_PATH_EXACT ? "exact path launch" : "tensor-core path launch", e);
         return GLA_ERR_LAUNCH;
     }
     return GLA_OK;

@@ -188,7 +188,7 @@ __device__ __forceinline__ void gate_cumsum(const float *gs, float *xch, int qq,
 }
 
 // ======================================================================= output kernel
-__global__ void __maxnreg__(112)
+__global__ void __launch_bounds__(kOutThreads, 1)
 gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg,
                   const __grid_constant__ CUtensorMap to, const OutArgs a) {
@@ -845,7 +845,7 @@ cudaError_t launch_tc(const Problem &p, int splits, void *ws, size_t ws_bytes,
                        CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !make_bthd_map(&mo, p.o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.B, p.T, p.H, kD, 64, kC,
                        CU_TENSOR_MAP_SWIZZLE_128B))
-        return cudaErrorInvalidValue;
+        return cudaErrorInvalidResourceHandle;   // a tensor map could not be encoded
     const int nchunks = (int)((p.T + kC - 1) / kC);
     const int bh = (int)(p.B * p.H);
     float *E = nullptr, *gam = nullptr, *sstart = nullptr;

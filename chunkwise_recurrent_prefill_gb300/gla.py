@@ -29,9 +29,10 @@ IO_BF16, IO_F32 = 0, 1
 
 
 class GLAError(RuntimeError):
-    def __init__(self, status: int, where: str):
+    def __init__(self, status: int, where: str, detail: str = ""):
         self.status = status
-        super().__init__(f"{where}: {STATUS.get(status, status)}")
+        msg = f"{where}: {STATUS.get(status, status)}"
+        super().__init__(msg + (f" ({detail})" if detail else ""))
 
 
 class _Options(ctypes.Structure):
@@ -68,6 +69,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.gla_path_for.argtypes = [i64, i64, i64, i64, i64, ctypes.c_int,
                                          ctypes.POINTER(_Options)]
             lib.gla_path_for.restype = ctypes.c_int
+            lib.gla_last_error_detail.argtypes = []
+            lib.gla_last_error_detail.restype = ctypes.c_char_p
             lib.gla_launch_counter.argtypes = []
             lib.gla_launch_counter.restype = ctypes.c_uint64
             lib.gla_version.argtypes = []
@@ -161,7 +164,8 @@ def gla_fwd(q, k, v, g, scale: float, h0=None, *, o=None, hT=None, return_state:
                             _ptr(o), _ptr(hT), B, T, H, Dk, Dv, io, ctypes.byref(opt),
                             _stream_handle(stream))
     if rc != GLA_OK:
-        raise GLAError(rc, "gla_fwd_ex")
+        detail = lib.gla_last_error_detail().decode() if rc in (6, 9) else ""
+        raise GLAError(rc, "gla_fwd_ex", detail)
     return o, hT
 
 

@@ -125,6 +125,10 @@ int gla_path_for(int64_t B, int64_t T, int64_t H, int64_t Dk, int64_t Dv, int io
  */
 gla_status gla_last_device_status(gla_stream_t stream);
 
+/* Text of the last CUDA error behind a GLA_ERR_LAUNCH / GLA_ERR_WORKSPACE returned to
+ * this host thread ("" if none). Thread-local static storage; never NULL. */
+const char *gla_last_error_detail(void);
+
 /* Human-readable name of a status (static storage; never NULL). */
 const char *gla_status_string(gla_status s);
 
