@@ -80,33 +80,35 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
 
 // TMEM column map of the output kernel (512 columns).
 constexpr uint32_t kColS = 0;      // S^T fp32, 128 columns
-constexpr uint32_t kColSB = 128;   // S^T bf16 (A operand), 2 x 64 columns
+constexpr uint32_t kColSB = 128;   // S^T bf16 snapshot (A operand), 2 x 64 columns
 constexpr uint32_t kColP = 256;    // P fp32 (M=64 layout), 2 x 64 columns
 constexpr uint32_t kColO = 384;    // O^T fp32, 2 x 64 columns
 
-// Shared-memory map of the output kernel (bytes from a 1024-aligned base). A stage holds
-// the raw q, k, v tiles (128B-swizzled [64 x 64] bf16 boxes, two per tile) and the fp32
-// log-gate rows; the gate warps rewrite q -> Q~ and k -> K~ in place and write K^ over
-// the first half of the gate rows once every gate row has been read.
+// Shared-memory map of the output kernel (bytes from a 1024-aligned base).
+//   q/k/v ring (3 stages): raw tiles as 128B-swizzled [64 x 64] bf16 boxes, two per tile;
+//     the gate warps rewrite q -> Q~ and k -> K~ (or K^ in an extreme chunk) in place, and
+//     the epilogue stages the chunk's output in the dead Q~ tile for the bulk store.
+//   gate ring (2 slots): fp32 log-gate rows, released as soon as the cumsum has read them.
 namespace om {
-constexpr uint32_t Q = 0, K = 16384, V = 32768, G = 49152, KH = G, STAGE = 81920;
-constexpr uint32_t P = 2 * STAGE;      // 2 x [64 x 64] bf16 P tiles (128B swizzle)
-constexpr uint32_t OST = P + 16384;    // [64 x 128] bf16 output staging (two boxes)
-constexpr uint32_t GAM = OST + 16384;  // [2][128] f32 exp(Bc)
-constexpr uint32_t BV = GAM + 1024;    // [2][128] f32 Bc (log2 units)
-constexpr uint32_t XCH = BV + 1024;    // [4][128] f32 token-quarter totals
-constexpr uint32_t XF = XCH + 2048;    // [2] u32 "extreme chunk" flags
-constexpr uint32_t SCR = XF + 64;      // [4][64] f32 exact-path scratch
-constexpr uint32_t BAR = SCR + 1024;   // mbarriers
-constexpr uint32_t NBAR = 20;
+constexpr int NQ = 3, NG = 2;
+constexpr uint32_t Q = 0, K = 16384, V = 32768, QSTAGE = 49152;
+constexpr uint32_t G = NQ * QSTAGE, GSLOT = 32768;
+constexpr uint32_t P = G + NG * GSLOT;  // [64 x 64] bf16 P tile (128B swizzle)
+constexpr uint32_t GAM = P + 8192;      // [4][128] f32 exp(Bc) per chunk (ring of 4)
+constexpr uint32_t BV = GAM + 2048;     // [128] f32 Bc of the chunk being gated (log2 units)
+constexpr uint32_t XCH = BV + 512;      // [4][128] f32 token-quarter totals
+constexpr uint32_t XF = XCH + 2048;     // [4] u32 "extreme chunk" flags (ring of 4)
+constexpr uint32_t SCR = XF + 64;       // [4][64] f32 exact-path scratch
+constexpr uint32_t BAR = SCR + 1024;    // mbarriers
+constexpr uint32_t NBAR = 25;
 constexpr uint32_t TSLOT = BAR + NBAR * 8;
 constexpr uint32_t ALLOC = TSLOT + 16 + 1024;
 }  // namespace om
 
 // mbarrier indices of the output kernel
 enum {
-    FULL = 0, EMPTY = 2, GDONE = 4, PFULL = 6, PFREE = 8, PBF = 10, SREADY = 12, UDONE = 13,
-    OFULL = 14, OFREE = 16, FIN = 18,
+    QFULL = 0, QEMPTY = 3, GFULL = 6, GEMPTY = 8, GDONE = 10, PFULL = 13, PFREE = 15,
+    PBF = 17, SREADY = 18, UDONE = 19, OFULL = 20, OFREE = 22, FIN = 24,
 };
 
 constexpr int kOutThreads = 576;       // 18 warps
@@ -160,7 +162,8 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&out)[64]) {
 
 // In-chunk cumulative log-gate of one thread's column pair over 16 tokens, in log2 units,
 // shared with the other token quarters through `xch` (named barrier `bar`, 256 threads).
-// On return b0/b1 hold the chunk-inclusive cumulative log2-gates of the thread's tokens.
+// On return b0/b1 hold the chunk-inclusive cumulative log2-gates of the thread's tokens,
+// and every participating thread has finished reading `gs`.
 __device__ __forceinline__ void gate_cumsum(const float *gs, float *xch, int qq, int d,
                                             float (&b0)[16], float (&b1)[16], uint32_t bar) {
     float a0 = 0.f, a1 = 0.f;
@@ -187,19 +190,23 @@ __device__ __forceinline__ void gate_cumsum(const float *gs, float *xch, int qq,
     }
 }
 
+// Phase parity of the k-th use of a ring slot.
+__device__ __forceinline__ uint32_t par(int use) { return (uint32_t)use & 1u; }
+
 // ======================================================================= output kernel
 __global__ void __launch_bounds__(kOutThreads, 1)
 gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg,
                   const __grid_constant__ CUtensorMap to, const OutArgs a) {
+    using namespace om;
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = align1024(smraw);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + om::BAR);
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + om::TSLOT);
-    float *gam_s = reinterpret_cast<float *>(sm + om::GAM);
-    float *bv_s = reinterpret_cast<float *>(sm + om::BV);
-    float *xch = reinterpret_cast<float *>(sm + om::XCH);
-    uint32_t *xf = reinterpret_cast<uint32_t *>(sm + om::XF);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + BAR);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + TSLOT);
+    float *gam_s = reinterpret_cast<float *>(sm + GAM);
+    float *bv_s = reinterpret_cast<float *>(sm + BV);
+    float *xch = reinterpret_cast<float *>(sm + XCH);
+    uint32_t *xf = reinterpret_cast<uint32_t *>(sm + XF);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int seg = blockIdx.x % a.splits;
@@ -210,16 +217,22 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     const int n = ce - cb;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&bars[FULL + i], 1);
-            mbar_init(&bars[EMPTY + i], 1);
+        for (int i = 0; i < NQ; ++i) {
+            mbar_init(&bars[QFULL + i], 1);
+            mbar_init(&bars[QEMPTY + i], 1);
             mbar_init(&bars[GDONE + i], 8);
+        }
+        for (int i = 0; i < NG; ++i) {
+            mbar_init(&bars[GFULL + i], 1);
+            mbar_init(&bars[GEMPTY + i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&bars[PFULL + i], 1);
             mbar_init(&bars[PFREE + i], 4);
-            mbar_init(&bars[PBF + i], 4);
             mbar_init(&bars[OFULL + i], 1);
             mbar_init(&bars[OFREE + i], 4);
         }
+        mbar_init(&bars[PBF], 4);
         mbar_init(&bars[SREADY], 4);
         mbar_init(&bars[UDONE], 1);
         mbar_init(&bars[FIN], 1);
@@ -241,91 +254,121 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     if (threadIdx.x == 0) TRACE_OUT(14, 0);
 
     if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
+        // ------------------------------------------------------------ TMA producer (2 rings)
         if (lane == 0) {
-            int issued[2] = {0, 0};
-            for (int lc = 0; lc < n; ++lc) {
-                const int st = lc & 1;
-                const uint32_t u = lc >> 1;
-                if (lc >= 2 && !mbar_wait(&bars[EMPTY + st], (u - 1) & 1)) { ok = false; break; }
-                uint8_t *base = sm + st * om::STAGE;
-                uint64_t *fb = &bars[FULL + st];
-                TRACE_OUT(0, lc);
-                mbar_arrive_expect_tx(fb, 3 * 16384 + 32768);
-                const int t = (cb + lc) * kC;
-                tma_load_4d(base + om::G, &tg, fb, 0, h, t, bidx);
-                tma_load_4d(base + om::Q, &tq, fb, 0, h, t, bidx);
-                tma_load_4d(base + om::Q + 8192, &tq, fb, 64, h, t, bidx);
-                tma_load_4d(base + om::K, &tk, fb, 0, h, t, bidx);
-                tma_load_4d(base + om::K + 8192, &tk, fb, 64, h, t, bidx);
-                tma_load_4d(base + om::V, &tv, fb, 0, h, t, bidx);
-                tma_load_4d(base + om::V + 8192, &tv, fb, 64, h, t, bidx);
-                ++issued[st];
+            int ng = 0, nq = 0;
+            uint64_t t_last = global_ns();
+            while (ng < n || nq < n) {
+                bool prog = false;
+                if (ng < n && (ng < NG || mbar_try_wait(&bars[GEMPTY + ng % NG], par(ng / NG - 1)))) {
+                    uint64_t *fb = &bars[GFULL + ng % NG];
+                    mbar_arrive_expect_tx(fb, 32768);
+                    tma_load_4d(sm + G + (ng % NG) * GSLOT, &tg, fb, 0, h, (cb + ng) * kC, bidx);
+                    ++ng;
+                    prog = true;
+                }
+                if (nq < n && (nq < NQ || mbar_try_wait(&bars[QEMPTY + nq % NQ], par(nq / NQ - 1)))) {
+                    uint8_t *base = sm + (nq % NQ) * QSTAGE;
+                    uint64_t *fb = &bars[QFULL + nq % NQ];
+                    TRACE_OUT(0, nq);
+                    mbar_arrive_expect_tx(fb, 3 * 16384);
+                    const int t = (cb + nq) * kC;
+                    tma_load_4d(base + Q, &tq, fb, 0, h, t, bidx);
+                    tma_load_4d(base + Q + 8192, &tq, fb, 64, h, t, bidx);
+                    tma_load_4d(base + K, &tk, fb, 0, h, t, bidx);
+                    tma_load_4d(base + K + 8192, &tk, fb, 64, h, t, bidx);
+                    tma_load_4d(base + V, &tv, fb, 0, h, t, bidx);
+                    tma_load_4d(base + V + 8192, &tv, fb, 64, h, t, bidx);
+                    ++nq;
+                    prog = true;
+                }
+                if (prog) {
+                    t_last = global_ns();
+                } else if (global_ns() - t_last > kWaitLimitNs) {
+                    ok = false;
+                    break;
+                }
             }
             // never leave with a bulk copy still landing in this CTA's shared memory
-            for (int st = 0; st < 2; ++st)
-                if (issued[st] > 0 && !mbar_wait(&bars[FULL + st], (issued[st] - 1) & 1)) ok = false;
+            for (int i = 0; i < NG; ++i) {
+                const int uses = ng > i ? (ng - 1 - i) / NG + 1 : 0;
+                if (uses > 0 && !mbar_wait(&bars[GFULL + i], par(uses - 1))) ok = false;
+            }
+            for (int i = 0; i < NQ; ++i) {
+                const int uses = nq > i ? (nq - 1 - i) / NQ + 1 : 0;
+                if (uses > 0 && !mbar_wait(&bars[QFULL + i], par(uses - 1))) ok = false;
+            }
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        // order per chunk c: U(c) [needs S_c ready], P(c+1) [needs gates of c+1], O(c)
+        // ------------------------------------------------------------ MMA scheduler
+        // P(c): gates of c ready;  U(c): state snapshot of c taken;  O(c): P tile of c and
+        // U(c) issued. Issued in that order per chunk, interleaved across chunks as their
+        // inputs become ready (non-blocking polls).
         if (lane == 0) {
             const uint32_t idP = idesc_bf16(64, 64, 0, 0);
             const uint32_t idU = idesc_bf16(128, 128, 1, 1);
             const uint32_t idOi = idesc_bf16(128, 64, 1, 0);
             const uint32_t idOs = idesc_bf16(128, 64, 0, 0);
-            auto issue_p = [&](int lc) -> bool {
-                const int st = lc & 1;
-                const uint32_t u = lc >> 1;
-                if (!mbar_wait(&bars[GDONE + st], u & 1)) return false;
-                if (lc >= 2 && !mbar_wait(&bars[PFREE + st], (u - 1) & 1)) return false;
-                TRACE_OUT(3, lc);
-                tc_fence_after();
-                const uint32_t base = smem_u32(sm + st * om::STAGE);
+            int np = 0, nu = 0, no = 0;
+            uint64_t t_last = global_ns();
+            while (no < n) {
+                bool prog = false;
+                if (np < n && mbar_try_wait(&bars[GDONE + np % NQ], par(np / NQ)) &&
+                    (np < 2 || mbar_try_wait(&bars[PFREE + (np & 1)], par(np / 2 - 1)))) {
+                    tc_fence_after();
+                    TRACE_OUT(3, np);
+                    const uint32_t base = smem_u32(sm + (np % NQ) * QSTAGE);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
-                    mma_ss(tm + kColP + st * 64, smem_desc(base + om::Q + off, 16, 1024),
-                           smem_desc(base + om::K + off, 16, 1024), idP, kk > 0);
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
+                        mma_ss(tm + kColP + (np & 1) * 64, smem_desc(base + Q + off, 16, 1024),
+                               smem_desc(base + K + off, 16, 1024), idP, kk > 0);
+                    }
+                    mma_commit(&bars[PFULL + (np & 1)]);
+                    TRACE_OUT(4, np);
+                    ++np;
+                    prog = true;
                 }
-                mma_commit(&bars[PFULL + st]);
-                TRACE_OUT(4, lc);
-                return true;
-            };
-            if (n > 0 && !issue_p(0)) ok = false;
-            for (int lc = 0; lc < n && ok; ++lc) {
-                const int st = lc & 1;
-                const uint32_t u = lc >> 1;
-                const uint32_t base = smem_u32(sm + st * om::STAGE);
-                // S^T += V^T K^   (128 x 128, K = 64 tokens)
-                if (!mbar_wait(&bars[SREADY], lc & 1)) { ok = false; break; }
-                TRACE_OUT(5, lc);
-                tc_fence_after();
+                if (nu < np && mbar_try_wait(&bars[SREADY], par(nu))) {
+                    tc_fence_after();
+                    TRACE_OUT(5, nu);
+                    const uint32_t base = smem_u32(sm + (nu % NQ) * QSTAGE);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_ss(tm + kColS, smem_desc(base + om::V + kk * 2048, 8192, 1024),
-                           smem_desc(base + om::KH + kk * 2048, 8192, 1024), idU, 1);
-                mma_commit(&bars[UDONE]);
-                if (lc + 1 < n && !issue_p(lc + 1)) { ok = false; break; }
-                // O^T = V^T P^T + S^T Q~^T   (128 x 64)
-                if (!mbar_wait(&bars[PBF + st], u & 1)) { ok = false; break; }
-                if (lc >= 2 && !mbar_wait(&bars[OFREE + st], (u - 1) & 1)) { ok = false; break; }
-                TRACE_OUT(6, lc);
-                tc_fence_after();
-                const uint32_t pbase = smem_u32(sm + om::P + st * 8192);
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_ss(tm + kColS, smem_desc(base + V + kk * 2048, 8192, 1024),
+                               smem_desc(base + K + kk * 2048, 8192, 1024), idU, 1);
+                    mma_commit(&bars[UDONE]);
+                    ++nu;
+                    prog = true;
+                }
+                if (no < nu && mbar_try_wait(&bars[PBF], par(no)) &&
+                    (no < 2 || mbar_try_wait(&bars[OFREE + (no & 1)], par(no / 2 - 1)))) {
+                    tc_fence_after();
+                    TRACE_OUT(6, no);
+                    const uint32_t base = smem_u32(sm + (no % NQ) * QSTAGE);
+                    const uint32_t pbase = smem_u32(sm + P);
+                    const uint32_t od = tm + kColO + (no & 1) * 64;
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_ss(tm + kColO + st * 64, smem_desc(base + om::V + kk * 2048, 8192, 1024),
-                           smem_desc(pbase + kk * 32, 16, 1024), idOi, kk > 0);
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_ss(od, smem_desc(base + V + kk * 2048, 8192, 1024),
+                               smem_desc(pbase + kk * 32, 16, 1024), idOi, kk > 0);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ts(tm + kColO + st * 64, tm + kColSB + st * 64 + kk * 8,
-                           smem_desc(base + om::Q + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
-                           idOs, 1);
-                mma_commit(&bars[OFULL + st]);
-                mma_commit(&bars[EMPTY + st]);
-                TRACE_OUT(7, lc);
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_ts(od, tm + kColSB + (no & 1) * 64 + kk * 8,
+                               smem_desc(base + Q + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
+                               idOs, 1);
+                    mma_commit(&bars[OFULL + (no & 1)]);
+                    TRACE_OUT(7, no);
+                    ++no;
+                    prog = true;
+                }
+                if (prog) {
+                    t_last = global_ns();
+                } else if (global_ns() - t_last > kWaitLimitNs) {
+                    ok = false;
+                    break;
+                }
             }
             // all issued MMAs complete before the CTA tears down its TMEM
             mma_commit(&bars[FIN]);
@@ -337,28 +380,27 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         const int j = warp & 3;
         const int et = (warp - 4) * 32 + lane;      // 0..127
         const int v = j * 32 + lane;                // O^T lane = value column
-        float *scr = reinterpret_cast<float *>(sm + om::SCR);
-        uint8_t *ost = sm + om::OST + (v >> 6) * 8192;
-        const uint32_t vcol = (uint32_t)(v & 63);
-        for (int lc = 0; lc <= n && ok; ++lc) {
-            if (lc < n) {
-                const int st = lc & 1;
-                const uint32_t u = lc >> 1;
-                bool w = mbar_wait(&bars[GDONE + st], u & 1) && mbar_wait(&bars[PFULL + st], u & 1);
+        float *scr = reinterpret_cast<float *>(sm + SCR);
+        const uint32_t vbox = (uint32_t)(v >> 6) * 8192, vcol = (uint32_t)(v & 63);
+        for (int c = 0; c <= n && ok; ++c) {
+            if (c < n) {
+                bool w = mbar_wait(&bars[GDONE + c % NQ], par(c / NQ)) &&
+                         mbar_wait(&bars[PFULL + (c & 1)], par(c / 2)) &&
+                         (c == 0 || mbar_wait(&bars[OFULL + ((c - 1) & 1)], par((c - 1) / 2)));
                 if (named_bar_or(2, 128, !w)) { ok = false; break; }
-                if (et == 0) TRACE_OUT(10, lc);
+                if (et == 0) TRACE_OUT(10, c);
                 tc_fence_after();
-                const bool extreme = xf[st] != 0;
+                const bool extreme = xf[c & 3] != 0;
                 float prow[64];
                 const int i = 16 * j + lane;        // P row held by this lane (lane < 16)
                 if (!extreme) {
-                    tmem_ld64(tmem_addr(tm, j, kColP + st * 64), prow);
+                    tmem_ld64(tmem_addr(tm, j, kColP + (c & 1) * 64), prow);
                 } else {
                     // exact route: P_ij = sum_d q_id k_jd exp(b_id - b_jd), j <= i
 #pragma unroll
                     for (int x = 0; x < 64; ++x) prow[x] = 0.f;
                     float *gcol = scr, *qcol = scr + 64, *kcol = scr + 128, *bcol = scr + 192;
-                    const int64_t t0 = (int64_t)(cb + lc) * kC;
+                    const int64_t t0 = (int64_t)(cb + c) * kC;
                     for (int d = 0; d < kD; ++d) {
                         if (et < 64) {
                             const int64_t t = t0 + et;
@@ -385,16 +427,17 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[PFREE + st]);
+                if (lane == 0) mbar_arrive(&bars[PFREE + (c & 1)]);
                 if (lane < 16) {
-                    uint8_t *pt = sm + om::P + st * 8192;
+                    uint8_t *pt = sm + P;
 #pragma unroll
                     for (int cc = 0; cc < 8; ++cc) {
                         uint32_t wv[4];
 #pragma unroll
                         for (int x = 0; x < 4; ++x) {
-                            const int c = cc * 8 + 2 * x;
-                            wv[x] = pack_bf16(c <= i ? prow[c] : 0.f, c + 1 <= i ? prow[c + 1] : 0.f);
+                            const int col = cc * 8 + 2 * x;
+                            wv[x] = pack_bf16(col <= i ? prow[col] : 0.f,
+                                              col + 1 <= i ? prow[col + 1] : 0.f);
                         }
                         *reinterpret_cast<uint4 *>(pt + sw128_offset(i, cc * 8)) =
                             make_uint4(wv[0], wv[1], wv[2], wv[3]);
@@ -402,36 +445,43 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[PBF + st]);
-                if (et == 0) TRACE_OUT(11, lc);
+                if (lane == 0) mbar_arrive(&bars[PBF]);
+                if (et == 0) TRACE_OUT(11, c);
             }
-            if (lc >= 1) {
-                const int pc = lc - 1;
-                const int st = pc & 1;
-                const uint32_t u = pc >> 1;
-                const bool w = mbar_wait(&bars[OFULL + st], u & 1);
-                if (named_bar_or(2, 128, !w)) { ok = false; break; }
+            if (c >= 1) {
+                // epilogue of chunk c-1 (its O is complete: waited above, or here at the end)
+                const int pc = c - 1;
+                if (c == n) {
+                    const bool w = mbar_wait(&bars[OFULL + (pc & 1)], par(pc / 2));
+                    if (named_bar_or(2, 128, !w)) { ok = false; break; }
+                }
                 if (et == 0) TRACE_OUT(12, pc);
                 tc_fence_after();
                 float ov[64];
-                tmem_ld64(tmem_addr(tm, j, kColO + st * 64), ov);
+                tmem_ld64(tmem_addr(tm, j, kColO + (pc & 1) * 64), ov);
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[OFREE + st]);
-                // stage O (bf16, 128B-swizzled boxes) and write it with two bulk tensor stores
-                if (et == 0) bulk_wait_read_all();
-                named_bar_sync(2, 128);
+                if (lane == 0) mbar_arrive(&bars[OFREE + (pc & 1)]);
+                // stage O (bf16, 128B-swizzled boxes) in the chunk's dead Q~ tile
+                uint8_t *ost = sm + (pc % NQ) * QSTAGE + Q + vbox;
 #pragma unroll
-                for (int x = 0; x < 64; ++x)
+                for (int x = 0; x < 64; x += 2) {
+                    const float o0 = a.scale * ov[x], o1 = a.scale * ov[x + 1];
                     *reinterpret_cast<__nv_bfloat16 *>(ost + sw128_offset(x, vcol)) =
-                        __float2bfloat16_rn(a.scale * ov[x]);
+                        __float2bfloat16_rn(o0);
+                    *reinterpret_cast<__nv_bfloat16 *>(ost + sw128_offset(x + 1, vcol)) =
+                        __float2bfloat16_rn(o1);
+                }
                 fence_proxy_async_smem();
                 named_bar_sync(2, 128);
                 if (et == 0) {
                     const int t0 = (cb + pc) * kC;
-                    tma_store_4d(&to, sm + om::OST, 0, h, t0, bidx);
-                    tma_store_4d(&to, sm + om::OST + 8192, 64, h, t0, bidx);
+                    uint8_t *ob = sm + (pc % NQ) * QSTAGE + Q;
+                    tma_store_4d(&to, ob, 0, h, t0, bidx);
+                    tma_store_4d(&to, ob + 8192, 64, h, t0, bidx);
                     bulk_commit();
+                    bulk_wait_read_all();
+                    mbar_arrive(&bars[QEMPTY + pc % NQ]);   // the stage may be refilled
                     TRACE_OUT(13, pc);
                 }
             }
@@ -439,7 +489,10 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         if (et == 0) bulk_wait_all();
         __syncwarp();
     } else if (warp >= 8 && warp < 12) {
-        // ------------------------------------------------------------ state scan (TMEM)
+        // ------------------------------------------------------------ state (TMEM)
+        // After U(c-1) the TMEM state holds S_{c-1} + K~^T V (a normal chunk: exp(Bc) still
+        // to apply) or S_c already (an extreme chunk was scaled before its U). Pass c:
+        // finish S_c, snapshot it in bf16 for O(c), and pre-scale if chunk c is extreme.
         const int j = warp & 3;
         const int v = j * 32 + lane;
         const float *init = nullptr;
@@ -456,50 +509,67 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             tmem_st16(tmem_addr(tm, j, kColS + d0), r);
         }
         tmem_wait_st();
-        for (int lc = 0; lc < n; ++lc) {
-            const int st = lc & 1;
-            const uint32_t u = lc >> 1;
-            if (lc >= 1 && !mbar_wait(&bars[UDONE], (lc - 1) & 1)) { ok = false; break; }
-            if (!mbar_wait(&bars[GDONE + st], u & 1)) { ok = false; break; }
-            if (v == 0) TRACE_OUT(8, lc);
+        for (int c = 0; c < n; ++c) {
+            if (c >= 1 && !mbar_wait(&bars[UDONE], par(c - 1))) { ok = false; break; }
+            if (!mbar_wait(&bars[GDONE + c % NQ], par(c / NQ))) { ok = false; break; }
+            if (c >= 2 && !mbar_wait(&bars[OFULL + (c & 1)], par(c / 2 - 1))) { ok = false; break; }
+            if (v == 0) TRACE_OUT(8, c);
             tc_fence_after();
-            const float *gam = gam_s + st * 128;
+            const bool post = c >= 1 && xf[(c - 1) & 3] == 0;   // finish S_c = exp(B_{c-1}) (.)
+            const bool pre = xf[c & 3] != 0;                     // extreme chunk c: scale now
+            const float *gprev = gam_s + ((c - 1) & 3) * 128;
+            const float *gcur = gam_s + (c & 3) * 128;
 #pragma unroll 1
             for (int half = 0; half < 2; ++half) {
                 float sv[64];
                 tmem_ld64(tmem_addr(tm, j, kColS + half * 64), sv);
+                if (post) {
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                    for (int x = 0; x < 64; ++x) sv[x] *= gprev[half * 64 + x];
+                }
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
                     uint32_t pk[8];
 #pragma unroll
                     for (int x = 0; x < 8; ++x)
-                        pk[x] = pack_bf16(sv[16 * c + 2 * x], sv[16 * c + 2 * x + 1]);
-                    tmem_st8(tmem_addr(tm, j, kColSB + st * 64 + half * 32 + c * 8), pk);
-                    uint32_t r[16];
+                        pk[x] = pack_bf16(sv[16 * cc + 2 * x], sv[16 * cc + 2 * x + 1]);
+                    tmem_st8(tmem_addr(tm, j, kColSB + (c & 1) * 64 + half * 32 + cc * 8), pk);
+                }
+                if (pre) {
 #pragma unroll
-                    for (int x = 0; x < 16; ++x)
-                        r[x] = __float_as_uint(sv[16 * c + x] * gam[half * 64 + 16 * c + x]);
-                    tmem_st16(tmem_addr(tm, j, kColS + half * 64 + 16 * c), r);
+                    for (int x = 0; x < 64; ++x) sv[x] *= gcur[half * 64 + x];
+                }
+                if (post || pre) {
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        uint32_t r[16];
+#pragma unroll
+                        for (int x = 0; x < 16; ++x) r[x] = __float_as_uint(sv[16 * cc + x]);
+                        tmem_st16(tmem_addr(tm, j, kColS + half * 64 + 16 * cc), r);
+                    }
                 }
             }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[SREADY]);
-            if (v == 0) TRACE_OUT(9, lc);
+            if (v == 0) TRACE_OUT(9, c);
         }
         if (ok && a.hT && seg == a.splits - 1) {
-            if (!mbar_wait(&bars[UDONE], (n - 1) & 1)) {
+            if (!mbar_wait(&bars[UDONE], par(n - 1))) {
                 ok = false;
             } else {
                 tc_fence_after();
+                const bool post = xf[(n - 1) & 3] == 0;
+                const float *gprev = gam_s + ((n - 1) & 3) * 128;
                 float *hp = a.hT + (size_t)bh * (kD * kD) + v;
 #pragma unroll 1
                 for (int half = 0; half < 2; ++half) {
                     float sv[64];
                     tmem_ld64(tmem_addr(tm, j, kColS + half * 64), sv);
 #pragma unroll
-                    for (int x = 0; x < 64; ++x) hp[(half * 64 + x) * kD] = sv[x];
+                    for (int x = 0; x < 64; ++x)
+                        hp[(half * 64 + x) * kD] = post ? sv[x] * gprev[half * 64 + x] : sv[x];
                 }
             }
         }
@@ -513,55 +583,48 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         const uint32_t boxo = (uint32_t)(p >> 5) * 8192;
         const uint32_t col = (uint32_t)(d & 63);
         const float lim = kExtreme * kLog2e;
-        for (int lc = 0; lc < n; ++lc) {
-            const int st = lc & 1;
-            const uint32_t u = lc >> 1;
-            const bool w = mbar_wait(&bars[FULL + st], u & 1);
+        for (int c = 0; c < n; ++c) {
+            bool w = mbar_wait(&bars[GFULL + c % NG], par(c / NG));
             if (named_bar_or(1, 256, !w)) { ok = false; break; }
-            if (gt == 0) TRACE_OUT(1, lc);
-            uint8_t *base = sm + st * om::STAGE;
+            if (gt == 0) TRACE_OUT(1, c);
             float b0[16], b1[16];   // cumulative log2-gates of this thread's tokens
-            gate_cumsum(reinterpret_cast<const float *>(base + om::G), xch, qq, d, b0, b1, 1);
+            gate_cumsum(reinterpret_cast<const float *>(sm + G + (c % NG) * GSLOT), xch, qq, d,
+                        b0, b1, 1);
+            if (gt == 0) mbar_arrive(&bars[GEMPTY + c % NG]);   // gate rows all read
             float mx = 0.f;
 #pragma unroll
             for (int x = 0; x < 16; ++x) mx = fmaxf(mx, fmaxf(fabsf(b0[x]), fabsf(b1[x])));
-            if (qq == 3) {   // chunk totals -> exp(Bc) for the state warps and K^
-                bv_s[st * 128 + d] = b0[15];
-                bv_s[st * 128 + d + 1] = b1[15];
-                gam_s[st * 128 + d] = ex2(b0[15]);
-                gam_s[st * 128 + d + 1] = ex2(b1[15]);
+            if (qq == 3) {   // chunk totals: Bc, and exp(Bc) for the state warps
+                bv_s[d] = b0[15];
+                bv_s[d + 1] = b1[15];
+                gam_s[(c & 3) * 128 + d] = ex2(b0[15]);
+                gam_s[(c & 3) * 128 + d + 1] = ex2(b1[15]);
             }
             const bool extreme = named_bar_or(1, 256, mx > lim);
-            // every gate row has been read (the barriers above): K^ may overwrite them
-            const float G0 = gam_s[st * 128 + d], G1 = gam_s[st * 128 + d + 1];
-            const float B0 = bv_s[st * 128 + d], B1 = bv_s[st * 128 + d + 1];
-            uint8_t *qt = base + om::Q + boxo;
-            uint8_t *kt = base + om::K + boxo;
-            uint8_t *kh = base + om::KH + boxo;
+            w = mbar_wait(&bars[QFULL + c % NQ], par(c / NQ));
+            if (named_bar_or(1, 256, !w)) { ok = false; break; }
+            const float B0 = bv_s[d], B1 = bv_s[d + 1];
+            uint8_t *base = sm + (c % NQ) * QSTAGE;
+            uint8_t *qt = base + Q + boxo;
+            uint8_t *kt = base + K + boxo;
 #pragma unroll
             for (int x = 0; x < 16; ++x) {
                 const uint32_t off = sw128_offset(16 * qq + x, col);
                 const float2 qv = unpack_bf16(*reinterpret_cast<const uint32_t *>(qt + off));
                 const float2 kv = unpack_bf16(*reinterpret_cast<const uint32_t *>(kt + off));
-                const float ep0 = ex2(b0[x]), ep1 = ex2(b1[x]);
-                const float em0 = ex2(-b0[x]), em1 = ex2(-b1[x]);
-                *reinterpret_cast<uint32_t *>(qt + off) = pack_bf16(qv.x * ep0, qv.y * ep1);
-                *reinterpret_cast<uint32_t *>(kt + off) = pack_bf16(kv.x * em0, kv.y * em1);
-                float kh0, kh1;
-                if (!extreme) {
-                    kh0 = kv.x * em0 * G0;
-                    kh1 = kv.y * em1 * G1;
-                } else {
-                    kh0 = kv.x * ex2(B0 - b0[x]);
-                    kh1 = kv.y * ex2(B1 - b1[x]);
-                }
-                *reinterpret_cast<uint32_t *>(kh + off) = pack_bf16(kh0, kh1);
+                *reinterpret_cast<uint32_t *>(qt + off) =
+                    pack_bf16(qv.x * ex2(b0[x]), qv.y * ex2(b1[x]));
+                // normal chunk: K~ = k exp(-b) (exp(Bc) is applied to the state after U);
+                // extreme chunk: K^ = k exp(Bc - b) (the state is scaled before U)
+                const float e0 = extreme ? B0 - b0[x] : -b0[x];
+                const float e1 = extreme ? B1 - b1[x] : -b1[x];
+                *reinterpret_cast<uint32_t *>(kt + off) = pack_bf16(kv.x * ex2(e0), kv.y * ex2(e1));
             }
-            if (gt == 0) xf[st] = extreme ? 1u : 0u;
+            if (gt == 0) xf[c & 3] = extreme ? 1u : 0u;
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[GDONE + st]);
-            if (gt == 0) TRACE_OUT(2, lc);
+            if (lane == 0) mbar_arrive(&bars[GDONE + c % NQ]);
+            if (gt == 0) TRACE_OUT(2, c);
         }
         __syncwarp();
     }
@@ -577,29 +640,36 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
 }
 
 // ======================================================================= state kernel
-// Three-stage ring of k, v and gate rows; the suffix-decayed keys K^' overwrite the gate
-// rows of their stage once all of them have been read.
+// k/v ring of four stages and a two-slot gate ring (released after the cumsum); the
+// suffix-decayed keys K^' overwrite k in place.
 namespace sm_ {
-constexpr int NST = 3;
-constexpr uint32_t K = 0, V = 16384, G = 32768, KH = G, STAGE = 65536;
-constexpr uint32_t BV = NST * STAGE;   // [3][128] f32 chunk totals
-constexpr uint32_t XCH = BV + 1536;    // [4][128] f32
+constexpr int NKV = 4, NG = 2;
+constexpr uint32_t K = 0, V = 16384, KVSTAGE = 32768;
+constexpr uint32_t G = NKV * KVSTAGE, GSLOT = 32768;
+constexpr uint32_t BV = G + NG * GSLOT;  // [128] f32 chunk totals
+constexpr uint32_t XCH = BV + 512;       // [4][128] f32
 constexpr uint32_t BAR = XCH + 2048;
-constexpr uint32_t TSLOT = BAR + 80;
+constexpr uint32_t NBAR = 17;
+constexpr uint32_t TSLOT = BAR + NBAR * 8;
 constexpr uint32_t ALLOC = TSLOT + 16 + 1024;
 }  // namespace sm_
 
-enum { SFULL = 0, SEMPTY = 3, SGDONE = 6, SEDONE = 9 };
+// The gate-done ring has as many slots as the k/v ring: gate(c + NKV) needs the k/v stage
+// that U(c) releases, so the MMA thread has always observed gate-done(c) before its slot
+// is reused (no phase can be lapped).
+enum { SKFULL = 0, SKEMPTY = 4, SGFULL = 8, SGEMPTY = 10, SGDONE = 12, SEDONE = 16 };
+static_assert(SGDONE + sm_::NKV <= SEDONE, "state-kernel barrier map");
 
 __global__ void __launch_bounds__(kStateThreads, 1)
 gla_tc_state_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                     const __grid_constant__ CUtensorMap tg, const StateArgs a) {
+    using namespace sm_;
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = align1024(smraw);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + sm_::BAR);
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + sm_::TSLOT);
-    float *bv_s = reinterpret_cast<float *>(sm + sm_::BV);
-    float *xch = reinterpret_cast<float *>(sm + sm_::XCH);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + BAR);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + TSLOT);
+    float *bv_s = reinterpret_cast<float *>(sm + BV);
+    float *xch = reinterpret_cast<float *>(sm + XCH);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nseg = a.splits - 1;
     const int seg = blockIdx.x % nseg;
@@ -608,14 +678,18 @@ gla_tc_state_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
     int cb, ce;
     seg_range(seg, a.nchunks, a.splits, cb, ce);
     const int n = ce - cb;
-    constexpr int NST = sm_::NST;
+    constexpr int NGD = NKV;   // gate-done ring
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < NST; ++i) {
-            mbar_init(&bars[SFULL + i], 1);
-            mbar_init(&bars[SEMPTY + i], 1);
-            mbar_init(&bars[SGDONE + i], 8);
+        for (int i = 0; i < NKV; ++i) {
+            mbar_init(&bars[SKFULL + i], 1);
+            mbar_init(&bars[SKEMPTY + i], 1);
         }
+        for (int i = 0; i < NG; ++i) {
+            mbar_init(&bars[SGFULL + i], 1);
+            mbar_init(&bars[SGEMPTY + i], 1);
+        }
+        for (int i = 0; i < NGD; ++i) mbar_init(&bars[SGDONE + i], 8);
         mbar_init(&bars[SEDONE], 1);
         fence_mbar_init();
     }
@@ -633,43 +707,61 @@ gla_tc_state_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
 
     if (warp == 0) {
         if (lane == 0) {
-            int issued[NST] = {0, 0, 0};
-            for (int lc = 0; lc < n; ++lc) {
-                const int st = lc % NST;
-                const uint32_t u = lc / NST;
-                if (lc >= NST && !mbar_wait(&bars[SEMPTY + st], (u - 1) & 1)) { ok = false; break; }
-                uint8_t *base = sm + st * sm_::STAGE;
-                uint64_t *fb = &bars[SFULL + st];
-                TRACE_ST(0, lc);
-                mbar_arrive_expect_tx(fb, 2 * 16384 + 32768);
-                const int t = (ce - 1 - lc) * kC;      // last chunk first
-                tma_load_4d(base + sm_::G, &tg, fb, 0, h, t, bidx);
-                tma_load_4d(base + sm_::K, &tk, fb, 0, h, t, bidx);
-                tma_load_4d(base + sm_::K + 8192, &tk, fb, 64, h, t, bidx);
-                tma_load_4d(base + sm_::V, &tv, fb, 0, h, t, bidx);
-                tma_load_4d(base + sm_::V + 8192, &tv, fb, 64, h, t, bidx);
-                ++issued[st];
+            int ng = 0, nk = 0;
+            uint64_t t_last = global_ns();
+            while (ng < n || nk < n) {
+                bool prog = false;
+                if (ng < n && (ng < NG || mbar_try_wait(&bars[SGEMPTY + ng % NG], par(ng / NG - 1)))) {
+                    uint64_t *fb = &bars[SGFULL + ng % NG];
+                    TRACE_ST(0, ng);
+                    mbar_arrive_expect_tx(fb, 32768);
+                    tma_load_4d(sm + G + (ng % NG) * GSLOT, &tg, fb, 0, h, (ce - 1 - ng) * kC, bidx);
+                    ++ng;
+                    prog = true;
+                }
+                if (nk < n && (nk < NKV || mbar_try_wait(&bars[SKEMPTY + nk % NKV], par(nk / NKV - 1)))) {
+                    uint8_t *base = sm + (nk % NKV) * KVSTAGE;
+                    uint64_t *fb = &bars[SKFULL + nk % NKV];
+                    mbar_arrive_expect_tx(fb, 2 * 16384);
+                    const int t = (ce - 1 - nk) * kC;      // last chunk first
+                    tma_load_4d(base + K, &tk, fb, 0, h, t, bidx);
+                    tma_load_4d(base + K + 8192, &tk, fb, 64, h, t, bidx);
+                    tma_load_4d(base + V, &tv, fb, 0, h, t, bidx);
+                    tma_load_4d(base + V + 8192, &tv, fb, 64, h, t, bidx);
+                    ++nk;
+                    prog = true;
+                }
+                if (prog) {
+                    t_last = global_ns();
+                } else if (global_ns() - t_last > kWaitLimitNs) {
+                    ok = false;
+                    break;
+                }
             }
-            for (int st = 0; st < NST; ++st)
-                if (issued[st] > 0 && !mbar_wait(&bars[SFULL + st], (issued[st] - 1) & 1)) ok = false;
+            for (int i = 0; i < NG; ++i) {
+                const int uses = ng > i ? (ng - 1 - i) / NG + 1 : 0;
+                if (uses > 0 && !mbar_wait(&bars[SGFULL + i], par(uses - 1))) ok = false;
+            }
+            for (int i = 0; i < NKV; ++i) {
+                const int uses = nk > i ? (nk - 1 - i) / NKV + 1 : 0;
+                if (uses > 0 && !mbar_wait(&bars[SKFULL + i], par(uses - 1))) ok = false;
+            }
         }
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) {
             const uint32_t idU = idesc_bf16(128, 128, 1, 1);
-            for (int lc = 0; lc < n; ++lc) {
-                const int st = lc % NST;
-                const uint32_t u = lc / NST;
-                if (!mbar_wait(&bars[SGDONE + st], u & 1)) { ok = false; break; }
+            for (int c = 0; c < n; ++c) {
+                if (!mbar_wait(&bars[SGDONE + c % NGD], par(c / NGD))) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t base = smem_u32(sm + st * sm_::STAGE);
+                const uint32_t base = smem_u32(sm + (c % NKV) * KVSTAGE);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_ss(tm, smem_desc(base + sm_::V + kk * 2048, 8192, 1024),
-                           smem_desc(base + sm_::KH + kk * 2048, 8192, 1024), idU,
-                           (lc > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(&bars[SEMPTY + st]);
-                TRACE_ST(3, lc);
+                    mma_ss(tm, smem_desc(base + V + kk * 2048, 8192, 1024),
+                           smem_desc(base + K + kk * 2048, 8192, 1024), idU,
+                           (c > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(&bars[SKEMPTY + c % NKV]);
+                TRACE_ST(3, c);
             }
             mma_commit(&bars[SEDONE]);
             if (!mbar_wait(&bars[SEDONE], 0)) ok = false;
@@ -682,37 +774,36 @@ gla_tc_state_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
         const int d = 2 * p;
         const uint32_t boxo = (uint32_t)(p >> 5) * 8192;
         const uint32_t col = (uint32_t)(d & 63);
-        float l0 = 0.f, l1 = 0.f;   // log2 of the decay from this chunk's end to the segment end
-        for (int lc = 0; lc < n; ++lc) {
-            const int st = lc % NST;
-            const uint32_t u = lc / NST;
-            const bool w = mbar_wait(&bars[SFULL + st], u & 1);
+        float l0 = 0.f, l1 = 0.f;   // log2 decay from this chunk's end to the segment end
+        for (int c = 0; c < n; ++c) {
+            bool w = mbar_wait(&bars[SGFULL + c % NG], par(c / NG));
             if (named_bar_or(1, 256, !w)) { ok = false; break; }
-            if (gt == 0) TRACE_ST(1, lc);
-            uint8_t *base = sm + st * sm_::STAGE;
+            if (gt == 0) TRACE_ST(1, c);
             float b0[16], b1[16];
-            gate_cumsum(reinterpret_cast<const float *>(base + sm_::G), xch, qq, d, b0, b1, 1);
+            gate_cumsum(reinterpret_cast<const float *>(sm + G + (c % NG) * GSLOT), xch, qq, d,
+                        b0, b1, 1);
+            if (gt == 0) mbar_arrive(&bars[SGEMPTY + c % NG]);
             if (qq == 3) {
-                bv_s[st * 128 + d] = b0[15];
-                bv_s[st * 128 + d + 1] = b1[15];
+                bv_s[d] = b0[15];
+                bv_s[d + 1] = b1[15];
             }
-            named_bar_sync(1, 256);
-            const float s0 = bv_s[st * 128 + d] + l0, s1 = bv_s[st * 128 + d + 1] + l1;
-            const uint8_t *kt = base + sm_::K + boxo;
-            uint8_t *kh = base + sm_::KH + boxo;
+            w = mbar_wait(&bars[SKFULL + c % NKV], par(c / NKV));
+            if (named_bar_or(1, 256, !w)) { ok = false; break; }   // also publishes bv_s
+            const float s0 = bv_s[d] + l0, s1 = bv_s[d + 1] + l1;
+            uint8_t *kt = sm + (c % NKV) * KVSTAGE + K + boxo;
 #pragma unroll
             for (int x = 0; x < 16; ++x) {
                 const uint32_t off = sw128_offset(16 * qq + x, col);
                 const float2 kv = unpack_bf16(*reinterpret_cast<const uint32_t *>(kt + off));
-                *reinterpret_cast<uint32_t *>(kh + off) =
+                *reinterpret_cast<uint32_t *>(kt + off) =
                     pack_bf16(kv.x * ex2(s0 - b0[x]), kv.y * ex2(s1 - b1[x]));
             }
             l0 = s0;
             l1 = s1;
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[SGDONE + st]);
-            if (gt == 0) TRACE_ST(2, lc);
+            if (lane == 0) mbar_arrive(&bars[SGDONE + c % NGD]);
+            if (gt == 0) TRACE_ST(2, c);
         }
         if (ok && qq == 0) {
             float *gp = a.gam + ((size_t)bh * (a.splits - 1) + seg) * kD;
