@@ -85,30 +85,31 @@ constexpr uint32_t kColP = 256;    // P fp32 (M=64 layout), 2 x 64 columns
 constexpr uint32_t kColO = 384;    // O^T fp32, 2 x 64 columns
 
 // Shared-memory map of the output kernel (bytes from a 1024-aligned base).
-//   q/k/v ring (3 stages): raw tiles as 128B-swizzled [64 x 64] bf16 boxes, two per tile;
-//     the gate warps rewrite q -> Q~ and k -> K~ (or K^ in an extreme chunk) in place, and
-//     the epilogue stages the chunk's output in the dead Q~ tile for the bulk store.
-//   gate ring (2 slots): fp32 log-gate rows, released as soon as the cumsum has read them.
+//   q/k/v ring (4 stages): raw tiles as 128B-swizzled [64 x 64] bf16 boxes, two per tile;
+//     the gate warps rewrite q -> Q~ and k -> K~ (or K^ in an extreme chunk) in place.
+//   The log-gate rows are read by the gate warps straight from global memory (one chunk
+//   ahead, after a TMA prefetch into L2), so they take no shared memory.
 namespace om {
-constexpr int NQ = 3, NG = 2;
+constexpr int NQ = 4;                   // q/k/v stages
+constexpr int NR = 8;                   // per-chunk ring of exp(Bc) and extreme flags
 constexpr uint32_t Q = 0, K = 16384, V = 32768, QSTAGE = 49152;
-constexpr uint32_t G = NQ * QSTAGE, GSLOT = 32768;
-constexpr uint32_t P = G + NG * GSLOT;  // [64 x 64] bf16 P tile (128B swizzle)
-constexpr uint32_t GAM = P + 8192;      // [4][128] f32 exp(Bc) per chunk (ring of 4)
-constexpr uint32_t BV = GAM + 2048;     // [128] f32 Bc of the chunk being gated (log2 units)
+constexpr uint32_t P = NQ * QSTAGE;     // [64 x 64] bf16 P tile (128B swizzle)
+constexpr uint32_t OST = P + 8192;      // [64 x 128] bf16 output staging (two boxes)
+constexpr uint32_t GAM = OST + 16384;   // [NR][128] f32 exp(Bc) per chunk
+constexpr uint32_t BV = GAM + NR * 512; // [128] f32 Bc of the chunk being gated (log2 units)
 constexpr uint32_t XCH = BV + 512;      // [4][128] f32 token-quarter totals
-constexpr uint32_t XF = XCH + 2048;     // [4] u32 "extreme chunk" flags (ring of 4)
+constexpr uint32_t XF = XCH + 2048;     // [NR] u32 "extreme chunk" flags
 constexpr uint32_t SCR = XF + 64;       // [4][64] f32 exact-path scratch
 constexpr uint32_t BAR = SCR + 1024;    // mbarriers
-constexpr uint32_t NBAR = 25;
+constexpr uint32_t NBAR = 24;
 constexpr uint32_t TSLOT = BAR + NBAR * 8;
 constexpr uint32_t ALLOC = TSLOT + 16 + 1024;
 }  // namespace om
 
 // mbarrier indices of the output kernel
 enum {
-    QFULL = 0, QEMPTY = 3, GFULL = 6, GEMPTY = 8, GDONE = 10, PFULL = 13, PFREE = 15,
-    PBF = 17, SREADY = 18, UDONE = 19, OFULL = 20, OFREE = 22, FIN = 24,
+    QFULL = 0, QEMPTY = 4, GDONE = 8, PFULL = 12, PFREE = 14, PBF = 16, SREADY = 17,
+    UDONE = 18, OFULL = 19, OFREE = 21, FIN = 23,
 };
 
 constexpr int kOutThreads = 576;       // 18 warps
@@ -222,10 +223,6 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             mbar_init(&bars[QEMPTY + i], 1);
             mbar_init(&bars[GDONE + i], 8);
         }
-        for (int i = 0; i < NG; ++i) {
-            mbar_init(&bars[GFULL + i], 1);
-            mbar_init(&bars[GEMPTY + i], 1);
-        }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars[PFULL + i], 1);
             mbar_init(&bars[PFREE + i], 4);
@@ -254,46 +251,26 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     if (threadIdx.x == 0) TRACE_OUT(14, 0);
 
     if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer (2 rings)
+        // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            int ng = 0, nq = 0;
-            uint64_t t_last = global_ns();
-            while (ng < n || nq < n) {
-                bool prog = false;
-                if (ng < n && (ng < NG || mbar_try_wait(&bars[GEMPTY + ng % NG], par(ng / NG - 1)))) {
-                    uint64_t *fb = &bars[GFULL + ng % NG];
-                    mbar_arrive_expect_tx(fb, 32768);
-                    tma_load_4d(sm + G + (ng % NG) * GSLOT, &tg, fb, 0, h, (cb + ng) * kC, bidx);
-                    ++ng;
-                    prog = true;
-                }
-                if (nq < n && (nq < NQ || mbar_try_wait(&bars[QEMPTY + nq % NQ], par(nq / NQ - 1)))) {
-                    uint8_t *base = sm + (nq % NQ) * QSTAGE;
-                    uint64_t *fb = &bars[QFULL + nq % NQ];
-                    TRACE_OUT(0, nq);
-                    mbar_arrive_expect_tx(fb, 3 * 16384);
-                    const int t = (cb + nq) * kC;
-                    tma_load_4d(base + Q, &tq, fb, 0, h, t, bidx);
-                    tma_load_4d(base + Q + 8192, &tq, fb, 64, h, t, bidx);
-                    tma_load_4d(base + K, &tk, fb, 0, h, t, bidx);
-                    tma_load_4d(base + K + 8192, &tk, fb, 64, h, t, bidx);
-                    tma_load_4d(base + V, &tv, fb, 0, h, t, bidx);
-                    tma_load_4d(base + V + 8192, &tv, fb, 64, h, t, bidx);
-                    ++nq;
-                    prog = true;
-                }
-                if (prog) {
-                    t_last = global_ns();
-                } else if (global_ns() - t_last > kWaitLimitNs) {
-                    ok = false;
-                    break;
-                }
+            int nq = 0;
+            for (; nq < n; ++nq) {
+                const int st = nq % NQ;
+                if (nq >= NQ && !mbar_wait(&bars[QEMPTY + st], par(nq / NQ - 1))) { ok = false; break; }
+                uint8_t *base = sm + st * QSTAGE;
+                uint64_t *fb = &bars[QFULL + st];
+                TRACE_OUT(0, nq);
+                const int t = (cb + nq) * kC;
+                tma_prefetch_l2_4d(&tg, 0, h, t, bidx);   // gate rows, read later by the gate warps
+                mbar_arrive_expect_tx(fb, 3 * 16384);
+                tma_load_4d(base + Q, &tq, fb, 0, h, t, bidx);
+                tma_load_4d(base + Q + 8192, &tq, fb, 64, h, t, bidx);
+                tma_load_4d(base + K, &tk, fb, 0, h, t, bidx);
+                tma_load_4d(base + K + 8192, &tk, fb, 64, h, t, bidx);
+                tma_load_4d(base + V, &tv, fb, 0, h, t, bidx);
+                tma_load_4d(base + V + 8192, &tv, fb, 64, h, t, bidx);
             }
             // never leave with a bulk copy still landing in this CTA's shared memory
-            for (int i = 0; i < NG; ++i) {
-                const int uses = ng > i ? (ng - 1 - i) / NG + 1 : 0;
-                if (uses > 0 && !mbar_wait(&bars[GFULL + i], par(uses - 1))) ok = false;
-            }
             for (int i = 0; i < NQ; ++i) {
                 const int uses = nq > i ? (nq - 1 - i) / NQ + 1 : 0;
                 if (uses > 0 && !mbar_wait(&bars[QFULL + i], par(uses - 1))) ok = false;
@@ -359,6 +336,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                                smem_desc(base + Q + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
                                idOs, 1);
                     mma_commit(&bars[OFULL + (no & 1)]);
+                    mma_commit(&bars[QEMPTY + no % NQ]);   // P, U and O of chunk no read it
                     TRACE_OUT(7, no);
                     ++no;
                     prog = true;
@@ -381,7 +359,8 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         const int et = (warp - 4) * 32 + lane;      // 0..127
         const int v = j * 32 + lane;                // O^T lane = value column
         float *scr = reinterpret_cast<float *>(sm + SCR);
-        const uint32_t vbox = (uint32_t)(v >> 6) * 8192, vcol = (uint32_t)(v & 63);
+        uint8_t *ost = sm + OST + (uint32_t)(v >> 6) * 8192;
+        const uint32_t vcol = (uint32_t)(v & 63);
         for (int c = 0; c <= n && ok; ++c) {
             if (c < n) {
                 bool w = mbar_wait(&bars[GDONE + c % NQ], par(c / NQ)) &&
@@ -390,7 +369,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 if (named_bar_or(2, 128, !w)) { ok = false; break; }
                 if (et == 0) TRACE_OUT(10, c);
                 tc_fence_after();
-                const bool extreme = xf[c & 3] != 0;
+                const bool extreme = xf[c & (NR - 1)] != 0;
                 float prow[64];
                 const int i = 16 * j + lane;        // P row held by this lane (lane < 16)
                 if (!extreme) {
@@ -462,26 +441,20 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[OFREE + (pc & 1)]);
-                // stage O (bf16, 128B-swizzled boxes) in the chunk's dead Q~ tile
-                uint8_t *ost = sm + (pc % NQ) * QSTAGE + Q + vbox;
+                // stage O (bf16, 128B-swizzled boxes) once the previous store has read it
+                if (et == 0) bulk_wait_read_all();
+                named_bar_sync(2, 128);
 #pragma unroll
-                for (int x = 0; x < 64; x += 2) {
-                    const float o0 = a.scale * ov[x], o1 = a.scale * ov[x + 1];
+                for (int x = 0; x < 64; ++x)
                     *reinterpret_cast<__nv_bfloat16 *>(ost + sw128_offset(x, vcol)) =
-                        __float2bfloat16_rn(o0);
-                    *reinterpret_cast<__nv_bfloat16 *>(ost + sw128_offset(x + 1, vcol)) =
-                        __float2bfloat16_rn(o1);
-                }
+                        __float2bfloat16_rn(a.scale * ov[x]);
                 fence_proxy_async_smem();
                 named_bar_sync(2, 128);
                 if (et == 0) {
                     const int t0 = (cb + pc) * kC;
-                    uint8_t *ob = sm + (pc % NQ) * QSTAGE + Q;
-                    tma_store_4d(&to, ob, 0, h, t0, bidx);
-                    tma_store_4d(&to, ob + 8192, 64, h, t0, bidx);
+                    tma_store_4d(&to, sm + OST, 0, h, t0, bidx);
+                    tma_store_4d(&to, sm + OST + 8192, 64, h, t0, bidx);
                     bulk_commit();
-                    bulk_wait_read_all();
-                    mbar_arrive(&bars[QEMPTY + pc % NQ]);   // the stage may be refilled
                     TRACE_OUT(13, pc);
                 }
             }
@@ -515,10 +488,10 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             if (c >= 2 && !mbar_wait(&bars[OFULL + (c & 1)], par(c / 2 - 1))) { ok = false; break; }
             if (v == 0) TRACE_OUT(8, c);
             tc_fence_after();
-            const bool post = c >= 1 && xf[(c - 1) & 3] == 0;   // finish S_c = exp(B_{c-1}) (.)
-            const bool pre = xf[c & 3] != 0;                     // extreme chunk c: scale now
-            const float *gprev = gam_s + ((c - 1) & 3) * 128;
-            const float *gcur = gam_s + (c & 3) * 128;
+            const bool post = c >= 1 && xf[(c - 1) & (NR - 1)] == 0;   // finish S_c
+            const bool pre = xf[c & (NR - 1)] != 0;                     // extreme chunk c
+            const float *gprev = gam_s + ((c - 1) & (NR - 1)) * 128;
+            const float *gcur = gam_s + (c & (NR - 1)) * 128;
 #pragma unroll 1
             for (int half = 0; half < 2; ++half) {
                 float sv[64];
@@ -560,8 +533,8 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 ok = false;
             } else {
                 tc_fence_after();
-                const bool post = xf[(n - 1) & 3] == 0;
-                const float *gprev = gam_s + ((n - 1) & 3) * 128;
+                const bool post = xf[(n - 1) & (NR - 1)] == 0;
+                const float *gprev = gam_s + ((n - 1) & (NR - 1)) * 128;
                 float *hp = a.hT + (size_t)bh * (kD * kD) + v;
 #pragma unroll 1
                 for (int half = 0; half < 2; ++half) {
@@ -583,26 +556,54 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         const uint32_t boxo = (uint32_t)(p >> 5) * 8192;
         const uint32_t col = (uint32_t)(d & 63);
         const float lim = kExtreme * kLog2e;
+        const int64_t rs = (int64_t)a.H * kD;               // row stride of g (elements)
+        const float *gp = a.g + ((int64_t)bidx * a.T * a.H + h) * kD + d;
+        // this thread's 16 gate rows of a chunk, loaded a chunk ahead
+        float2 gn[16];
+        auto load_g = [&](int c) {
+            const int64_t t0 = (int64_t)(cb + c) * kC + 16 * qq;
+#pragma unroll
+            for (int x = 0; x < 16; ++x)
+                gn[x] = (t0 + x < a.T) ? __ldg(reinterpret_cast<const float2 *>(gp + (t0 + x) * rs))
+                                       : make_float2(0.f, 0.f);
+        };
+        if (n > 0) load_g(0);
         for (int c = 0; c < n; ++c) {
-            bool w = mbar_wait(&bars[GFULL + c % NG], par(c / NG));
-            if (named_bar_or(1, 256, !w)) { ok = false; break; }
-            if (gt == 0) TRACE_OUT(1, c);
             float b0[16], b1[16];   // cumulative log2-gates of this thread's tokens
-            gate_cumsum(reinterpret_cast<const float *>(sm + G + (c % NG) * GSLOT), xch, qq, d,
-                        b0, b1, 1);
-            if (gt == 0) mbar_arrive(&bars[GEMPTY + c % NG]);   // gate rows all read
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int x = 0; x < 16; ++x) {
+                a0 = fmaf(gn[x].x, kLog2e, a0);
+                a1 = fmaf(gn[x].y, kLog2e, a1);
+                b0[x] = a0;
+                b1[x] = a1;
+            }
+            if (c + 1 < n) load_g(c + 1);
+            *reinterpret_cast<float2 *>(xch + qq * kD + d) = make_float2(a0, a1);
+            named_bar_sync(1, 256);
+            float o0 = 0.f, o1 = 0.f;
+            for (int q2 = 0; q2 < qq; ++q2) {
+                const float2 t = *reinterpret_cast<const float2 *>(xch + q2 * kD + d);
+                o0 += t.x;
+                o1 += t.y;
+            }
             float mx = 0.f;
 #pragma unroll
-            for (int x = 0; x < 16; ++x) mx = fmaxf(mx, fmaxf(fabsf(b0[x]), fabsf(b1[x])));
+            for (int x = 0; x < 16; ++x) {
+                b0[x] += o0;
+                b1[x] += o1;
+                mx = fmaxf(mx, fmaxf(fabsf(b0[x]), fabsf(b1[x])));
+            }
             if (qq == 3) {   // chunk totals: Bc, and exp(Bc) for the state warps
                 bv_s[d] = b0[15];
                 bv_s[d + 1] = b1[15];
-                gam_s[(c & 3) * 128 + d] = ex2(b0[15]);
-                gam_s[(c & 3) * 128 + d + 1] = ex2(b1[15]);
+                gam_s[(c & (NR - 1)) * 128 + d] = ex2(b0[15]);
+                gam_s[(c & (NR - 1)) * 128 + d + 1] = ex2(b1[15]);
             }
             const bool extreme = named_bar_or(1, 256, mx > lim);
-            w = mbar_wait(&bars[QFULL + c % NQ], par(c / NQ));
+            const bool w = mbar_wait(&bars[QFULL + c % NQ], par(c / NQ));
             if (named_bar_or(1, 256, !w)) { ok = false; break; }
+            if (gt == 0) TRACE_OUT(1, c);
             const float B0 = bv_s[d], B1 = bv_s[d + 1];
             uint8_t *base = sm + (c % NQ) * QSTAGE;
             uint8_t *qt = base + Q + boxo;
@@ -620,7 +621,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 const float e1 = extreme ? B1 - b1[x] : -b1[x];
                 *reinterpret_cast<uint32_t *>(kt + off) = pack_bf16(kv.x * ex2(e0), kv.y * ex2(e1));
             }
-            if (gt == 0) xf[c & 3] = extreme ? 1u : 0u;
+            if (gt == 0) xf[c & (NR - 1)] = extreme ? 1u : 0u;
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[GDONE + c % NQ]);

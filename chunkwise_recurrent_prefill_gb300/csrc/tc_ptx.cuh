@@ -116,6 +116,16 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const void *tmap, uint64_
         : "memory");
 }
 
+// Prefetch a 4-D tile of a tensor into L2 (no shared-memory destination, no completion).
+__device__ __forceinline__ void tma_prefetch_l2_4d(const void *tmap, int c0, int c1, int c2,
+                                                   int c3) {
+    asm volatile(
+        "cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+            reinterpret_cast<uint64_t>(tmap)),
+        "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+
 // 4-D tiled bulk tensor store from shared memory (bulk-group completion). Rows outside
 // the tensor are not written.
 __device__ __forceinline__ void tma_store_4d(const void *tmap, const void *src, int c0, int c1,
