@@ -7,13 +7,18 @@
 //
 // Per (batch, head) and chunk of C = 64 tokens with in-chunk inclusive cumulative
 // log-gate b (a Dk vector per token) and chunk total Bc = b_63:
-//     Q~ = q * exp(b)          K~ = k * exp(-b)         K^ = k * exp(Bc - b)
-//     P  = (Q~ K~^T) masked to j <= i                                (M=64 MMA)
+//     P  = (Q~ K~^T) masked to j <= i,  Q~ = q exp(b), K~ = k exp(-b)      (M=64 MMA)
 //     O^T = V^T P^T + S^T Q~^T       (S^T bf16 from TMEM as the A operand)   (M=128)
-//     S^T <- diag-scaled S^T * exp(Bc) + V^T K^                              (M=128)
+//     S  <- diag(exp(Bc)) S + (k exp(Bc - b))^T V                            (M=128)
 //     o  = scale * O
 // The state is stored transposed in TMEM (lane = value column v, column = key row d),
-// so every large MMA has M = 128.
+// so every large MMA has M = 128. The output kernel keeps it decay-normalised:
+// S = diag(exp(L)) S~, with L the per-key-row cumulative log-decay since the last
+// renormalisation. Then the update is a pure accumulation S~ += K'^T V with
+// K' = k exp(-(b + L)) and the inter term is Q' S~ with Q' = q exp(b + L); since
+// Q' K'^T = Q~ K~^T the same two tiles serve the intra term too. No CUDA-core pass
+// touches the fp32 state between two chunks except a bf16 snapshot for the inter MMA;
+// the state is rescaled back (S~ <- exp(L) S~, L <- 0) only when |L| grows past a bound.
 //
 // Range: K~ = k * exp(-b) is finite only while |b| stays below ~88. A chunk whose
 // |cumulative log-gate| exceeds kExtreme anywhere is flagged by the gate warps, and its
@@ -47,7 +52,8 @@ using namespace tc;
 constexpr int kC = 64;                 // chunk length (tokens)
 constexpr int kD = 128;                // Dk = Dv
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kExtreme = 60.f;       // |b| beyond which a chunk takes the exact P route
+constexpr float kExtreme2 = 50.f;      // |b| (log2 units) beyond which P takes the exact route
+constexpr float kRenorm2 = 50.f;       // |L| (log2 units) beyond which the state is renormalised
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -91,14 +97,17 @@ constexpr uint32_t kColO = 384;    // O^T fp32, 2 x 64 columns
 //   ahead, after a TMA prefetch into L2), so they take no shared memory.
 namespace om {
 constexpr int NQ = 4;                   // q/k/v stages
-constexpr int NR = 8;                   // per-chunk ring of exp(Bc) and extreme flags
+constexpr int NR = 4;                   // per-chunk ring of scales and flags (written by the
+                                        // gates of c, read before O(c) completes)
 constexpr uint32_t Q = 0, K = 16384, V = 32768, QSTAGE = 49152;
 constexpr uint32_t P = NQ * QSTAGE;     // [64 x 64] bf16 P tile (128B swizzle)
 constexpr uint32_t OST = P + 8192;      // [64 x 128] bf16 output staging (two boxes)
-constexpr uint32_t GAM = OST + 16384;   // [NR][128] f32 exp(Bc) per chunk
-constexpr uint32_t BV = GAM + NR * 512; // [128] f32 Bc of the chunk being gated (log2 units)
+constexpr uint32_t GAM = OST + 16384;   // [NR][128] f32 exp(L_c): renormalisation scale
+constexpr uint32_t GAM2 = GAM + NR * 512; // [NR][128] f32 exp(Bc) (extreme chunks)
+constexpr uint32_t ENDS = GAM2 + NR * 512; // [128] f32 exp(L) after the latest chunk
+constexpr uint32_t BV = ENDS + 512;     // [128] f32 Bc of the chunk being gated (log2 units)
 constexpr uint32_t XCH = BV + 512;      // [4][128] f32 token-quarter totals
-constexpr uint32_t XF = XCH + 2048;     // [NR] u32 "extreme chunk" flags
+constexpr uint32_t XF = XCH + 2048;     // [NR] u32 chunk flags: 1 = extreme, 2 = renormalise
 constexpr uint32_t SCR = XF + 64;       // [4][64] f32 exact-path scratch
 constexpr uint32_t BAR = SCR + 1024;    // mbarriers
 constexpr uint32_t NBAR = 24;
@@ -205,6 +214,8 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + BAR);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + TSLOT);
     float *gam_s = reinterpret_cast<float *>(sm + GAM);
+    float *gam2_s = reinterpret_cast<float *>(sm + GAM2);
+    float *ends_s = reinterpret_cast<float *>(sm + ENDS);
     float *bv_s = reinterpret_cast<float *>(sm + BV);
     float *xch = reinterpret_cast<float *>(sm + XCH);
     uint32_t *xf = reinterpret_cast<uint32_t *>(sm + XF);
@@ -369,7 +380,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 if (named_bar_or(2, 128, !w)) { ok = false; break; }
                 if (et == 0) TRACE_OUT(10, c);
                 tc_fence_after();
-                const bool extreme = xf[c & (NR - 1)] != 0;
+                const bool extreme = (xf[c & (NR - 1)] & 1u) != 0;
                 float prow[64];
                 const int i = 16 * j + lane;        // P row held by this lane (lane < 16)
                 if (!extreme) {
@@ -396,7 +407,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                         }
                         named_bar_sync(2, 128);
                         if (lane < 16) {
-                            const float qi = qcol[i], bi = bcol[i];
+                            const float qi = a.scale * qcol[i], bi = bcol[i];
 #pragma unroll
                             for (int x = 0; x < 64; ++x)
                                 if (x <= i) prow[x] += qi * kcol[x] * ex2((bi - bcol[x]) * kLog2e);
@@ -447,7 +458,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
 #pragma unroll
                 for (int x = 0; x < 64; ++x)
                     *reinterpret_cast<__nv_bfloat16 *>(ost + sw128_offset(x, vcol)) =
-                        __float2bfloat16_rn(a.scale * ov[x]);
+                        __float2bfloat16_rn(ov[x]);   // the output scale is folded into the Q tile
                 fence_proxy_async_smem();
                 named_bar_sync(2, 128);
                 if (et == 0) {
@@ -463,9 +474,9 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         __syncwarp();
     } else if (warp >= 8 && warp < 12) {
         // ------------------------------------------------------------ state (TMEM)
-        // After U(c-1) the TMEM state holds S_{c-1} + K~^T V (a normal chunk: exp(Bc) still
-        // to apply) or S_c already (an extreme chunk was scaled before its U). Pass c:
-        // finish S_c, snapshot it in bf16 for O(c), and pre-scale if chunk c is extreme.
+        // The TMEM state is decay-normalised: S_c = diag(exp(L_c)) S~_c. Pass c takes the
+        // bf16 snapshot of S~_c for O(c); a renormalising chunk first restores S~ = S_c,
+        // an extreme chunk also pre-scales by exp(Bc) before its U (its keys are K^).
         const int j = warp & 3;
         const int v = j * 32 + lane;
         const float *init = nullptr;
@@ -488,17 +499,17 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             if (c >= 2 && !mbar_wait(&bars[OFULL + (c & 1)], par(c / 2 - 1))) { ok = false; break; }
             if (v == 0) TRACE_OUT(8, c);
             tc_fence_after();
-            const bool post = c >= 1 && xf[(c - 1) & (NR - 1)] == 0;   // finish S_c
-            const bool pre = xf[c & (NR - 1)] != 0;                     // extreme chunk c
-            const float *gprev = gam_s + ((c - 1) & (NR - 1)) * 128;
-            const float *gcur = gam_s + (c & (NR - 1)) * 128;
+            const uint32_t fl = xf[c & (NR - 1)];
+            const bool ext = (fl & 1u) != 0, ren = (fl & 2u) != 0;
+            const float *gl = gam_s + (c & (NR - 1)) * 128;    // exp(L_c)
+            const float *gb = gam2_s + (c & (NR - 1)) * 128;   // exp(Bc)
 #pragma unroll 1
             for (int half = 0; half < 2; ++half) {
                 float sv[64];
                 tmem_ld64(tmem_addr(tm, j, kColS + half * 64), sv);
-                if (post) {
+                if (ren) {
 #pragma unroll
-                    for (int x = 0; x < 64; ++x) sv[x] *= gprev[half * 64 + x];
+                    for (int x = 0; x < 64; ++x) sv[x] *= gl[half * 64 + x];
                 }
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
@@ -508,11 +519,11 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                         pk[x] = pack_bf16(sv[16 * cc + 2 * x], sv[16 * cc + 2 * x + 1]);
                     tmem_st8(tmem_addr(tm, j, kColSB + (c & 1) * 64 + half * 32 + cc * 8), pk);
                 }
-                if (pre) {
+                if (ext) {
 #pragma unroll
-                    for (int x = 0; x < 64; ++x) sv[x] *= gcur[half * 64 + x];
+                    for (int x = 0; x < 64; ++x) sv[x] *= gb[half * 64 + x];
                 }
-                if (post || pre) {
+                if (ren) {
 #pragma unroll
                     for (int cc = 0; cc < 4; ++cc) {
                         uint32_t r[16];
@@ -533,8 +544,6 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 ok = false;
             } else {
                 tc_fence_after();
-                const bool post = xf[(n - 1) & (NR - 1)] == 0;
-                const float *gprev = gam_s + ((n - 1) & (NR - 1)) * 128;
                 float *hp = a.hT + (size_t)bh * (kD * kD) + v;
 #pragma unroll 1
                 for (int half = 0; half < 2; ++half) {
@@ -542,7 +551,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     tmem_ld64(tmem_addr(tm, j, kColS + half * 64), sv);
 #pragma unroll
                     for (int x = 0; x < 64; ++x)
-                        hp[(half * 64 + x) * kD] = post ? sv[x] * gprev[half * 64 + x] : sv[x];
+                        hp[(half * 64 + x) * kD] = sv[x] * ends_s[half * 64 + x];
                 }
             }
         }
@@ -555,7 +564,6 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         const int d = 2 * p;
         const uint32_t boxo = (uint32_t)(p >> 5) * 8192;
         const uint32_t col = (uint32_t)(d & 63);
-        const float lim = kExtreme * kLog2e;
         const int64_t rs = (int64_t)a.H * kD;               // row stride of g (elements)
         const float *gp = a.g + ((int64_t)bidx * a.T * a.H + h) * kD + d;
         // this thread's 16 gate rows of a chunk, loaded a chunk ahead
@@ -567,6 +575,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 gn[x] = (t0 + x < a.T) ? __ldg(reinterpret_cast<const float2 *>(gp + (t0 + x) * rs))
                                        : make_float2(0.f, 0.f);
         };
+        float L0 = 0.f, L1 = 0.f;   // log2 decay of the normalised state (S = 2^L S~)
         if (n > 0) load_g(0);
         for (int c = 0; c < n; ++c) {
             float b0[16], b1[16];   // cumulative log2-gates of this thread's tokens
@@ -580,7 +589,8 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             }
             if (c + 1 < n) load_g(c + 1);
             *reinterpret_cast<float2 *>(xch + qq * kD + d) = make_float2(a0, a1);
-            named_bar_sync(1, 256);
+            // exchange the quarter totals; decide a renormalisation from |L|
+            bool ren = named_bar_or(1, 256, fabsf(L0) > kRenorm2 || fabsf(L1) > kRenorm2);
             float o0 = 0.f, o1 = 0.f;
             for (int q2 = 0; q2 < qq; ++q2) {
                 const float2 t = *reinterpret_cast<const float2 *>(xch + q2 * kD + d);
@@ -594,34 +604,49 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 b1[x] += o1;
                 mx = fmaxf(mx, fmaxf(fabsf(b0[x]), fabsf(b1[x])));
             }
-            if (qq == 3) {   // chunk totals: Bc, and exp(Bc) for the state warps
+            if (qq == 3) {
                 bv_s[d] = b0[15];
                 bv_s[d + 1] = b1[15];
-                gam_s[(c & (NR - 1)) * 128 + d] = ex2(b0[15]);
-                gam_s[(c & (NR - 1)) * 128 + d + 1] = ex2(b1[15]);
             }
-            const bool extreme = named_bar_or(1, 256, mx > lim);
+            const bool ext = named_bar_or(1, 256, mx > kExtreme2);   // also publishes bv_s
+            ren = ren || ext;
+            const float B0 = bv_s[d], B1 = bv_s[d + 1];
+            const float Lc0 = L0, Lc1 = L1;
+            const float Lq0 = ren ? 0.f : L0, Lq1 = ren ? 0.f : L1;   // L used by this chunk
+            L0 = ext ? 0.f : Lq0 + B0;
+            L1 = ext ? 0.f : Lq1 + B1;
             const bool w = mbar_wait(&bars[QFULL + c % NQ], par(c / NQ));
             if (named_bar_or(1, 256, !w)) { ok = false; break; }
+            // ring entries of chunk c: written only now, after the stage of chunk c arrived
+            // (which required O(c - NQ) done, so pass c - NQ has read the slot)
+            if (qq == 0) {
+                gam_s[(c & (NR - 1)) * 128 + d] = ex2(Lc0);       // restores S~ -> S_c
+                gam_s[(c & (NR - 1)) * 128 + d + 1] = ex2(Lc1);
+                if (ext) {
+                    gam2_s[(c & (NR - 1)) * 128 + d] = ex2(B0);
+                    gam2_s[(c & (NR - 1)) * 128 + d + 1] = ex2(B1);
+                }
+                ends_s[d] = ex2(L0);
+                ends_s[d + 1] = ex2(L1);
+            }
             if (gt == 0) TRACE_OUT(1, c);
-            const float B0 = bv_s[d], B1 = bv_s[d + 1];
             uint8_t *base = sm + (c % NQ) * QSTAGE;
             uint8_t *qt = base + Q + boxo;
             uint8_t *kt = base + K + boxo;
+            const float sc = a.scale;
 #pragma unroll
             for (int x = 0; x < 16; ++x) {
                 const uint32_t off = sw128_offset(16 * qq + x, col);
                 const float2 qv = unpack_bf16(*reinterpret_cast<const uint32_t *>(qt + off));
                 const float2 kv = unpack_bf16(*reinterpret_cast<const uint32_t *>(kt + off));
+                // Q' = scale q 2^(b + L); K' = k 2^-(b + L), or K^ = k 2^(Bc - b) when extreme
                 *reinterpret_cast<uint32_t *>(qt + off) =
-                    pack_bf16(qv.x * ex2(b0[x]), qv.y * ex2(b1[x]));
-                // normal chunk: K~ = k exp(-b) (exp(Bc) is applied to the state after U);
-                // extreme chunk: K^ = k exp(Bc - b) (the state is scaled before U)
-                const float e0 = extreme ? B0 - b0[x] : -b0[x];
-                const float e1 = extreme ? B1 - b1[x] : -b1[x];
+                    pack_bf16(sc * qv.x * ex2(b0[x] + Lq0), sc * qv.y * ex2(b1[x] + Lq1));
+                const float e0 = ext ? B0 - b0[x] : -(b0[x] + Lq0);
+                const float e1 = ext ? B1 - b1[x] : -(b1[x] + Lq1);
                 *reinterpret_cast<uint32_t *>(kt + off) = pack_bf16(kv.x * ex2(e0), kv.y * ex2(e1));
             }
-            if (gt == 0) xf[c & (NR - 1)] = extreme ? 1u : 0u;
+            if (gt == 0) xf[c & (NR - 1)] = (ext ? 1u : 0u) | (ren ? 2u : 0u);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[GDONE + c % NQ]);

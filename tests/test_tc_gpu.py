@@ -97,6 +97,8 @@ def _extreme(x, kind):
         x["g"] = -5.0 * torch.rand_like(g)
     elif kind == "mixed":
         x["g"] = torch.where(torch.rand_like(g) < 0.02, torch.full_like(g, -200.0), g)
+    elif kind == "renorm":       # ~-23 log2 units per chunk: renormalisation every ~3 chunks
+        x["g"] = -0.5 * torch.rand_like(g)
     elif kind == "one_chunk_extreme":
         g[:, 64:128] = -3.0
         x["g"] = g
@@ -106,10 +108,10 @@ def _extreme(x, kind):
     return x
 
 
-@pytest.mark.parametrize("kind", ["forget", "no_decay", "tiny", "strong", "mixed",
+@pytest.mark.parametrize("kind", ["forget", "no_decay", "tiny", "strong", "mixed", "renorm",
                                   "one_chunk_extreme", "big_values"])
 def test_tc_extreme_gates(kind):
-    x = _extreme(_inputs(B=1, T=300, H=2, seed=3), kind)
+    x = _extreme(_inputs(B=1, T=700, H=2, seed=3), kind)
     o, hT = _run(x, seq_splits=2)
     assert torch.isfinite(o.float()).all() and torch.isfinite(hT).all()
     o_ref, h_ref = _oracle(x)
