@@ -146,10 +146,14 @@ gla_status library_workspace(DeviceState *st, size_t need, void **out) {
     return GLA_OK;
 }
 
+// AUTO: tensor cores for bf16 I/O, except sequences shorter than one 64-token chunk.
+// There each output is a handful of bf16-rounded dot products with no averaging, and the
+// exact fp32 kernel is both more accurate and as fast.
 int resolve_path(const gla_options *opt, const gla::Problem &p) {
     const int path = opt ? opt->path : GLA_PATH_AUTO;
     if (path != GLA_PATH_AUTO) return path;
-    return (p.io == GLA_IO_BF16 && gla::tc_supported(p)) ? GLA_PATH_TC : GLA_PATH_EXACT;
+    return (p.io == GLA_IO_BF16 && p.T >= 64 && gla::tc_supported(p)) ? GLA_PATH_TC
+                                                                       : GLA_PATH_EXACT;
 }
 
 }  // namespace
