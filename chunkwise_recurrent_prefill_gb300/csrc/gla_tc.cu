@@ -85,10 +85,12 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
 }
 
 // TMEM column map of the output kernel (512 columns).
-constexpr uint32_t kColS = 0;      // S^T fp32, 128 columns
-constexpr uint32_t kColSB = 128;   // S^T bf16 snapshot (A operand), 2 x 64 columns
-constexpr uint32_t kColP = 256;    // P fp32 (M=64 layout), 2 x 64 columns
-constexpr uint32_t kColO = 384;    // O^T fp32, 2 x 64 columns
+constexpr uint32_t kColS = 0;      // S~^T fp32, 128 columns
+constexpr uint32_t kColSB = 128;   // S~^T bf16 snapshot (A operand), 2 x 64 columns
+constexpr uint32_t kColP1 = 256;   // P over key dims 0..63 (M=64 layout), 64 columns
+constexpr uint32_t kColP2 = 320;   // P over key dims 64..127, 64 columns
+constexpr uint32_t kColOi = 384;   // O^T intra term, 64 columns
+constexpr uint32_t kColOs = 448;   // O^T inter term, 64 columns
 
 // Shared-memory map of the output kernel (bytes from a 1024-aligned base).
 //   q/k/v ring (4 stages): raw tiles as 128B-swizzled [64 x 64] bf16 boxes, two per tile;
@@ -110,15 +112,15 @@ constexpr uint32_t XCH = BV + 512;      // [4][128] f32 token-quarter totals
 constexpr uint32_t XF = XCH + 2048;     // [NR] u32 chunk flags: 1 = extreme, 2 = renormalise
 constexpr uint32_t SCR = XF + 64;       // [4][64] f32 exact-path scratch
 constexpr uint32_t BAR = SCR + 1024;    // mbarriers
-constexpr uint32_t NBAR = 24;
+constexpr uint32_t NBAR = 20;
 constexpr uint32_t TSLOT = BAR + NBAR * 8;
 constexpr uint32_t ALLOC = TSLOT + 16 + 1024;
 }  // namespace om
 
 // mbarrier indices of the output kernel
 enum {
-    QFULL = 0, QEMPTY = 4, GDONE = 8, PFULL = 12, PFREE = 14, PBF = 16, SREADY = 17,
-    UDONE = 18, OFULL = 19, OFREE = 21, FIN = 23,
+    QFULL = 0, QEMPTY = 4, GDONE = 8, PFULL = 12, PFREE = 13, PBF = 14, SREADY = 15,
+    UDONE = 16, OFULL = 17, OFREE = 18, FIN = 19,
 };
 
 constexpr int kOutThreads = 576;       // 18 warps
@@ -204,6 +206,8 @@ __device__ __forceinline__ void gate_cumsum(const float *gs, float *xch, int qq,
 __device__ __forceinline__ uint32_t par(int use) { return (uint32_t)use & 1u; }
 
 // ======================================================================= output kernel
+// Warp roles (18 warps): 0 TMA producer, 1 MMA scheduler (one thread), 2-3 and 12-17
+// gate warps, 4-7 epilogue, 8-11 state + P conversion.
 __global__ void __launch_bounds__(kOutThreads, 1)
 gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg,
@@ -234,15 +238,13 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             mbar_init(&bars[QEMPTY + i], 1);
             mbar_init(&bars[GDONE + i], 8);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&bars[PFULL + i], 1);
-            mbar_init(&bars[PFREE + i], 4);
-            mbar_init(&bars[OFULL + i], 1);
-            mbar_init(&bars[OFREE + i], 4);
-        }
+        mbar_init(&bars[PFULL], 1);
+        mbar_init(&bars[PFREE], 4);
         mbar_init(&bars[PBF], 4);
         mbar_init(&bars[SREADY], 4);
         mbar_init(&bars[UDONE], 1);
+        mbar_init(&bars[OFULL], 1);
+        mbar_init(&bars[OFREE], 4);
         mbar_init(&bars[FIN], 1);
         fence_mbar_init();
     }
@@ -290,66 +292,99 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA scheduler
-        // P(c): gates of c ready;  U(c): state snapshot of c taken;  O(c): P tile of c and
-        // U(c) issued. Issued in that order per chunk, interleaved across chunks as their
-        // inputs become ready (non-blocking polls).
+        // Three MMA groups per chunk c, started as their inputs become ready:
+        //   P(c): gates of c done, P(c-1) read      -> P1 (d 0..63) and P2 (d 64..127)
+        //   U(c): snapshot of S~_c taken            -> S~ += K'^T V
+        //   O(c): P tile of c written, O(c-1) read  -> Oi = V^T P^T, Os = S~_c^T Q'^T
+        // Accumulating into one TMEM tile serialises MMAs at their latency, so the active
+        // groups (and the two tiles inside P and O) are issued round-robin, one
+        // instruction per group per turn, to keep several independent chains in flight.
         if (lane == 0) {
             const uint32_t idP = idesc_bf16(64, 64, 0, 0);
             const uint32_t idU = idesc_bf16(128, 128, 1, 1);
             const uint32_t idOi = idesc_bf16(128, 64, 1, 0);
             const uint32_t idOs = idesc_bf16(128, 64, 0, 0);
-            int np = 0, nu = 0, no = 0;
+            int np = 0, nu = 0, no = 0;          // groups started
+            int ip = 8, iu = 4, io = 12;         // next instruction of the active group
+            int udone_n = 0, odone_n = 0, qe = 0;
             uint64_t t_last = global_ns();
-            while (no < n) {
+            while (qe < n) {
                 bool prog = false;
-                if (np < n && mbar_try_wait(&bars[GDONE + np % NQ], par(np / NQ)) &&
-                    (np < 2 || mbar_try_wait(&bars[PFREE + (np & 1)], par(np / 2 - 1)))) {
+                // ---- start groups whose inputs are ready
+                if (ip == 8 && np < n && mbar_try_wait(&bars[GDONE + np % NQ], par(np / NQ)) &&
+                    (np == 0 || mbar_try_wait(&bars[PFREE], par(np - 1)))) {
                     tc_fence_after();
                     TRACE_OUT(3, np);
-                    const uint32_t base = smem_u32(sm + (np % NQ) * QSTAGE);
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
-                        mma_ss(tm + kColP + (np & 1) * 64, smem_desc(base + Q + off, 16, 1024),
-                               smem_desc(base + K + off, 16, 1024), idP, kk > 0);
-                    }
-                    mma_commit(&bars[PFULL + (np & 1)]);
-                    TRACE_OUT(4, np);
+                    ip = 0;
                     ++np;
                     prog = true;
                 }
-                if (nu < np && mbar_try_wait(&bars[SREADY], par(nu))) {
+                if (iu == 4 && nu < np && mbar_try_wait(&bars[SREADY], par(nu))) {
                     tc_fence_after();
                     TRACE_OUT(5, nu);
-                    const uint32_t base = smem_u32(sm + (nu % NQ) * QSTAGE);
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_ss(tm + kColS, smem_desc(base + V + kk * 2048, 8192, 1024),
-                               smem_desc(base + K + kk * 2048, 8192, 1024), idU, 1);
-                    mma_commit(&bars[UDONE]);
+                    iu = 0;
                     ++nu;
                     prog = true;
                 }
-                if (no < nu && mbar_try_wait(&bars[PBF], par(no)) &&
-                    (no < 2 || mbar_try_wait(&bars[OFREE + (no & 1)], par(no / 2 - 1)))) {
+                if (io == 12 && no < nu && mbar_try_wait(&bars[PBF], par(no)) &&
+                    (no == 0 || mbar_try_wait(&bars[OFREE], par(no - 1)))) {
                     tc_fence_after();
                     TRACE_OUT(6, no);
-                    const uint32_t base = smem_u32(sm + (no % NQ) * QSTAGE);
-                    const uint32_t pbase = smem_u32(sm + P);
-                    const uint32_t od = tm + kColO + (no & 1) * 64;
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_ss(od, smem_desc(base + V + kk * 2048, 8192, 1024),
-                               smem_desc(pbase + kk * 32, 16, 1024), idOi, kk > 0);
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_ts(od, tm + kColSB + (no & 1) * 64 + kk * 8,
-                               smem_desc(base + Q + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
-                               idOs, 1);
-                    mma_commit(&bars[OFULL + (no & 1)]);
-                    mma_commit(&bars[QEMPTY + no % NQ]);   // P, U and O of chunk no read it
-                    TRACE_OUT(7, no);
+                    io = 0;
                     ++no;
+                    prog = true;
+                }
+                // ---- one instruction from each active group
+                if (ip < 8) {
+                    const int c = np - 1;
+                    const uint32_t base = smem_u32(sm + (c % NQ) * QSTAGE);
+                    const int half = ip & 1, kk = ip >> 1;   // alternate the two P tiles
+                    const uint32_t off = half * 8192 + kk * 32;
+                    mma_ss(tm + (half ? kColP2 : kColP1), smem_desc(base + Q + off, 16, 1024),
+                           smem_desc(base + K + off, 16, 1024), idP, kk > 0);
+                    if (++ip == 8) {
+                        mma_commit(&bars[PFULL]);
+                        TRACE_OUT(4, c);
+                    }
+                    prog = true;
+                }
+                if (iu < 4) {
+                    const int c = nu - 1;
+                    const uint32_t base = smem_u32(sm + (c % NQ) * QSTAGE);
+                    mma_ss(tm + kColS, smem_desc(base + V + iu * 2048, 8192, 1024),
+                           smem_desc(base + K + iu * 2048, 8192, 1024), idU, 1);
+                    if (++iu == 4) {
+                        mma_commit(&bars[UDONE]);
+                        ++udone_n;
+                    }
+                    prog = true;
+                }
+                if (io < 12) {
+                    const int c = no - 1;
+                    const uint32_t base = smem_u32(sm + (c % NQ) * QSTAGE);
+                    // Os k0, Oi k0, Os k1, Oi k1, ..., Os k3, Oi k3, Os k4 .. Os k7
+                    const bool intra = io < 8 && (io & 1);
+                    if (intra) {
+                        const int kk = io >> 1;
+                        mma_ss(tm + kColOi, smem_desc(base + V + kk * 2048, 8192, 1024),
+                               smem_desc(smem_u32(sm + P) + kk * 32, 16, 1024), idOi, kk > 0);
+                    } else {
+                        const int kk = io < 8 ? io >> 1 : io - 4;
+                        mma_ts(tm + kColOs, tm + kColSB + (c & 1) * 64 + kk * 8,
+                               smem_desc(base + Q + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
+                               idOs, kk > 0);
+                    }
+                    if (++io == 12) {
+                        mma_commit(&bars[OFULL]);
+                        ++odone_n;
+                        TRACE_OUT(7, c);
+                    }
+                    prog = true;
+                }
+                // ---- a stage is free once P, U and O of its chunk have all been issued
+                if (qe < udone_n && qe < odone_n) {
+                    mma_commit(&bars[QEMPTY + qe % NQ]);
+                    ++qe;
                     prog = true;
                 }
                 if (prog) {
@@ -365,120 +400,78 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         }
         __syncwarp();
     } else if (warp >= 4 && warp < 8) {
-        // ------------------------------------------------------------ P conversion + epilogue
+        // ------------------------------------------------------------ epilogue
         const int j = warp & 3;
         const int et = (warp - 4) * 32 + lane;      // 0..127
         const int v = j * 32 + lane;                // O^T lane = value column
-        float *scr = reinterpret_cast<float *>(sm + SCR);
         uint8_t *ost = sm + OST + (uint32_t)(v >> 6) * 8192;
         const uint32_t vcol = (uint32_t)(v & 63);
-        for (int c = 0; c <= n && ok; ++c) {
-            if (c < n) {
-                bool w = mbar_wait(&bars[GDONE + c % NQ], par(c / NQ)) &&
-                         mbar_wait(&bars[PFULL + (c & 1)], par(c / 2)) &&
-                         (c == 0 || mbar_wait(&bars[OFULL + ((c - 1) & 1)], par((c - 1) / 2)));
-                if (named_bar_or(2, 128, !w)) { ok = false; break; }
-                if (et == 0) TRACE_OUT(10, c);
-                tc_fence_after();
-                const bool extreme = (xf[c & (NR - 1)] & 1u) != 0;
-                float prow[64];
-                const int i = 16 * j + lane;        // P row held by this lane (lane < 16)
-                if (!extreme) {
-                    tmem_ld64(tmem_addr(tm, j, kColP + (c & 1) * 64), prow);
-                } else {
-                    // exact route: P_ij = sum_d q_id k_jd exp(b_id - b_jd), j <= i
+        for (int c = 0; c < n; ++c) {
+            const bool w = mbar_wait(&bars[OFULL], par(c));
+            if (named_bar_or(2, 128, !w)) { ok = false; break; }
+            if (et == 0) TRACE_OUT(12, c);
+            tc_fence_after();
+            float o0[32], o1[32];
+            {
+                uint32_t r0[16], r1[16], r2[16], r3[16];
+                tmem_ld16(tmem_addr(tm, j, kColOi), r0);
+                tmem_ld16(tmem_addr(tm, j, kColOi + 16), r1);
+                tmem_ld16(tmem_addr(tm, j, kColOs), r2);
+                tmem_ld16(tmem_addr(tm, j, kColOs + 16), r3);
+                tmem_wait_ld();
+                reg_fence(r0); reg_fence(r1); reg_fence(r2); reg_fence(r3);
 #pragma unroll
-                    for (int x = 0; x < 64; ++x) prow[x] = 0.f;
-                    float *gcol = scr, *qcol = scr + 64, *kcol = scr + 128, *bcol = scr + 192;
-                    const int64_t t0 = (int64_t)(cb + c) * kC;
-                    for (int d = 0; d < kD; ++d) {
-                        if (et < 64) {
-                            const int64_t t = t0 + et;
-                            const bool in = t < a.T;
-                            const int64_t idx = (((int64_t)bidx * a.T + t) * a.H + h) * kD + d;
-                            gcol[et] = in ? a.g[idx] : 0.f;
-                            qcol[et] = in ? __bfloat162float(a.q[idx]) : 0.f;
-                            kcol[et] = in ? __bfloat162float(a.k[idx]) : 0.f;
-                        }
-                        named_bar_sync(2, 128);
-                        if (et == 0) {
-                            float s = 0.f;
-                            for (int t = 0; t < 64; ++t) { s += gcol[t]; bcol[t] = s; }
-                        }
-                        named_bar_sync(2, 128);
-                        if (lane < 16) {
-                            const float qi = a.scale * qcol[i], bi = bcol[i];
-#pragma unroll
-                            for (int x = 0; x < 64; ++x)
-                                if (x <= i) prow[x] += qi * kcol[x] * ex2((bi - bcol[x]) * kLog2e);
-                        }
-                        named_bar_sync(2, 128);
-                    }
+                for (int x = 0; x < 16; ++x) {
+                    o0[x] = __uint_as_float(r0[x]) + __uint_as_float(r2[x]);
+                    o0[16 + x] = __uint_as_float(r1[x]) + __uint_as_float(r3[x]);
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[PFREE + (c & 1)]);
-                if (lane < 16) {
-                    uint8_t *pt = sm + P;
+                tmem_ld16(tmem_addr(tm, j, kColOi + 32), r0);
+                tmem_ld16(tmem_addr(tm, j, kColOi + 48), r1);
+                tmem_ld16(tmem_addr(tm, j, kColOs + 32), r2);
+                tmem_ld16(tmem_addr(tm, j, kColOs + 48), r3);
+                tmem_wait_ld();
+                reg_fence(r0); reg_fence(r1); reg_fence(r2); reg_fence(r3);
 #pragma unroll
-                    for (int cc = 0; cc < 8; ++cc) {
-                        uint32_t wv[4];
-#pragma unroll
-                        for (int x = 0; x < 4; ++x) {
-                            const int col = cc * 8 + 2 * x;
-                            wv[x] = pack_bf16(col <= i ? prow[col] : 0.f,
-                                              col + 1 <= i ? prow[col + 1] : 0.f);
-                        }
-                        *reinterpret_cast<uint4 *>(pt + sw128_offset(i, cc * 8)) =
-                            make_uint4(wv[0], wv[1], wv[2], wv[3]);
-                    }
+                for (int x = 0; x < 16; ++x) {
+                    o1[x] = __uint_as_float(r0[x]) + __uint_as_float(r2[x]);
+                    o1[16 + x] = __uint_as_float(r1[x]) + __uint_as_float(r3[x]);
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[PBF]);
-                if (et == 0) TRACE_OUT(11, c);
             }
-            if (c >= 1) {
-                // epilogue of chunk c-1 (its O is complete: waited above, or here at the end)
-                const int pc = c - 1;
-                if (c == n) {
-                    const bool w = mbar_wait(&bars[OFULL + (pc & 1)], par(pc / 2));
-                    if (named_bar_or(2, 128, !w)) { ok = false; break; }
-                }
-                if (et == 0) TRACE_OUT(12, pc);
-                tc_fence_after();
-                float ov[64];
-                tmem_ld64(tmem_addr(tm, j, kColO + (pc & 1) * 64), ov);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[OFREE + (pc & 1)]);
-                // stage O (bf16, 128B-swizzled boxes) once the previous store has read it
-                if (et == 0) bulk_wait_read_all();
-                named_bar_sync(2, 128);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[OFREE]);
+            // stage O (bf16, 128B-swizzled boxes) once the previous store has read it
+            if (et == 0) bulk_wait_read_all();
+            named_bar_sync(2, 128);
 #pragma unroll
-                for (int x = 0; x < 64; ++x)
-                    *reinterpret_cast<__nv_bfloat16 *>(ost + sw128_offset(x, vcol)) =
-                        __float2bfloat16_rn(ov[x]);   // the output scale is folded into the Q tile
-                fence_proxy_async_smem();
-                named_bar_sync(2, 128);
-                if (et == 0) {
-                    const int t0 = (cb + pc) * kC;
-                    tma_store_4d(&to, sm + OST, 0, h, t0, bidx);
-                    tma_store_4d(&to, sm + OST + 8192, 64, h, t0, bidx);
-                    bulk_commit();
-                    TRACE_OUT(13, pc);
-                }
+            for (int x = 0; x < 32; ++x) {
+                *reinterpret_cast<__nv_bfloat16 *>(ost + sw128_offset(x, vcol)) =
+                    __float2bfloat16_rn(o0[x]);   // the output scale is folded into the Q tile
+                *reinterpret_cast<__nv_bfloat16 *>(ost + sw128_offset(32 + x, vcol)) =
+                    __float2bfloat16_rn(o1[x]);
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(2, 128);
+            if (et == 0) {
+                const int t0 = (cb + c) * kC;
+                tma_store_4d(&to, sm + OST, 0, h, t0, bidx);
+                tma_store_4d(&to, sm + OST + 8192, 64, h, t0, bidx);
+                bulk_commit();
+                TRACE_OUT(13, c);
             }
         }
         if (et == 0) bulk_wait_all();
         __syncwarp();
     } else if (warp >= 8 && warp < 12) {
-        // ------------------------------------------------------------ state (TMEM)
+        // ------------------------------------------------------------ state + P conversion
         // The TMEM state is decay-normalised: S_c = diag(exp(L_c)) S~_c. Pass c takes the
-        // bf16 snapshot of S~_c for O(c); a renormalising chunk first restores S~ = S_c,
-        // an extreme chunk also pre-scales by exp(Bc) before its U (its keys are K^).
+        // bf16 snapshot of S~_c for O(c) (a renormalising chunk first restores S~ = S_c, an
+        // extreme chunk also pre-scales by exp(Bc) before its U), then turns P(c) into the
+        // masked bf16 P tile.
         const int j = warp & 3;
         const int v = j * 32 + lane;
+        const int st_t = (warp - 8) * 32 + lane;     // 0..127
+        float *scr = reinterpret_cast<float *>(sm + SCR);
         const float *init = nullptr;
         if (seg > 0)
             init = a.sstart + ((size_t)bh * (a.splits - 1) + (seg - 1)) * (kD * kD);
@@ -494,9 +487,10 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         }
         tmem_wait_st();
         for (int c = 0; c < n; ++c) {
-            if (c >= 1 && !mbar_wait(&bars[UDONE], par(c - 1))) { ok = false; break; }
-            if (!mbar_wait(&bars[GDONE + c % NQ], par(c / NQ))) { ok = false; break; }
-            if (c >= 2 && !mbar_wait(&bars[OFULL + (c & 1)], par(c / 2 - 1))) { ok = false; break; }
+            // ---- snapshot of S~_c
+            bool w = (c == 0 || mbar_wait(&bars[UDONE], par(c - 1))) &&
+                     mbar_wait(&bars[GDONE + c % NQ], par(c / NQ));
+            if (named_bar_or(3, 128, !w)) { ok = false; break; }
             if (v == 0) TRACE_OUT(8, c);
             tc_fence_after();
             const uint32_t fl = xf[c & (NR - 1)];
@@ -538,6 +532,78 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[SREADY]);
             if (v == 0) TRACE_OUT(9, c);
+            // ---- P(c) -> masked bf16 P tile (the tile is free once O(c-1) completed)
+            w = mbar_wait(&bars[PFULL], par(c)) && (c == 0 || mbar_wait(&bars[OFULL], par(c - 1)));
+            if (named_bar_or(3, 128, !w)) { ok = false; break; }
+            if (v == 0) TRACE_OUT(10, c);
+            tc_fence_after();
+            float prow[64];
+            const int i = 16 * j + lane;        // P row held by this lane (lane < 16)
+            if (!ext) {
+                uint32_t r0[16], r1[16];
+#pragma unroll
+                for (int c0 = 0; c0 < 64; c0 += 16) {
+                    tmem_ld16(tmem_addr(tm, j, kColP1 + c0), r0);
+                    tmem_ld16(tmem_addr(tm, j, kColP2 + c0), r1);
+                    tmem_wait_ld();
+                    reg_fence(r0);
+                    reg_fence(r1);
+#pragma unroll
+                    for (int x = 0; x < 16; ++x)
+                        prow[c0 + x] = __uint_as_float(r0[x]) + __uint_as_float(r1[x]);
+                }
+            } else {
+                // exact route: P_ij = scale sum_d q_id k_jd exp(b_id - b_jd), j <= i
+#pragma unroll
+                for (int x = 0; x < 64; ++x) prow[x] = 0.f;
+                float *gcol = scr, *qcol = scr + 64, *kcol = scr + 128, *bcol = scr + 192;
+                const int64_t t0 = (int64_t)(cb + c) * kC;
+                for (int d = 0; d < kD; ++d) {
+                    if (st_t < 64) {
+                        const int64_t t = t0 + st_t;
+                        const bool in = t < a.T;
+                        const int64_t idx = (((int64_t)bidx * a.T + t) * a.H + h) * kD + d;
+                        gcol[st_t] = in ? a.g[idx] : 0.f;
+                        qcol[st_t] = in ? __bfloat162float(a.q[idx]) : 0.f;
+                        kcol[st_t] = in ? __bfloat162float(a.k[idx]) : 0.f;
+                    }
+                    named_bar_sync(3, 128);
+                    if (st_t == 0) {
+                        float s = 0.f;
+                        for (int t = 0; t < 64; ++t) { s += gcol[t]; bcol[t] = s; }
+                    }
+                    named_bar_sync(3, 128);
+                    if (lane < 16) {
+                        const float qi = a.scale * qcol[i], bi = bcol[i];
+#pragma unroll
+                        for (int x = 0; x < 64; ++x)
+                            if (x <= i) prow[x] += qi * kcol[x] * ex2((bi - bcol[x]) * kLog2e);
+                    }
+                    named_bar_sync(3, 128);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[PFREE]);
+            if (lane < 16) {
+                uint8_t *pt = sm + P;
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc) {
+                    uint32_t wv[4];
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) {
+                        const int col = cc * 8 + 2 * x;
+                        wv[x] = pack_bf16(col <= i ? prow[col] : 0.f,
+                                          col + 1 <= i ? prow[col + 1] : 0.f);
+                    }
+                    *reinterpret_cast<uint4 *>(pt + sw128_offset(i, cc * 8)) =
+                        make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[PBF]);
+            if (v == 0) TRACE_OUT(11, c);
         }
         if (ok && a.hT && seg == a.splits - 1) {
             if (!mbar_wait(&bars[UDONE], par(n - 1))) {
