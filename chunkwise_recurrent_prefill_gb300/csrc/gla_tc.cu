@@ -311,23 +311,23 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             while (qe < n) {
                 bool prog = false;
                 // ---- start groups whose inputs are ready
-                if (ip == 8 && np < n && mbar_try_wait(&bars[GDONE + np % NQ], par(np / NQ)) &&
-                    (np == 0 || mbar_try_wait(&bars[PFREE], par(np - 1)))) {
+                if (ip == 8 && np < n && mbar_test(&bars[GDONE + np % NQ], par(np / NQ)) &&
+                    (np == 0 || mbar_test(&bars[PFREE], par(np - 1)))) {
                     tc_fence_after();
                     TRACE_OUT(3, np);
                     ip = 0;
                     ++np;
                     prog = true;
                 }
-                if (iu == 4 && nu < np && mbar_try_wait(&bars[SREADY], par(nu))) {
+                if (iu == 4 && nu < np && mbar_test(&bars[SREADY], par(nu))) {
                     tc_fence_after();
                     TRACE_OUT(5, nu);
                     iu = 0;
                     ++nu;
                     prog = true;
                 }
-                if (io == 12 && no < nu && mbar_try_wait(&bars[PBF], par(no)) &&
-                    (no == 0 || mbar_try_wait(&bars[OFREE], par(no - 1)))) {
+                if (io == 12 && no < nu && mbar_test(&bars[PBF], par(no)) &&
+                    (no == 0 || mbar_test(&bars[OFREE], par(no - 1)))) {
                     tc_fence_after();
                     TRACE_OUT(6, no);
                     io = 0;
@@ -803,7 +803,7 @@ gla_tc_state_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
             uint64_t t_last = global_ns();
             while (ng < n || nk < n) {
                 bool prog = false;
-                if (ng < n && (ng < NG || mbar_try_wait(&bars[SGEMPTY + ng % NG], par(ng / NG - 1)))) {
+                if (ng < n && (ng < NG || mbar_test(&bars[SGEMPTY + ng % NG], par(ng / NG - 1)))) {
                     uint64_t *fb = &bars[SGFULL + ng % NG];
                     TRACE_ST(0, ng);
                     mbar_arrive_expect_tx(fb, 32768);
@@ -811,7 +811,7 @@ gla_tc_state_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
                     ++ng;
                     prog = true;
                 }
-                if (nk < n && (nk < NKV || mbar_try_wait(&bars[SKEMPTY + nk % NKV], par(nk / NKV - 1)))) {
+                if (nk < n && (nk < NKV || mbar_test(&bars[SKEMPTY + nk % NKV], par(nk / NKV - 1)))) {
                     uint8_t *base = sm + (nk % NKV) * KVSTAGE;
                     uint64_t *fb = &bars[SKFULL + nk % NKV];
                     mbar_arrive_expect_tx(fb, 2 * 16384);
