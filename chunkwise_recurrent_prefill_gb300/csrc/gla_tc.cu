@@ -307,7 +307,8 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             int np = 0, nu = 0, no = 0;          // groups started
             int ip = 8, iu = 4, io = 12;         // next instruction of the active group
             int udone_n = 0, odone_n = 0, qe = 0;
-            uint64_t t_last = global_ns();
+            uint32_t idle = 0;
+            uint64_t t_idle = 0;
             while (qe < n) {
                 bool prog = false;
                 // ---- start groups whose inputs are ready
@@ -388,8 +389,10 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     prog = true;
                 }
                 if (prog) {
-                    t_last = global_ns();
-                } else if (global_ns() - t_last > kWaitLimitNs) {
+                    idle = 0;
+                } else if (++idle == 256) {
+                    t_idle = global_ns();   // the timer is read only on long idle streaks
+                } else if ((idle & 1023) == 0 && global_ns() - t_idle > kWaitLimitNs) {
                     ok = false;
                     break;
                 }
@@ -800,7 +803,8 @@ gla_tc_state_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
     if (warp == 0) {
         if (lane == 0) {
             int ng = 0, nk = 0;
-            uint64_t t_last = global_ns();
+            uint32_t idle = 0;
+            uint64_t t_idle = 0;
             while (ng < n || nk < n) {
                 bool prog = false;
                 if (ng < n && (ng < NG || mbar_test(&bars[SGEMPTY + ng % NG], par(ng / NG - 1)))) {
@@ -824,8 +828,10 @@ gla_tc_state_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
                     prog = true;
                 }
                 if (prog) {
-                    t_last = global_ns();
-                } else if (global_ns() - t_last > kWaitLimitNs) {
+                    idle = 0;
+                } else if (++idle == 256) {
+                    t_idle = global_ns();   // the timer is read only on long idle streaks
+                } else if ((idle & 1023) == 0 && global_ns() - t_idle > kWaitLimitNs) {
                     ok = false;
                     break;
                 }
