@@ -292,100 +292,70 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA scheduler
-        // Three MMA groups per chunk c, started as their inputs become ready:
-        //   P(c): gates of c done, P(c-1) read      -> P1 (d 0..63) and P2 (d 64..127)
-        //   U(c): snapshot of S~_c taken            -> S~ += K'^T V
-        //   O(c): P tile of c written, O(c-1) read  -> Oi = V^T P^T, Os = S~_c^T Q'^T
-        // Accumulating into one TMEM tile serialises MMAs at their latency, so the active
-        // groups (and the two tiles inside P and O) are issued round-robin, one
-        // instruction per group per turn, to keep several independent chains in flight.
+        // Three MMA groups per chunk c, each issued back to back once its inputs are ready:
+        //   U(c): snapshot of S~_c taken            -> S~ += K'^T V                (4 steps)
+        //   P(c): gates of c done, P(c-1) read      -> P1 (d 0..63), P2 (d 64..127) (2 x 4)
+        //   O(c): P tile of c written, O(c-1) read  -> Oi = V^T P^T (4), Os = S~^T Q'^T (8)
+        // MMAs that accumulate into TMEM run at their latency, one after another, so the
+        // order only decides who waits: U first (the state chain), then P, then O.
         if (lane == 0) {
             const uint32_t idP = idesc_bf16(64, 64, 0, 0);
             const uint32_t idU = idesc_bf16(128, 128, 1, 1);
             const uint32_t idOi = idesc_bf16(128, 64, 1, 0);
             const uint32_t idOs = idesc_bf16(128, 64, 0, 0);
-            int np = 0, nu = 0, no = 0;          // groups started
-            int ip = 8, iu = 4, io = 12;         // next instruction of the active group
-            int udone_n = 0, odone_n = 0, qe = 0;
+            int np = 0, nu = 0, no = 0;
             uint32_t idle = 0;
             uint64_t t_idle = 0;
-            while (qe < n) {
+            while (no < n) {
                 bool prog = false;
-                // ---- start groups whose inputs are ready
-                if (ip == 8 && np < n && mbar_test(&bars[GDONE + np % NQ], par(np / NQ)) &&
-                    (np == 0 || mbar_test(&bars[PFREE], par(np - 1)))) {
-                    tc_fence_after();
-                    TRACE_OUT(3, np);
-                    ip = 0;
-                    ++np;
-                    prog = true;
-                }
-                if (iu == 4 && nu < np && mbar_test(&bars[SREADY], par(nu))) {
+                if (nu < np && mbar_test(&bars[SREADY], par(nu))) {
                     tc_fence_after();
                     TRACE_OUT(5, nu);
-                    iu = 0;
+                    const uint32_t base = smem_u32(sm + (nu % NQ) * QSTAGE);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_ss(tm + kColS, smem_desc(base + V + kk * 2048, 8192, 1024),
+                               smem_desc(base + K + kk * 2048, 8192, 1024), idU, 1);
+                    mma_commit(&bars[UDONE]);
                     ++nu;
                     prog = true;
                 }
-                if (io == 12 && no < nu && mbar_test(&bars[PBF], par(no)) &&
+                if (np < n && mbar_test(&bars[GDONE + np % NQ], par(np / NQ)) &&
+                    (np == 0 || mbar_test(&bars[PFREE], par(np - 1)))) {
+                    tc_fence_after();
+                    TRACE_OUT(3, np);
+                    const uint32_t base = smem_u32(sm + (np % NQ) * QSTAGE);
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) {
+                        const int half = x & 1, kk = x >> 1;   // the two P tiles alternate
+                        const uint32_t off = half * 8192 + kk * 32;
+                        mma_ss(tm + (half ? kColP2 : kColP1), smem_desc(base + Q + off, 16, 1024),
+                               smem_desc(base + K + off, 16, 1024), idP, kk > 0);
+                    }
+                    mma_commit(&bars[PFULL]);
+                    TRACE_OUT(4, np);
+                    ++np;
+                    prog = true;
+                }
+                if (no < nu && mbar_test(&bars[PBF], par(no)) &&
                     (no == 0 || mbar_test(&bars[OFREE], par(no - 1)))) {
                     tc_fence_after();
                     TRACE_OUT(6, no);
-                    io = 0;
-                    ++no;
-                    prog = true;
-                }
-                // ---- one instruction from each active group
-                if (ip < 8) {
-                    const int c = np - 1;
-                    const uint32_t base = smem_u32(sm + (c % NQ) * QSTAGE);
-                    const int half = ip & 1, kk = ip >> 1;   // alternate the two P tiles
-                    const uint32_t off = half * 8192 + kk * 32;
-                    mma_ss(tm + (half ? kColP2 : kColP1), smem_desc(base + Q + off, 16, 1024),
-                           smem_desc(base + K + off, 16, 1024), idP, kk > 0);
-                    if (++ip == 8) {
-                        mma_commit(&bars[PFULL]);
-                        TRACE_OUT(4, c);
-                    }
-                    prog = true;
-                }
-                if (iu < 4) {
-                    const int c = nu - 1;
-                    const uint32_t base = smem_u32(sm + (c % NQ) * QSTAGE);
-                    mma_ss(tm + kColS, smem_desc(base + V + iu * 2048, 8192, 1024),
-                           smem_desc(base + K + iu * 2048, 8192, 1024), idU, 1);
-                    if (++iu == 4) {
-                        mma_commit(&bars[UDONE]);
-                        ++udone_n;
-                    }
-                    prog = true;
-                }
-                if (io < 12) {
-                    const int c = no - 1;
-                    const uint32_t base = smem_u32(sm + (c % NQ) * QSTAGE);
-                    // Os k0, Oi k0, Os k1, Oi k1, ..., Os k3, Oi k3, Os k4 .. Os k7
-                    const bool intra = io < 8 && (io & 1);
-                    if (intra) {
-                        const int kk = io >> 1;
-                        mma_ss(tm + kColOi, smem_desc(base + V + kk * 2048, 8192, 1024),
-                               smem_desc(smem_u32(sm + P) + kk * 32, 16, 1024), idOi, kk > 0);
-                    } else {
-                        const int kk = io < 8 ? io >> 1 : io - 4;
-                        mma_ts(tm + kColOs, tm + kColSB + (c & 1) * 64 + kk * 8,
+                    const uint32_t base = smem_u32(sm + (no % NQ) * QSTAGE);
+                    const uint32_t pbase = smem_u32(sm + P);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        mma_ts(tm + kColOs, tm + kColSB + (no & 1) * 64 + kk * 8,
                                smem_desc(base + Q + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
                                idOs, kk > 0);
+                        if (kk < 4)
+                            mma_ss(tm + kColOi, smem_desc(base + V + kk * 2048, 8192, 1024),
+                                   smem_desc(pbase + kk * 32, 16, 1024), idOi, kk > 0);
                     }
-                    if (++io == 12) {
-                        mma_commit(&bars[OFULL]);
-                        ++odone_n;
-                        TRACE_OUT(7, c);
-                    }
-                    prog = true;
-                }
-                // ---- a stage is free once P, U and O of its chunk have all been issued
-                if (qe < udone_n && qe < odone_n) {
-                    mma_commit(&bars[QEMPTY + qe % NQ]);
-                    ++qe;
+                    mma_commit(&bars[OFULL]);
+                    mma_commit(&bars[QEMPTY + no % NQ]);   // U(no) was issued before O(no)
+                    TRACE_OUT(7, no);
+                    ++no;
                     prog = true;
                 }
                 if (prog) {
