@@ -6,6 +6,7 @@ The compute runs in ``_build/libgla.so`` (CUDA kernels behind the C ABI of
 from .gla import (  # noqa: F401
     GLAError,
     gla_fwd,
+    gla_fwd_noalloc,
     last_device_status,
     load_library,
     workspace_size,

@@ -160,6 +160,7 @@ int resolve_path(const gla_options *opt, const gla::Problem &p) {
 
 namespace gla {
 void count_launches(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+void set_error_detail(const char *text) { snprintf(g_detail, sizeof(g_detail), "%s", text); }
 }  // namespace gla
 
 extern "C" {

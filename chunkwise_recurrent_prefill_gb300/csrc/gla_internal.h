@@ -28,6 +28,9 @@ enum : unsigned int {
 // Host-side count of kernel launches issued by the library (gla_launch_counter).
 void count_launches(unsigned n);
 
+// Sets the text gla_last_error_detail() returns on this host thread.
+void set_error_detail(const char *text);
+
 // Exact fp32 CUDA-core chunkwise kernel (any io, Dk/Dv in {64,128}).
 bool exact_supported(int64_t Dk, int64_t Dv);
 cudaError_t launch_exact(const Problem &p, unsigned int *dev_err, cudaStream_t s);

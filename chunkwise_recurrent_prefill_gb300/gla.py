@@ -59,6 +59,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.gla_fwd_ex.argtypes = sig + [ctypes.c_int, ctypes.POINTER(_Options), vp]
             for f in (lib.gla_fwd, lib.gla_fwd_f32, lib.gla_fwd_ex):
                 f.restype = ctypes.c_int
+            lib.gla_fwd_noalloc.argtypes = sig + [ctypes.c_int, vp]
+            lib.gla_fwd_noalloc.restype = ctypes.c_int
             lib.gla_fwd_workspace_size.argtypes = [i64, i64, i64, i64, i64, ctypes.c_int,
                                                    ctypes.POINTER(_Options)]
             lib.gla_fwd_workspace_size.restype = ctypes.c_size_t
@@ -166,6 +168,37 @@ def gla_fwd(q, k, v, g, scale: float, h0=None, *, o=None, hT=None, return_state:
     if rc != GLA_OK:
         detail = lib.gla_last_error_detail().decode() if rc in (6, 9) else ""
         raise GLAError(rc, "gla_fwd_ex", detail)
+    return o, hT
+
+
+def gla_fwd_noalloc(q, k, v, g, scale: float, h0=None, *, o, hT=None, seq_splits: int = 0,
+                    stream=None):
+    """GLA prefill forward through ``gla_fwd_noalloc``: bf16 q, k, v, o; the library takes
+    its scratch from a fixed array compiled into it and allocates no device memory. The
+    caller passes the outputs (``o`` and, optionally, ``hT``) already allocated. Calls that
+    overlap on the GPU share that array and race; keep them on one stream. Returns (o, hT).
+    """
+    lib = load_library()
+    B, T, H, Dk = q.shape
+    Dv = v.shape[-1]
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("tensors must be on a CUDA device")
+    for t, name, shape in ((q, "q", (B, T, H, Dk)), (k, "k", (B, T, H, Dk)),
+                           (v, "v", (B, T, H, Dv)), (o, "o", (B, T, H, Dv))):
+        _check(t, name, torch.bfloat16, shape, dev)
+    _check(g, "g", torch.float32, (B, T, H, Dk), dev)
+    if h0 is not None:
+        _check(h0, "h0", torch.float32, (B, H, Dk, Dv), dev)
+    if hT is not None:
+        _check(hT, "hT", torch.float32, (B, H, Dk, Dv), dev)
+    with torch.cuda.device(dev):
+        rc = lib.gla_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), ctypes.c_float(scale),
+                                 _ptr(h0), _ptr(o), _ptr(hT), B, T, H, Dk, Dv, int(seq_splits),
+                                 _stream_handle(stream))
+    if rc != GLA_OK:
+        detail = lib.gla_last_error_detail().decode() if rc in (6, 9) else ""
+        raise GLAError(rc, "gla_fwd_noalloc", detail)
     return o, hT
 
 

@@ -137,6 +137,40 @@ const char *gla_status_string(gla_status s);
  * the library's kernels ran inside a timed region. */
 uint64_t gla_launch_counter(void);
 
+/* Size in bytes of the fixed scratch array behind gla_fwd_noalloc (16 MiB). */
+#define GLA_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+
+/*
+ * gla_fwd_noalloc — gla_fwd (bf16 q, k, v, o; same arguments, same path choice, same
+ * results) that never allocates device memory. The method itself has no counterpart to
+ * this entry point; it serves callers that cannot call cudaMalloc: a host that has handed
+ * all device memory to its own pool or arena and must account for every byte, and code
+ * on a latency-critical path where the library's own workspace growth (cudaFree followed
+ * by cudaMalloc, which synchronises the whole device) would stall other streams.
+ *
+ * Scratch: the tensor-core path's sequence split needs B*H*(splits-1)*131584 bytes of
+ * scratch. This entry point takes it from one array of GLA_NOALLOC_SCRATCH_BYTES compiled
+ * into the library, which every GPU that runs this entry point holds until the process
+ * exits. seq_splits = 0 picks the split automatically, capped at the largest count whose
+ * scratch fits; seq_splits > 0 whose scratch does not fit returns GLA_ERR_WORKSPACE
+ * (gla_last_error_detail() gives the bytes needed) before anything is launched.
+ * seq_splits < 0 returns GLA_ERR_BAD_OPTION.
+ *
+ * Set-up: the first call on a device (with that device current) looks up the array's
+ * device address with cudaGetSymbolAddress and caches it; make that first call before
+ * any stream capture begins. A failed lookup returns GLA_ERR_LAUNCH.
+ *
+ * Sharing: every call on a device uses the same array. Nothing in it needs to start at
+ * zero (a call writes every scratch element before reading it), but calls whose kernels
+ * overlap on the GPU (different streams, or several host threads without ordering) race
+ * on it and give wrong results; order them on one stream or serialise them.
+ * Errors otherwise as gla_fwd_ex.
+ */
+gla_status gla_fwd_noalloc(const void *q, const void *k, const void *v, const float *g_log,
+                           float scale, const float *h0, void *o, float *hT,
+                           int64_t B, int64_t T, int64_t H, int64_t Dk, int64_t Dv,
+                           int seq_splits, gla_stream_t stream);
+
 /* Library ABI version: major * 10000 + minor * 100 + patch. */
 int gla_version(void);
 
