@@ -50,6 +50,7 @@ namespace {
 using namespace tc;
 
 constexpr int kC = 64;                 // chunk length (tokens)
+constexpr int kMaxSplits = 256;        // sequence segments per head, at most
 constexpr int kD = 128;                // Dk = Dv
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kExtreme2 = 50.f;      // |b| (log2 units) beyond which P takes the exact route
@@ -910,24 +911,38 @@ gla_tc_state_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
 
 // ======================================================================= scan kernel
 // S_start(s+1) = Gamma_s (.) S_start(s) + E_s, rows scaled by Gamma_s[d]; S_start(0) = h0.
-// Block (bh, 8-row slab of d), thread = value column v.
-__global__ void __launch_bounds__(128)
+// One thread per state element (d, v) of one head; the loads of a batch of segments are
+// issued together so the chain costs one memory round trip per batch, not per segment.
+constexpr int kScanThreads = 256;
+constexpr int kScanBatch = 8;
+
+__global__ void __launch_bounds__(kScanThreads)
 gla_tc_scan_kernel(const float *__restrict__ E, const float *__restrict__ gam,
                    const float *__restrict__ h0, float *__restrict__ sstart, int splits) {
-    const int bh = blockIdx.x;
-    const int d0 = blockIdx.y * 8;
-    const int v = threadIdx.x;
+    const size_t bh = blockIdx.x;
+    const int e = blockIdx.y * kScanThreads + threadIdx.x;   // d * kD + v
+    const int d = e / kD;
     const int nseg = splits - 1;
-    float s[8];
+    constexpr size_t kDD = (size_t)kD * kD;
+    float s = h0 ? h0[bh * kDD + e] : 0.f;
+    const float *Eb = E + bh * nseg * kDD + e;
+    const float *gb = gam + bh * nseg * kD + d;
+    float *ob = sstart + bh * nseg * kDD + e;
+    for (int r0 = 0; r0 < nseg; r0 += kScanBatch) {
+        float ev[kScanBatch], gv[kScanBatch];
 #pragma unroll
-    for (int x = 0; x < 8; ++x) s[x] = h0 ? h0[((size_t)bh * kD + d0 + x) * kD + v] : 0.f;
-    for (int r = 0; r < nseg; ++r) {
-        const size_t base = ((size_t)bh * nseg + r) * (kD * kD) + (size_t)d0 * kD + v;
-        const float *gp = gam + ((size_t)bh * nseg + r) * kD + d0;
+        for (int j = 0; j < kScanBatch; ++j) {
+            if (r0 + j < nseg) {
+                ev[j] = Eb[(size_t)(r0 + j) * kDD];
+                gv[j] = gb[(size_t)(r0 + j) * kD];
+            }
+        }
 #pragma unroll
-        for (int x = 0; x < 8; ++x) {
-            s[x] = gp[x] * s[x] + E[base + x * kD];
-            sstart[base + x * kD] = s[x];
+        for (int j = 0; j < kScanBatch; ++j) {
+            if (r0 + j < nseg) {
+                s = gv[j] * s + ev[j];
+                ob[(size_t)(r0 + j) * kDD] = s;
+            }
         }
     }
 }
@@ -949,7 +964,7 @@ cudaError_t set_attrs() {
 int clamp_splits(const Problem &p, int splits) {
     const int64_t nchunks = (p.T + kC - 1) / kC;
     int64_t s = std::max<int64_t>(1, std::min<int64_t>(splits, nchunks));
-    return (int)std::min<int64_t>(s, 64);
+    return (int)std::min<int64_t>(s, kMaxSplits);
 }
 
 }  // namespace
@@ -963,21 +978,12 @@ int tc_auto_splits(const Problem &p, int num_sms) {
     const int64_t nchunks = (p.T + kC - 1) / kC;
     const int64_t bh = p.B * p.H;
     if (nchunks <= 1 || bh <= 0) return 1;
-    // modelled time: waves of the output pass x chunks per segment, plus the state
-    // pass (about 0.4 of an output-pass chunk) for every segment but the last
-    double best = 1e30;
-    int best_s = 1;
-    for (int s = 1; s <= 32 && s <= nchunks; ++s) {
-        const double per = (double)((nchunks + s - 1) / s);
-        const double out_waves = (double)((bh * s + num_sms - 1) / num_sms);
-        const double st_waves = s > 1 ? (double)((bh * (s - 1) + num_sms - 1) / num_sms) : 0.0;
-        const double cost = out_waves * per + 0.4 * st_waves * per + 2.0 * (s > 1);
-        if (cost < best - 1e-9) {
-            best = cost;
-            best_s = s;
-        }
-    }
-    return best_s;
+    // The output pass runs one CTA per SM; a second wave of CTAs costs a whole extra
+    // segment of latency-bound chunks. So: the most segments per head that still fit in
+    // one wave of output CTAs (which also keeps the state pass to one wave).
+    int64_t s = std::max<int64_t>(1, num_sms / bh);
+    s = std::min<int64_t>(s, nchunks);
+    return (int)std::min<int64_t>(s, kMaxSplits);
 }
 
 size_t tc_workspace_bytes(const Problem &p, int splits) {
@@ -1016,7 +1022,8 @@ cudaError_t launch_tc(const Problem &p, int splits, void *ws, size_t ws_bytes,
         StateArgs sa{E, gam, p.T, (int)p.H, nchunks, s, dev_err};
         gla_tc_state_kernel<<<bh * (s - 1), kStateThreads, sm_::ALLOC, stream>>>(mk, mv, mg, sa);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        gla_tc_scan_kernel<<<dim3(bh, kD / 8), 128, 0, stream>>>(E, gam, p.h0, sstart, s);
+        gla_tc_scan_kernel<<<dim3(bh, kD * kD / kScanThreads), kScanThreads, 0, stream>>>(
+            E, gam, p.h0, sstart, s);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         count_launches(2);
     }
