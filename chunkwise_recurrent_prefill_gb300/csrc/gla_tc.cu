@@ -55,6 +55,9 @@ constexpr int kD = 128;                // Dk = Dv
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kExtreme2 = 50.f;      // |b| (log2 units) beyond which P takes the exact route
 constexpr float kRenorm2 = 50.f;       // |L| (log2 units) beyond which the state is renormalised
+constexpr int kGateBlock = 8;          // tokens per load/compute/store block of the gate warps
+constexpr unsigned kProducerNapNs = 128;  // idle back-off of the TMA producer's polling loop
+constexpr unsigned kIssuerNapNs = 32;     // idle back-off of the MMA issuers' polling loops
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -94,37 +97,41 @@ constexpr uint32_t kColOi = 384;   // O^T intra term, 64 columns
 constexpr uint32_t kColOs = 448;   // O^T inter term, 64 columns
 
 // Shared-memory map of the output kernel (bytes from a 1024-aligned base).
-//   q/k/v ring (4 stages): raw tiles as 128B-swizzled [64 x 64] bf16 boxes, two per tile;
-//     the gate warps rewrite q -> Q~ and k -> K~ (or K^ in an extreme chunk) in place.
-//   The log-gate rows are read by the gate warps straight from global memory (one chunk
-//   ahead, after a TMA prefetch into L2), so they take no shared memory.
+//   q/k/v ring (3 stages): raw tiles as 128B-swizzled [64 x 64] bf16 boxes, two per tile;
+//     the gate warps rewrite q -> Q' and k -> K' (or K^ in an extreme chunk) in place, and
+//     once O(c) has been read the epilogue stages the chunk's bf16 output in its dead Q'
+//     tile, so the stage is released only after that store has read it.
+//   g ring (2 slots): the chunk's log-gates, [64 tokens][128] f32, loaded by TMA and
+//     released as soon as the gate warps have scaled the chunk.
 namespace om {
-constexpr int NQ = 4;                   // q/k/v stages
+constexpr int NQ = 3;                   // q/k/v stages
+constexpr int NG = 2;                   // log-gate slots
 constexpr int NR = 4;                   // per-chunk ring of scales and flags (written by the
                                         // gates of c, read before O(c) completes)
 constexpr uint32_t Q = 0, K = 16384, V = 32768, QSTAGE = 49152;
-constexpr uint32_t P = NQ * QSTAGE;     // [64 x 64] bf16 P tile (128B swizzle)
-constexpr uint32_t OST = P + 8192;      // [64 x 128] bf16 output staging (two boxes)
-constexpr uint32_t GAM = OST + 16384;   // [NR][128] f32 exp(L_c): renormalisation scale
+constexpr uint32_t G = NQ * QSTAGE, GSLOT = 32768;
+constexpr uint32_t P = G + NG * GSLOT;  // [64 x 64] bf16 P tile (128B swizzle)
+constexpr uint32_t GAM = P + 8192;      // [NR][128] f32 exp(L_c): renormalisation scale
 constexpr uint32_t GAM2 = GAM + NR * 512; // [NR][128] f32 exp(Bc) (extreme chunks)
 constexpr uint32_t ENDS = GAM2 + NR * 512; // [128] f32 exp(L) after the latest chunk
-constexpr uint32_t BV = ENDS + 512;     // [128] f32 Bc of the chunk being gated (log2 units)
-constexpr uint32_t XCH = BV + 512;      // [4][128] f32 token-quarter totals
-constexpr uint32_t XF = XCH + 2048;     // [NR] u32 chunk flags: 1 = extreme, 2 = renormalise
-constexpr uint32_t SCR = XF + 64;       // [4][64] f32 exact-path scratch
+constexpr uint32_t XF = ENDS + 512;     // [NR] u32 chunk flags: 1 = extreme, 2 = renormalise
+constexpr uint32_t XCH = XF + 64;       // [2][128] f32 token-half totals of the gate warps
+constexpr uint32_t SCR = XCH + 1024;    // [4][64] f32 exact-path scratch
 constexpr uint32_t BAR = SCR + 1024;    // mbarriers
-constexpr uint32_t NBAR = 20;
+constexpr uint32_t NBAR = 24;
 constexpr uint32_t TSLOT = BAR + NBAR * 8;
 constexpr uint32_t ALLOC = TSLOT + 16 + 1024;
+static_assert(ALLOC <= 232448, "output kernel shared memory");
 }  // namespace om
 
 // mbarrier indices of the output kernel
 enum {
-    QFULL = 0, QEMPTY = 4, GDONE = 8, PFULL = 12, PFREE = 13, PBF = 14, SREADY = 15,
-    UDONE = 16, OFULL = 17, OFREE = 18, FIN = 19,
+    QFULL = 0, QEMPTY = 3, GFULL = 6, GEMPTY = 8, GDONE = 10, PFULL = 13, PFREE = 14, PBF = 15,
+    SREADY = 16, UDONE = 17, OFULL = 18, OFREE = 19, FIN = 20,
 };
+static_assert(FIN < (int)om::NBAR, "output kernel barrier map");
 
-constexpr int kOutThreads = 576;       // 18 warps
+constexpr int kOutThreads = 448;       // 14 warps (at most 4 per SM sub-partition: 128 registers)
 constexpr int kStateThreads = 320;     // 10 warps
 
 struct OutArgs {
@@ -207,8 +214,8 @@ __device__ __forceinline__ void gate_cumsum(const float *gs, float *xch, int qq,
 __device__ __forceinline__ uint32_t par(int use) { return (uint32_t)use & 1u; }
 
 // ======================================================================= output kernel
-// Warp roles (18 warps): 0 TMA producer, 1 MMA scheduler (one thread), 2-3 and 12-17
-// gate warps, 4-7 epilogue, 8-11 state + P conversion.
+// Warp roles (14 warps): 0 TMA producer, 1 MMA scheduler (one thread), 2-5 epilogue,
+// 6-9 state + P conversion, 10-13 gate warps.
 __global__ void __launch_bounds__(kOutThreads, 1)
 gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg,
@@ -221,8 +228,6 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     float *gam_s = reinterpret_cast<float *>(sm + GAM);
     float *gam2_s = reinterpret_cast<float *>(sm + GAM2);
     float *ends_s = reinterpret_cast<float *>(sm + ENDS);
-    float *bv_s = reinterpret_cast<float *>(sm + BV);
-    float *xch = reinterpret_cast<float *>(sm + XCH);
     uint32_t *xf = reinterpret_cast<uint32_t *>(sm + XF);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -237,7 +242,11 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         for (int i = 0; i < NQ; ++i) {
             mbar_init(&bars[QFULL + i], 1);
             mbar_init(&bars[QEMPTY + i], 1);
-            mbar_init(&bars[GDONE + i], 8);
+            mbar_init(&bars[GDONE + i], 4);
+        }
+        for (int i = 0; i < NG; ++i) {
+            mbar_init(&bars[GFULL + i], 1);
+            mbar_init(&bars[GEMPTY + i], 4);
         }
         mbar_init(&bars[PFULL], 1);
         mbar_init(&bars[PFREE], 4);
@@ -266,28 +275,57 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
+        // Two rings filled independently: the log-gate slots (freed early, by the gate
+        // warps) and the q/k/v stages (freed after the chunk's output store read them).
         if (lane == 0) {
-            int nq = 0;
-            for (; nq < n; ++nq) {
-                const int st = nq % NQ;
-                if (nq >= NQ && !mbar_wait(&bars[QEMPTY + st], par(nq / NQ - 1))) { ok = false; break; }
-                uint8_t *base = sm + st * QSTAGE;
-                uint64_t *fb = &bars[QFULL + st];
-                TRACE_OUT(0, nq);
-                const int t = (cb + nq) * kC;
-                tma_prefetch_l2_4d(&tg, 0, h, t, bidx);   // gate rows, read later by the gate warps
-                mbar_arrive_expect_tx(fb, 3 * 16384);
-                tma_load_4d(base + Q, &tq, fb, 0, h, t, bidx);
-                tma_load_4d(base + Q + 8192, &tq, fb, 64, h, t, bidx);
-                tma_load_4d(base + K, &tk, fb, 0, h, t, bidx);
-                tma_load_4d(base + K + 8192, &tk, fb, 64, h, t, bidx);
-                tma_load_4d(base + V, &tv, fb, 0, h, t, bidx);
-                tma_load_4d(base + V + 8192, &tv, fb, 64, h, t, bidx);
+            int ng = 0, nq = 0;
+            uint32_t idle = 0;
+            uint64_t t_idle = 0;
+            while (ng < n || nq < n) {
+                bool prog = false;
+                if (ng < n && (ng < NG || mbar_test(&bars[GEMPTY + ng % NG], par(ng / NG - 1)))) {
+                    uint64_t *fb = &bars[GFULL + ng % NG];
+                    mbar_arrive_expect_tx(fb, GSLOT);
+                    tma_load_4d(sm + G + (ng % NG) * GSLOT, &tg, fb, 0, h, (cb + ng) * kC, bidx);
+                    ++ng;
+                    prog = true;
+                }
+                if (nq < n && (nq < NQ || mbar_test(&bars[QEMPTY + nq % NQ], par(nq / NQ - 1)))) {
+                    uint8_t *base = sm + (nq % NQ) * QSTAGE;
+                    uint64_t *fb = &bars[QFULL + nq % NQ];
+                    TRACE_OUT(0, nq);
+                    const int t = (cb + nq) * kC;
+                    mbar_arrive_expect_tx(fb, 3 * 16384);
+                    tma_load_4d(base + Q, &tq, fb, 0, h, t, bidx);
+                    tma_load_4d(base + Q + 8192, &tq, fb, 64, h, t, bidx);
+                    tma_load_4d(base + K, &tk, fb, 0, h, t, bidx);
+                    tma_load_4d(base + K + 8192, &tk, fb, 64, h, t, bidx);
+                    tma_load_4d(base + V, &tv, fb, 0, h, t, bidx);
+                    tma_load_4d(base + V + 8192, &tv, fb, 64, h, t, bidx);
+                    ++nq;
+                    prog = true;
+                }
+                if (prog) {
+                    idle = 0;
+                } else {
+                    // yield the issue slots of this sub-partition to the compute warps
+                    __nanosleep(kProducerNapNs);
+                    if (++idle == 256) {
+                        t_idle = global_ns();   // the timer is read only on long idle streaks
+                    } else if ((idle & 1023) == 0 && global_ns() - t_idle > kWaitLimitNs) {
+                        ok = false;
+                        break;
+                    }
+                }
             }
             // never leave with a bulk copy still landing in this CTA's shared memory
             for (int i = 0; i < NQ; ++i) {
                 const int uses = nq > i ? (nq - 1 - i) / NQ + 1 : 0;
                 if (uses > 0 && !mbar_wait(&bars[QFULL + i], par(uses - 1))) ok = false;
+            }
+            for (int i = 0; i < NG; ++i) {
+                const int uses = ng > i ? (ng - 1 - i) / NG + 1 : 0;
+                if (uses > 0 && !mbar_wait(&bars[GFULL + i], par(uses - 1))) ok = false;
             }
         }
         __syncwarp();
@@ -353,19 +391,22 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                             mma_ss(tm + kColOi, smem_desc(base + V + kk * 2048, 8192, 1024),
                                    smem_desc(pbase + kk * 32, 16, 1024), idOi, kk > 0);
                     }
-                    mma_commit(&bars[OFULL]);
-                    mma_commit(&bars[QEMPTY + no % NQ]);   // U(no) was issued before O(no)
+                    mma_commit(&bars[OFULL]);   // U(no) and P(no) were issued before O(no)
                     TRACE_OUT(7, no);
                     ++no;
                     prog = true;
                 }
                 if (prog) {
                     idle = 0;
-                } else if (++idle == 256) {
-                    t_idle = global_ns();   // the timer is read only on long idle streaks
-                } else if ((idle & 1023) == 0 && global_ns() - t_idle > kWaitLimitNs) {
-                    ok = false;
-                    break;
+                } else {
+                    // yield the issue slots of this sub-partition to the compute warps
+                    __nanosleep(kIssuerNapNs);
+                    if (++idle == 256) {
+                        t_idle = global_ns();   // the timer is read only on long idle streaks
+                    } else if ((idle & 1023) == 0 && global_ns() - t_idle > kWaitLimitNs) {
+                        ok = false;
+                        break;
+                    }
                 }
             }
             // all issued MMAs complete before the CTA tears down its TMEM
@@ -373,12 +414,12 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             if (!mbar_wait(&bars[FIN], 0)) ok = false;
         }
         __syncwarp();
-    } else if (warp >= 4 && warp < 8) {
+    } else if (warp >= 2 && warp < 6) {
         // ------------------------------------------------------------ epilogue
         const int j = warp & 3;
-        const int et = (warp - 4) * 32 + lane;      // 0..127
+        const int et = (warp - 2) * 32 + lane;      // 0..127
         const int v = j * 32 + lane;                // O^T lane = value column
-        uint8_t *ost = sm + OST + (uint32_t)(v >> 6) * 8192;
+        const uint32_t vbox = (uint32_t)(v >> 6) * 8192;
         const uint32_t vcol = (uint32_t)(v & 63);
         for (int c = 0; c < n; ++c) {
             const bool w = mbar_wait(&bars[OFULL], par(c));
@@ -414,9 +455,9 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[OFREE]);
-            // stage O (bf16, 128B-swizzled boxes) once the previous store has read it
-            if (et == 0) bulk_wait_read_all();
-            named_bar_sync(2, 128);
+            // stage O (bf16, 128B-swizzled boxes) in the chunk's Q' tile: every MMA of the
+            // chunk has completed, so nothing reads that tile any more
+            uint8_t *ost = sm + (c % NQ) * QSTAGE + Q + vbox;
 #pragma unroll
             for (int x = 0; x < 32; ++x) {
                 *reinterpret_cast<__nv_bfloat16 *>(ost + sw128_offset(x, vcol)) =
@@ -428,15 +469,18 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             named_bar_sync(2, 128);
             if (et == 0) {
                 const int t0 = (cb + c) * kC;
-                tma_store_4d(&to, sm + OST, 0, h, t0, bidx);
-                tma_store_4d(&to, sm + OST + 8192, 64, h, t0, bidx);
+                uint8_t *qt = sm + (c % NQ) * QSTAGE + Q;
+                tma_store_4d(&to, qt, 0, h, t0, bidx);
+                tma_store_4d(&to, qt + 8192, 64, h, t0, bidx);
                 bulk_commit();
+                bulk_wait_read_all();
+                mbar_arrive(&bars[QEMPTY + c % NQ]);   // the stage may be refilled
                 TRACE_OUT(13, c);
             }
         }
         if (et == 0) bulk_wait_all();
         __syncwarp();
-    } else if (warp >= 8 && warp < 12) {
+    } else if (warp >= 6 && warp < 10) {
         // ------------------------------------------------------------ state + P conversion
         // The TMEM state is decay-normalised: S_c = diag(exp(L_c)) S~_c. Pass c takes the
         // bf16 snapshot of S~_c for O(c) (a renormalising chunk first restores S~ = S_c, an
@@ -444,12 +488,15 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         // masked bf16 P tile.
         const int j = warp & 3;
         const int v = j * 32 + lane;
-        const int st_t = (warp - 8) * 32 + lane;     // 0..127
+        const int st_t = (warp - 6) * 32 + lane;     // 0..127
         float *scr = reinterpret_cast<float *>(sm + SCR);
         const float *init = nullptr;
-        if (seg > 0)
+        if (seg > 0) {
+            // the start states come from the scan kernel, which may still be running: this
+            // kernel is launched as its programmatic dependent
+            pdl_wait_prerequisites();
             init = a.sstart + ((size_t)bh * (a.splits - 1) + (seg - 1)) * (kD * kD);
-        else if (a.h0)
+        } else if (a.h0)
             init = a.h0 + (size_t)bh * (kD * kD);
 #pragma unroll 1
         for (int d0 = 0; d0 < kD; d0 += 16) {
@@ -597,99 +644,145 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------------------ gate warps (8)
-        const int gw = warp < 4 ? warp - 2 : warp - 10;   // 0..7
-        const int gt = gw * 32 + lane;                      // 0..255
-        const int p = gt & 63, qq = gt >> 6;                // key-dim pair, token quarter
-        const int d = 2 * p;
-        const uint32_t boxo = (uint32_t)(p >> 5) * 8192;
+        // ------------------------------------------------------------ gate warps (4)
+        // Thread (hf, dp) owns the key-dimension pair d = 2 dp, 2 dp + 1 over the token half
+        // hf of a chunk (tokens 32 hf .. 32 hf + 31). Pass 1 sums the half's log2-gates and
+        // records the range of the running sums; the halves exchange totals, and the warps
+        // agree on the chunk's flags (extreme, renormalise). Pass 2 recomputes the running
+        // sums while scaling q and k in place, two dimensions per 32-bit access.
+        const int gt = (warp - 10) * 32 + lane;             // 0..127
+        const int dp = gt & 63, hf = gt >> 6;
+        const int d = 2 * dp;
+        const uint32_t boxo = (uint32_t)(d >> 6) * 8192;
         const uint32_t col = (uint32_t)(d & 63);
-        const int64_t rs = (int64_t)a.H * kD;               // row stride of g (elements)
-        const float *gp = a.g + ((int64_t)bidx * a.T * a.H + h) * kD + d;
-        // this thread's 16 gate rows of a chunk, loaded a chunk ahead
-        float2 gn[16];
-        auto load_g = [&](int c) {
-            const int64_t t0 = (int64_t)(cb + c) * kC + 16 * qq;
-#pragma unroll
-            for (int x = 0; x < 16; ++x)
-                gn[x] = (t0 + x < a.T) ? __ldg(reinterpret_cast<const float2 *>(gp + (t0 + x) * rs))
-                                       : make_float2(0.f, 0.f);
-        };
+        const float sc = a.scale;
+        const float lsc = log2f(sc);                        // folded into the q exponent
+        float *xch = reinterpret_cast<float *>(sm + XCH);   // [2][128] half totals
         float L0 = 0.f, L1 = 0.f;   // log2 decay of the normalised state (S = 2^L S~)
-        if (n > 0) load_g(0);
         for (int c = 0; c < n; ++c) {
-            float b0[16], b1[16];   // cumulative log2-gates of this thread's tokens
-            float a0 = 0.f, a1 = 0.f;
+            const int gs = c % NG, qs = c % NQ, slot = c & (NR - 1);
+            bool w = mbar_wait(&bars[GFULL + gs], par(c / NG));
+            if (named_bar_or(1, 128, !w)) { ok = false; break; }
+            if (gt == 0) TRACE_OUT(16, c);
+            const float *grow = reinterpret_cast<const float *>(sm + G + gs * GSLOT) +
+                                (32 * hf) * kD + d;
+            float r0 = 0.f, r1 = 0.f;
+            float lo0 = 0.f, hi0 = 0.f, lo1 = 0.f, hi1 = 0.f;   // range of the running sums
+#pragma unroll 1
+            for (int t0 = 0; t0 < 32; t0 += kGateBlock) {
+                float2 gv[kGateBlock];
 #pragma unroll
-            for (int x = 0; x < 16; ++x) {
-                a0 = fmaf(gn[x].x, kLog2e, a0);
-                a1 = fmaf(gn[x].y, kLog2e, a1);
-                b0[x] = a0;
-                b1[x] = a1;
-            }
-            if (c + 1 < n) load_g(c + 1);
-            *reinterpret_cast<float2 *>(xch + qq * kD + d) = make_float2(a0, a1);
-            // exchange the quarter totals; decide a renormalisation from |L|
-            bool ren = named_bar_or(1, 256, fabsf(L0) > kRenorm2 || fabsf(L1) > kRenorm2);
-            float o0 = 0.f, o1 = 0.f;
-            for (int q2 = 0; q2 < qq; ++q2) {
-                const float2 t = *reinterpret_cast<const float2 *>(xch + q2 * kD + d);
-                o0 += t.x;
-                o1 += t.y;
-            }
-            float mx = 0.f;
+                for (int x = 0; x < kGateBlock; ++x) gv[x] = *reinterpret_cast<const float2 *>(grow + (t0 + x) * kD);
 #pragma unroll
-            for (int x = 0; x < 16; ++x) {
-                b0[x] += o0;
-                b1[x] += o1;
-                mx = fmaxf(mx, fmaxf(fabsf(b0[x]), fabsf(b1[x])));
+                for (int x = 0; x < kGateBlock; ++x) {
+                    r0 = fmaf(gv[x].x, kLog2e, r0);
+                    r1 = fmaf(gv[x].y, kLog2e, r1);
+                    lo0 = fminf(lo0, r0); hi0 = fmaxf(hi0, r0);
+                    lo1 = fminf(lo1, r1); hi1 = fmaxf(hi1, r1);
+                }
             }
-            if (qq == 3) {
-                bv_s[d] = b0[15];
-                bv_s[d + 1] = b1[15];
-            }
-            const bool ext = named_bar_or(1, 256, mx > kExtreme2);   // also publishes bv_s
-            ren = ren || ext;
-            const float B0 = bv_s[d], B1 = bv_s[d + 1];
-            const float Lc0 = L0, Lc1 = L1;
-            const float Lq0 = ren ? 0.f : L0, Lq1 = ren ? 0.f : L1;   // L used by this chunk
+            *reinterpret_cast<float2 *>(xch + hf * kD + d) = make_float2(r0, r1);
+            named_bar_sync(1, 128);
+            const float2 t0v = *reinterpret_cast<const float2 *>(xch + d);        // half 0 totals
+            const float2 t1v = *reinterpret_cast<const float2 *>(xch + kD + d);   // half 1 totals
+            const float off0 = hf ? t0v.x : 0.f, off1 = hf ? t0v.y : 0.f;
+            const float B0 = t0v.x + t1v.x, B1 = t0v.y + t1v.y;   // chunk totals
+            // largest |b| over this thread's tokens (attained at an end of the range)
+            const float mx = fmaxf(fmaxf(fabsf(off0 + lo0), fabsf(off0 + hi0)),
+                                   fmaxf(fabsf(off1 + lo1), fabsf(off1 + hi1)));
+            const bool ext = named_bar_or(1, 128, mx > kExtreme2);
+            const bool ren = named_bar_or(1, 128, fabsf(L0) > kRenorm2 || fabsf(L1) > kRenorm2) || ext;
+            if (gt == 0) TRACE_OUT(17, c);
+            const float Lc0 = L0, Lc1 = L1;                     // before this chunk
+            const float Lq0 = ren ? 0.f : L0, Lq1 = ren ? 0.f : L1;   // used by this chunk
             L0 = ext ? 0.f : Lq0 + B0;
             L1 = ext ? 0.f : Lq1 + B1;
-            const bool w = mbar_wait(&bars[QFULL + c % NQ], par(c / NQ));
-            if (named_bar_or(1, 256, !w)) { ok = false; break; }
+            if (gt == 0) TRACE_OUT(18, c);
+            w = mbar_wait(&bars[QFULL + qs], par(c / NQ));
+            if (named_bar_or(1, 128, !w)) { ok = false; break; }
             // ring entries of chunk c: written only now, after the stage of chunk c arrived
-            // (which required O(c - NQ) done, so pass c - NQ has read the slot)
-            if (qq == 0) {
-                gam_s[(c & (NR - 1)) * 128 + d] = ex2(Lc0);       // restores S~ -> S_c
-                gam_s[(c & (NR - 1)) * 128 + d + 1] = ex2(Lc1);
-                if (ext) {
-                    gam2_s[(c & (NR - 1)) * 128 + d] = ex2(B0);
-                    gam2_s[(c & (NR - 1)) * 128 + d + 1] = ex2(B1);
-                }
-                ends_s[d] = ex2(L0);
-                ends_s[d + 1] = ex2(L1);
+            // (which required the output of c - NQ stored, so pass c - NR has read the slot)
+            if (hf == 0) {
+                *reinterpret_cast<float2 *>(gam_s + slot * 128 + d) = make_float2(ex2(Lc0), ex2(Lc1));
+                if (ext)
+                    *reinterpret_cast<float2 *>(gam2_s + slot * 128 + d) = make_float2(ex2(B0), ex2(B1));
+                *reinterpret_cast<float2 *>(ends_s + d) = make_float2(ex2(L0), ex2(L1));
             }
             if (gt == 0) TRACE_OUT(1, c);
-            uint8_t *base = sm + (c % NQ) * QSTAGE;
-            uint8_t *qt = base + Q + boxo;
-            uint8_t *kt = base + K + boxo;
-            const float sc = a.scale;
+            uint8_t *qt = sm + qs * QSTAGE + Q + boxo;
+            uint8_t *kt = sm + qs * QSTAGE + K + boxo;
+            r0 = 0.f;
+            r1 = 0.f;
+            // blocks of kGateBlock tokens: all loads of a block are issued before its stores, so a
+            // block costs one shared-memory round trip
+            if (!ext) {
+                // Q' = scale q 2^(b + L), K' = k 2^-(b + L) with b = off + r: the per-chunk
+                // constants (offset, L, log2 scale) are folded into two exponent biases
+                const float eq0 = off0 + Lq0 + lsc, eq1 = off1 + Lq1 + lsc;
+                const float ek0 = -(off0 + Lq0), ek1 = -(off1 + Lq1);
+#pragma unroll 1
+                for (int t0 = 0; t0 < 32; t0 += kGateBlock) {
+                    float2 gv[kGateBlock];
+                    uint32_t qv[kGateBlock], kv[kGateBlock];
 #pragma unroll
-            for (int x = 0; x < 16; ++x) {
-                const uint32_t off = sw128_offset(16 * qq + x, col);
-                const float2 qv = unpack_bf16(*reinterpret_cast<const uint32_t *>(qt + off));
-                const float2 kv = unpack_bf16(*reinterpret_cast<const uint32_t *>(kt + off));
-                // Q' = scale q 2^(b + L); K' = k 2^-(b + L), or K^ = k 2^(Bc - b) when extreme
-                *reinterpret_cast<uint32_t *>(qt + off) =
-                    pack_bf16(sc * qv.x * ex2(b0[x] + Lq0), sc * qv.y * ex2(b1[x] + Lq1));
-                const float e0 = ext ? B0 - b0[x] : -(b0[x] + Lq0);
-                const float e1 = ext ? B1 - b1[x] : -(b1[x] + Lq1);
-                *reinterpret_cast<uint32_t *>(kt + off) = pack_bf16(kv.x * ex2(e0), kv.y * ex2(e1));
+                    for (int x = 0; x < kGateBlock; ++x) {
+                        const uint32_t off = sw128_offset(32 * hf + t0 + x, col);
+                        gv[x] = *reinterpret_cast<const float2 *>(grow + (t0 + x) * kD);
+                        qv[x] = *reinterpret_cast<const uint32_t *>(qt + off);
+                        kv[x] = *reinterpret_cast<const uint32_t *>(kt + off);
+                    }
+#pragma unroll
+                    for (int x = 0; x < kGateBlock; ++x) {
+                        r0 = fmaf(gv[x].x, kLog2e, r0);
+                        r1 = fmaf(gv[x].y, kLog2e, r1);
+                        const float2 qf = unpack_bf16(qv[x]), kf = unpack_bf16(kv[x]);
+                        qv[x] = pack_bf16(qf.x * ex2(r0 + eq0), qf.y * ex2(r1 + eq1));
+                        kv[x] = pack_bf16(kf.x * ex2(ek0 - r0), kf.y * ex2(ek1 - r1));
+                    }
+#pragma unroll
+                    for (int x = 0; x < kGateBlock; ++x) {
+                        const uint32_t off = sw128_offset(32 * hf + t0 + x, col);
+                        *reinterpret_cast<uint32_t *>(qt + off) = qv[x];
+                        *reinterpret_cast<uint32_t *>(kt + off) = kv[x];
+                    }
+                }
+            } else {
+                // extreme chunk: K^ = k 2^(Bc - b) with b = off + r formed exactly as the chunk
+                // total was, so that the last token's factor is exactly 1
+#pragma unroll 1
+                for (int t0 = 0; t0 < 32; t0 += kGateBlock) {
+                    float2 gv[kGateBlock];
+                    uint32_t qv[kGateBlock], kv[kGateBlock];
+#pragma unroll
+                    for (int x = 0; x < kGateBlock; ++x) {
+                        const uint32_t off = sw128_offset(32 * hf + t0 + x, col);
+                        gv[x] = *reinterpret_cast<const float2 *>(grow + (t0 + x) * kD);
+                        qv[x] = *reinterpret_cast<const uint32_t *>(qt + off);
+                        kv[x] = *reinterpret_cast<const uint32_t *>(kt + off);
+                    }
+#pragma unroll
+                    for (int x = 0; x < kGateBlock; ++x) {
+                        r0 = fmaf(gv[x].x, kLog2e, r0);
+                        r1 = fmaf(gv[x].y, kLog2e, r1);
+                        const float b0 = off0 + r0, b1 = off1 + r1;
+                        const float2 qf = unpack_bf16(qv[x]), kf = unpack_bf16(kv[x]);
+                        qv[x] = pack_bf16(sc * qf.x * ex2(b0), sc * qf.y * ex2(b1));
+                        kv[x] = pack_bf16(kf.x * ex2(B0 - b0), kf.y * ex2(B1 - b1));
+                    }
+#pragma unroll
+                    for (int x = 0; x < kGateBlock; ++x) {
+                        const uint32_t off = sw128_offset(32 * hf + t0 + x, col);
+                        *reinterpret_cast<uint32_t *>(qt + off) = qv[x];
+                        *reinterpret_cast<uint32_t *>(kt + off) = kv[x];
+                    }
+                }
             }
-            if (gt == 0) xf[c & (NR - 1)] = (ext ? 1u : 0u) | (ren ? 2u : 0u);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[GEMPTY + gs]);   // the g slot may be refilled
+            if (gt == 0) xf[slot] = (ext ? 1u : 0u) | (ren ? 2u : 0u);
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[GDONE + c % NQ]);
+            if (lane == 0) mbar_arrive(&bars[GDONE + qs]);
             if (gt == 0) TRACE_OUT(2, c);
         }
         __syncwarp();
@@ -736,6 +829,7 @@ gla_tc_state_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + TSLOT);
     float *bv_s = reinterpret_cast<float *>(sm + BV);
     float *xch = reinterpret_cast<float *>(sm + XCH);
+    pdl_launch_dependents();   // the scan kernel may be scheduled now; it waits for us
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nseg = a.splits - 1;
     const int seg = blockIdx.x % nseg;
@@ -800,11 +894,15 @@ gla_tc_state_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
                 }
                 if (prog) {
                     idle = 0;
-                } else if (++idle == 256) {
-                    t_idle = global_ns();   // the timer is read only on long idle streaks
-                } else if ((idle & 1023) == 0 && global_ns() - t_idle > kWaitLimitNs) {
-                    ok = false;
-                    break;
+                } else {
+                    // yield the issue slots of this sub-partition to the compute warps
+                    __nanosleep(kIssuerNapNs);
+                    if (++idle == 256) {
+                        t_idle = global_ns();   // the timer is read only on long idle streaks
+                    } else if ((idle & 1023) == 0 && global_ns() - t_idle > kWaitLimitNs) {
+                        ok = false;
+                        break;
+                    }
                 }
             }
             for (int i = 0; i < NG; ++i) {
@@ -911,37 +1009,51 @@ gla_tc_state_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
 
 // ======================================================================= scan kernel
 // S_start(s+1) = Gamma_s (.) S_start(s) + E_s, rows scaled by Gamma_s[d]; S_start(0) = h0.
-// One thread per state element (d, v) of one head; the loads of a batch of segments are
-// issued together so the chain costs one memory round trip per batch, not per segment.
+// Each thread carries kScanPer state elements (d, v) of one head, 256 apart; the loads of a
+// batch of segments are issued together so the chain costs one memory round trip per
+// batch, not per segment. The grid stays small (B*H x 16 CTAs) so that all of it can be
+// resident while it waits for the state kernel.
 constexpr int kScanThreads = 256;
-constexpr int kScanBatch = 8;
+constexpr int kScanPer = 4;
+constexpr int kScanBatch = 4;
 
 __global__ void __launch_bounds__(kScanThreads)
 gla_tc_scan_kernel(const float *__restrict__ E, const float *__restrict__ gam,
                    const float *__restrict__ h0, float *__restrict__ sstart, int splits) {
+    pdl_launch_dependents();    // the output kernel may be scheduled now; it waits for us
+    pdl_wait_prerequisites();   // the end states of the state kernel
     const size_t bh = blockIdx.x;
-    const int e = blockIdx.y * kScanThreads + threadIdx.x;   // d * kD + v
-    const int d = e / kD;
+    const int e0 = blockIdx.y * (kScanThreads * kScanPer) + threadIdx.x;   // d * kD + v
     const int nseg = splits - 1;
     constexpr size_t kDD = (size_t)kD * kD;
-    float s = h0 ? h0[bh * kDD + e] : 0.f;
-    const float *Eb = E + bh * nseg * kDD + e;
-    const float *gb = gam + bh * nseg * kD + d;
-    float *ob = sstart + bh * nseg * kDD + e;
+    float s[kScanPer];
+#pragma unroll
+    for (int i = 0; i < kScanPer; ++i)
+        s[i] = h0 ? h0[bh * kDD + e0 + i * kScanThreads] : 0.f;
+    const float *Eb = E + bh * nseg * kDD + e0;
+    const float *gb = gam + bh * nseg * kD;
+    float *ob = sstart + bh * nseg * kDD + e0;
     for (int r0 = 0; r0 < nseg; r0 += kScanBatch) {
-        float ev[kScanBatch], gv[kScanBatch];
+        float ev[kScanBatch][kScanPer], gv[kScanBatch][kScanPer];
 #pragma unroll
         for (int j = 0; j < kScanBatch; ++j) {
             if (r0 + j < nseg) {
-                ev[j] = Eb[(size_t)(r0 + j) * kDD];
-                gv[j] = gb[(size_t)(r0 + j) * kD];
+#pragma unroll
+                for (int i = 0; i < kScanPer; ++i) {
+                    const int e = e0 + i * kScanThreads;
+                    ev[j][i] = Eb[(size_t)(r0 + j) * kDD + i * kScanThreads];
+                    gv[j][i] = gb[(size_t)(r0 + j) * kD + e / kD];
+                }
             }
         }
 #pragma unroll
         for (int j = 0; j < kScanBatch; ++j) {
             if (r0 + j < nseg) {
-                s = gv[j] * s + ev[j];
-                ob[(size_t)(r0 + j) * kDD] = s;
+#pragma unroll
+                for (int i = 0; i < kScanPer; ++i) {
+                    s[i] = gv[j][i] * s[i] + ev[j][i];
+                    ob[(size_t)(r0 + j) * kDD + i * kScanThreads] = s[i];
+                }
             }
         }
     }
@@ -1022,15 +1134,44 @@ cudaError_t launch_tc(const Problem &p, int splits, void *ws, size_t ws_bytes,
         StateArgs sa{E, gam, p.T, (int)p.H, nchunks, s, dev_err};
         gla_tc_state_kernel<<<bh * (s - 1), kStateThreads, sm_::ALLOC, stream>>>(mk, mv, mg, sa);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        gla_tc_scan_kernel<<<dim3(bh, kD * kD / kScanThreads), kScanThreads, 0, stream>>>(
-            E, gam, p.h0, sstart, s);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        // scan and output kernels are programmatic dependents: each may be scheduled while its
+        // predecessor (one of ours) still runs, and waits for it in griddepcontrol.wait
+        // before reading what it wrote. The state kernel itself launches normally, so every
+        // kernel of this call starts after the caller's preceding work has completed.
+        cudaLaunchAttribute pdl[1];
+        pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        pdl[0].val.programmaticStreamSerializationAllowed = 1;
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(bh, kD * kD / (kScanThreads * kScanPer));
+        cfg.blockDim = dim3(kScanThreads);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = stream;
+        cfg.attrs = pdl;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, gla_tc_scan_kernel, (const float *)E, (const float *)gam,
+                               p.h0, sstart, s);
+        if (e != cudaSuccess) return e;
         count_launches(2);
     }
     OutArgs oa{static_cast<const __nv_bfloat16 *>(p.q), static_cast<const __nv_bfloat16 *>(p.k),
                p.g, p.h0, p.hT, sstart, p.T, (int)p.H, nchunks, s, p.scale, dev_err};
-    gla_tc_out_kernel<<<bh * s, kOutThreads, om::ALLOC, stream>>>(mq, mk, mv, mg, mo, oa);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (s > 1) {
+        cudaLaunchAttribute pdl[1];
+        pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        pdl[0].val.programmaticStreamSerializationAllowed = 1;
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(bh * s);
+        cfg.blockDim = dim3(kOutThreads);
+        cfg.dynamicSmemBytes = om::ALLOC;
+        cfg.stream = stream;
+        cfg.attrs = pdl;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, gla_tc_out_kernel, mq, mk, mv, mg, mo, oa);
+    } else {
+        gla_tc_out_kernel<<<bh * s, kOutThreads, om::ALLOC, stream>>>(mq, mk, mv, mg, mo, oa);
+        e = cudaGetLastError();
+    }
+    if (e != cudaSuccess) return e;
     count_launches(1);
     return cudaSuccess;
 }

@@ -114,6 +114,18 @@ __device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t nthreads, boo
     return out != 0;
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Lets the next kernel in the stream (launched with programmatic stream serialisation) be
+// scheduled before this grid has finished.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Blocks until every prerequisite grid has completed and its memory is visible.
+__device__ __forceinline__ void pdl_wait_prerequisites() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
