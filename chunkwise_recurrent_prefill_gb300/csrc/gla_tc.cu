@@ -39,6 +39,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <cstdlib>
 
 #include "gla_internal.h"
 #include "tc_ptx.cuh"
@@ -144,6 +145,7 @@ struct OutArgs {
     int H, nchunks, splits;
     float scale;
     unsigned *err;
+    int stall_chunk;                   // test hook: chunk whose q/k/v load is never issued (-1)
 };
 
 struct StateArgs {
@@ -296,6 +298,11 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     TRACE_OUT(0, nq);
                     const int t = (cb + nq) * kC;
                     mbar_arrive_expect_tx(fb, 3 * 16384);
+                    if (nq == a.stall_chunk) {   // test hook: the stage never fills
+                        ++nq;
+                        prog = true;
+                        continue;
+                    }
                     tma_load_4d(base + Q, &tq, fb, 0, h, t, bidx);
                     tma_load_4d(base + Q + 8192, &tq, fb, 64, h, t, bidx);
                     tma_load_4d(base + K, &tk, fb, 0, h, t, bidx);
@@ -1153,8 +1160,12 @@ cudaError_t launch_tc(const Problem &p, int splits, void *ws, size_t ws_bytes,
         if (e != cudaSuccess) return e;
         count_launches(2);
     }
+    // Test hook for the bounded waits: with GLA_TEST_STALL_ONE_LOAD set, every output CTA
+    // skips the q/k/v load of one chunk, so the waits for it run out and the call reports
+    // GLA_ERR_DEVICE_TIMEOUT (after ~2 s per wait) with the context intact.
+    const int stall = std::getenv("GLA_TEST_STALL_ONE_LOAD") ? std::min(1, nchunks / s - 1) : -1;
     OutArgs oa{static_cast<const __nv_bfloat16 *>(p.q), static_cast<const __nv_bfloat16 *>(p.k),
-               p.g, p.h0, p.hT, sstart, p.T, (int)p.H, nchunks, s, p.scale, dev_err};
+               p.g, p.h0, p.hT, sstart, p.T, (int)p.H, nchunks, s, p.scale, dev_err, stall};
     if (s > 1) {
         cudaLaunchAttribute pdl[1];
         pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
