@@ -56,6 +56,7 @@ constexpr int kD = 128;                // Dk = Dv
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kExtreme2 = 50.f;      // |b| (log2 units) beyond which P takes the exact route
 constexpr float kRenorm2 = 50.f;       // |L| (log2 units) beyond which the state is renormalised
+constexpr int64_t kL2KeepBytes = 80ll << 20;  // state-pass reads kept in L2 for the output pass
 constexpr int kGateBlock = 8;          // tokens per load/compute/store block of the gate warps
 constexpr unsigned kProducerNapNs = 128;  // idle back-off of the TMA producer's polling loop
 constexpr unsigned kIssuerNapNs = 32;     // idle back-off of the MMA issuers' polling loops
@@ -154,6 +155,7 @@ struct StateArgs {
     int64_t T;
     int H, nchunks, splits;
     unsigned *err;
+    int retain;                        // chunks per CTA (read last) loaded with evict_last
 };
 
 __device__ __forceinline__ void seg_range(int seg, int nchunks, int splits, int &cb, int &ce) {
@@ -280,6 +282,9 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         // Two rings filled independently: the log-gate slots (freed early, by the gate
         // warps) and the q/k/v stages (freed after the chunk's output store read them).
         if (lane == 0) {
+            // every tile is read here for the last time: do not let it displace the chunks
+            // the state kernel left in L2 for this kernel
+            const uint64_t pol = l2_policy_evict_first();
             int ng = 0, nq = 0;
             uint32_t idle = 0;
             uint64_t t_idle = 0;
@@ -288,7 +293,8 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 if (ng < n && (ng < NG || mbar_test(&bars[GEMPTY + ng % NG], par(ng / NG - 1)))) {
                     uint64_t *fb = &bars[GFULL + ng % NG];
                     mbar_arrive_expect_tx(fb, GSLOT);
-                    tma_load_4d(sm + G + (ng % NG) * GSLOT, &tg, fb, 0, h, (cb + ng) * kC, bidx);
+                    tma_load_4d_hint(sm + G + (ng % NG) * GSLOT, &tg, fb, 0, h, (cb + ng) * kC,
+                                     bidx, pol);
                     ++ng;
                     prog = true;
                 }
@@ -303,12 +309,12 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                         prog = true;
                         continue;
                     }
-                    tma_load_4d(base + Q, &tq, fb, 0, h, t, bidx);
-                    tma_load_4d(base + Q + 8192, &tq, fb, 64, h, t, bidx);
-                    tma_load_4d(base + K, &tk, fb, 0, h, t, bidx);
-                    tma_load_4d(base + K + 8192, &tk, fb, 64, h, t, bidx);
-                    tma_load_4d(base + V, &tv, fb, 0, h, t, bidx);
-                    tma_load_4d(base + V + 8192, &tv, fb, 64, h, t, bidx);
+                    tma_load_4d_hint(base + Q, &tq, fb, 0, h, t, bidx, pol);
+                    tma_load_4d_hint(base + Q + 8192, &tq, fb, 64, h, t, bidx, pol);
+                    tma_load_4d_hint(base + K, &tk, fb, 0, h, t, bidx, pol);
+                    tma_load_4d_hint(base + K + 8192, &tk, fb, 64, h, t, bidx, pol);
+                    tma_load_4d_hint(base + V, &tv, fb, 0, h, t, bidx, pol);
+                    tma_load_4d_hint(base + V + 8192, &tv, fb, 64, h, t, bidx, pol);
                     ++nq;
                     prog = true;
                 }
@@ -477,8 +483,9 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             if (et == 0) {
                 const int t0 = (cb + c) * kC;
                 uint8_t *qt = sm + (c % NQ) * QSTAGE + Q;
-                tma_store_4d(&to, qt, 0, h, t0, bidx);
-                tma_store_4d(&to, qt + 8192, 64, h, t0, bidx);
+                const uint64_t pol = l2_policy_evict_first();
+                tma_store_4d_hint(&to, qt, 0, h, t0, bidx, pol);
+                tma_store_4d_hint(&to, qt + 8192, 64, h, t0, bidx, pol);
                 bulk_commit();
                 bulk_wait_read_all();
                 mbar_arrive(&bars[QEMPTY + c % NQ]);   // the stage may be refilled
@@ -874,6 +881,9 @@ gla_tc_state_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
 
     if (warp == 0) {
         if (lane == 0) {
+            // The chunks this CTA reads last (the first ones of its segment) are the ones the
+            // output kernel reads first: keep them in L2 ahead of the rest.
+            const uint64_t keep = l2_policy_evict_last(), drop = l2_policy_evict_first();
             int ng = 0, nk = 0;
             uint32_t idle = 0;
             uint64_t t_idle = 0;
@@ -883,7 +893,8 @@ gla_tc_state_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
                     uint64_t *fb = &bars[SGFULL + ng % NG];
                     TRACE_ST(0, ng);
                     mbar_arrive_expect_tx(fb, 32768);
-                    tma_load_4d(sm + G + (ng % NG) * GSLOT, &tg, fb, 0, h, (ce - 1 - ng) * kC, bidx);
+                    tma_load_4d_hint(sm + G + (ng % NG) * GSLOT, &tg, fb, 0, h, (ce - 1 - ng) * kC,
+                                     bidx, ng >= n - a.retain ? keep : drop);
                     ++ng;
                     prog = true;
                 }
@@ -892,10 +903,11 @@ gla_tc_state_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
                     uint64_t *fb = &bars[SKFULL + nk % NKV];
                     mbar_arrive_expect_tx(fb, 2 * 16384);
                     const int t = (ce - 1 - nk) * kC;      // last chunk first
-                    tma_load_4d(base + K, &tk, fb, 0, h, t, bidx);
-                    tma_load_4d(base + K + 8192, &tk, fb, 64, h, t, bidx);
-                    tma_load_4d(base + V, &tv, fb, 0, h, t, bidx);
-                    tma_load_4d(base + V + 8192, &tv, fb, 64, h, t, bidx);
+                    const uint64_t pol = nk >= n - a.retain ? keep : drop;
+                    tma_load_4d_hint(base + K, &tk, fb, 0, h, t, bidx, pol);
+                    tma_load_4d_hint(base + K + 8192, &tk, fb, 64, h, t, bidx, pol);
+                    tma_load_4d_hint(base + V, &tv, fb, 0, h, t, bidx, pol);
+                    tma_load_4d_hint(base + V + 8192, &tv, fb, 64, h, t, bidx, pol);
                     ++nk;
                     prog = true;
                 }
@@ -1138,7 +1150,11 @@ cudaError_t launch_tc(const Problem &p, int splits, void *ws, size_t ws_bytes,
         E = static_cast<float *>(ws);
         sstart = E + (size_t)bh * (s - 1) * kD * kD;
         gam = sstart + (size_t)bh * (s - 1) * kD * kD;
-        StateArgs sa{E, gam, p.T, (int)p.H, nchunks, s, dev_err};
+        // keep about kL2KeepBytes of the state pass's last reads for the output kernel
+        const int64_t per_chunk = 2 * 16384 + 32768;   // k, v, g bytes of one chunk
+        const int retain = (int)std::min<int64_t>(
+            (nchunks + s - 1) / s, kL2KeepBytes / ((int64_t)bh * (s - 1) * per_chunk));
+        StateArgs sa{E, gam, p.T, (int)p.H, nchunks, s, dev_err, retain};
         gla_tc_state_kernel<<<bh * (s - 1), kStateThreads, sm_::ALLOC, stream>>>(mk, mv, mg, sa);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         // scan and output kernels are programmatic dependents: each may be scheduled while its

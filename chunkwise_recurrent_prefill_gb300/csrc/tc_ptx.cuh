@@ -142,6 +142,31 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const void *tmap, uint64_
         : "memory");
 }
 
+// L2 eviction-priority policies (createpolicy) for the cache-hinted copies below: lines
+// touched with evict_last are kept ahead of normal and evict_first lines.
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// tma_load_4d with an L2 cache policy.
+__device__ __forceinline__ void tma_load_4d_hint(void *dst, const void *tmap, uint64_t *bar,
+                                                 int c0, int c1, int c2, int c3, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2),
+        "r"(c3), "l"(pol)
+        : "memory");
+}
+
 // Prefetch a 4-D tile of a tensor into L2 (no shared-memory destination, no completion).
 __device__ __forceinline__ void tma_prefetch_l2_4d(const void *tmap, int c0, int c1, int c2,
                                                    int c3) {
@@ -160,6 +185,16 @@ __device__ __forceinline__ void tma_store_4d(const void *tmap, const void *src, 
         "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
             reinterpret_cast<uint64_t>(tmap)),
         "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+
+// tma_store_4d with an L2 cache policy.
+__device__ __forceinline__ void tma_store_4d_hint(const void *tmap, const void *src, int c0,
+                                                  int c1, int c2, int c3, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group.L2::cache_hint"
+        " [%0, {%2, %3, %4, %5}], [%1], %6;" ::"l"(reinterpret_cast<uint64_t>(tmap)),
+        "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(pol)
         : "memory");
 }
 
