@@ -56,7 +56,7 @@ constexpr int kD = 128;                // Dk = Dv
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kExtreme2 = 50.f;      // |b| (log2 units) beyond which P takes the exact route
 constexpr float kRenorm2 = 50.f;       // |L| (log2 units) beyond which the state is renormalised
-constexpr int64_t kL2KeepBytes = 80ll << 20;  // state-pass reads kept in L2 for the output pass
+constexpr int64_t kL2KeepBytes = 96ll << 20;  // state-pass reads kept in L2 for the output pass
 constexpr int kGateBlock = 8;          // tokens per load/compute/store block of the gate warps
 constexpr unsigned kProducerNapNs = 128;  // idle back-off of the TMA producer's polling loop
 constexpr unsigned kIssuerNapNs = 32;     // idle back-off of the MMA issuers' polling loops
@@ -669,6 +669,12 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         const int d = 2 * dp;
         const uint32_t boxo = (uint32_t)(d >> 6) * 8192;
         const uint32_t col = (uint32_t)(d & 63);
+        // byte offsets of this thread's column within each row of an 8-row swizzle atom
+        // (blocks start on multiples of 8 rows, so row % 8 is the index within the block)
+        static_assert(kGateBlock % 8 == 0, "gate blocks must cover whole swizzle atoms");
+        uint32_t swz[kGateBlock];
+#pragma unroll
+        for (int x = 0; x < kGateBlock; ++x) swz[x] = sw128_offset((uint32_t)x, col);
         const float sc = a.scale;
         const float lsc = log2f(sc);                        // folded into the q exponent
         float *xch = reinterpret_cast<float *>(sm + XCH);   // [2][128] half totals
@@ -740,7 +746,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     uint32_t qv[kGateBlock], kv[kGateBlock];
 #pragma unroll
                     for (int x = 0; x < kGateBlock; ++x) {
-                        const uint32_t off = sw128_offset(32 * hf + t0 + x, col);
+                        const uint32_t off = (uint32_t)(32 * hf + t0) * 128u + swz[x];
                         gv[x] = *reinterpret_cast<const float2 *>(grow + (t0 + x) * kD);
                         qv[x] = *reinterpret_cast<const uint32_t *>(qt + off);
                         kv[x] = *reinterpret_cast<const uint32_t *>(kt + off);
@@ -755,7 +761,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     }
 #pragma unroll
                     for (int x = 0; x < kGateBlock; ++x) {
-                        const uint32_t off = sw128_offset(32 * hf + t0 + x, col);
+                        const uint32_t off = (uint32_t)(32 * hf + t0) * 128u + swz[x];
                         *reinterpret_cast<uint32_t *>(qt + off) = qv[x];
                         *reinterpret_cast<uint32_t *>(kt + off) = kv[x];
                     }
@@ -769,7 +775,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     uint32_t qv[kGateBlock], kv[kGateBlock];
 #pragma unroll
                     for (int x = 0; x < kGateBlock; ++x) {
-                        const uint32_t off = sw128_offset(32 * hf + t0 + x, col);
+                        const uint32_t off = (uint32_t)(32 * hf + t0) * 128u + swz[x];
                         gv[x] = *reinterpret_cast<const float2 *>(grow + (t0 + x) * kD);
                         qv[x] = *reinterpret_cast<const uint32_t *>(qt + off);
                         kv[x] = *reinterpret_cast<const uint32_t *>(kt + off);
@@ -785,7 +791,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     }
 #pragma unroll
                     for (int x = 0; x < kGateBlock; ++x) {
-                        const uint32_t off = sw128_offset(32 * hf + t0 + x, col);
+                        const uint32_t off = (uint32_t)(32 * hf + t0) * 128u + swz[x];
                         *reinterpret_cast<uint32_t *>(qt + off) = qv[x];
                         *reinterpret_cast<uint32_t *>(kt + off) = kv[x];
                     }
