@@ -85,6 +85,20 @@ __device__ long long *g_trace_state;
 #endif
 #define TRACE_OUT(ev, lc) GLA_TRACE_AT(g_trace_out, ev, lc)
 #define TRACE_ST(ev, lc) GLA_TRACE_AT(g_trace_state, ev, lc)
+// Global-timer stamps of every CTA (kernel k, event ev < 4), for the cross-kernel timeline.
+#ifdef GLA_TRACE
+constexpr int kTraceGlobCtas = 1024;
+__device__ long long *g_trace_glob;
+#define TRACE_GLOB(k, ev)                                                                     \
+    do {                                                                                      \
+        if (g_trace_glob && blockIdx.x < kTraceGlobCtas)                                      \
+            g_trace_glob[((size_t)(k) * kTraceGlobCtas + blockIdx.x) * 4 + (ev)] = global_ns(); \
+    } while (0)
+#else
+#define TRACE_GLOB(k, ev) \
+    do {                  \
+    } while (0)
+#endif
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
     return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -147,6 +161,7 @@ struct OutArgs {
     float scale;
     unsigned *err;
     int stall_chunk;                   // test hook: chunk whose q/k/v load is never issued (-1)
+    int last16;                        // weight of the last segment in 16ths (see seg_bound)
 };
 
 struct StateArgs {
@@ -156,11 +171,24 @@ struct StateArgs {
     int H, nchunks, splits;
     unsigned *err;
     int retain;                        // chunks per CTA (read last) loaded with evict_last
+    int last16;                        // weight of the last segment in 16ths (see seg_bound)
 };
 
-__device__ __forceinline__ void seg_range(int seg, int nchunks, int splits, int &cb, int &ce) {
-    cb = (int)((int64_t)seg * nchunks / splits);
-    ce = (int)((int64_t)(seg + 1) * nchunks / splits);
+// Chunk range [cb, ce) of segment `seg`. Every segment weighs 16 except the last, which
+// weighs `last16`: it is the only one the state pass does not read, so none of its tiles are
+// in L2 when the output pass reaches them, and it is made shorter in proportion to what the
+// others gain from L2. Short segments (fewer than 8 chunks each) are split evenly, so no
+// segment is ever empty.
+__device__ __host__ __forceinline__ int seg_bound(int j, int nchunks, int splits, int last16) {
+    if (j >= splits) return nchunks;
+    if (nchunks < 8 * splits) return (int)((int64_t)j * nchunks / splits);
+    return (int)((int64_t)j * nchunks * 16 / (16 * (splits - 1) + last16));
+}
+
+__device__ __forceinline__ void seg_range(int seg, int nchunks, int splits, int last16, int &cb,
+                                          int &ce) {
+    cb = seg_bound(seg, nchunks, splits, last16);
+    ce = seg_bound(seg + 1, nchunks, splits, last16);
 }
 
 // Load 64 consecutive TMEM columns of this warp's lane quarter (one wait).
@@ -239,7 +267,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     const int bh = blockIdx.x / a.splits;
     const int bidx = bh / a.H, h = bh % a.H;
     int cb, ce;
-    seg_range(seg, a.nchunks, a.splits, cb, ce);
+    seg_range(seg, a.nchunks, a.splits, a.last16, cb, ce);
     const int n = ce - cb;
 
     if (threadIdx.x == 0) {
@@ -276,6 +304,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     const uint32_t tm = *tslot;
     bool ok = true;
     if (threadIdx.x == 0) TRACE_OUT(14, 0);
+    if (threadIdx.x == 0) TRACE_GLOB(0, 0);
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -509,6 +538,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             // the start states come from the scan kernel, which may still be running: this
             // kernel is launched as its programmatic dependent
             pdl_wait_prerequisites();
+            if (threadIdx.x == 6 * 32) TRACE_GLOB(0, 1);
             init = a.sstart + ((size_t)bh * (a.splits - 1) + (seg - 1)) * (kD * kD);
         } else if (a.h0)
             init = a.h0 + (size_t)bh * (kD * kD);
@@ -812,6 +842,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     tc_fence_before();
     __syncthreads();
     if (threadIdx.x == 0) TRACE_OUT(15, 0);
+    if (threadIdx.x == 0) TRACE_GLOB(0, 2);
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tm, 512);
@@ -850,13 +881,14 @@ gla_tc_state_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
     float *bv_s = reinterpret_cast<float *>(sm + BV);
     float *xch = reinterpret_cast<float *>(sm + XCH);
     pdl_launch_dependents();   // the scan kernel may be scheduled now; it waits for us
+    if (threadIdx.x == 0) TRACE_GLOB(1, 0);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nseg = a.splits - 1;
     const int seg = blockIdx.x % nseg;
     const int bh = blockIdx.x / nseg;
     const int bidx = bh / a.H, h = bh % a.H;
     int cb, ce;
-    seg_range(seg, a.nchunks, a.splits, cb, ce);
+    seg_range(seg, a.nchunks, a.splits, a.last16, cb, ce);
     const int n = ce - cb;
     constexpr int NGD = NKV;   // gate-done ring
 
@@ -1026,6 +1058,7 @@ gla_tc_state_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
     if (!ok) atomicOr(a.err, kDevErrTimeout);
     tc_fence_before();
     __syncthreads();
+    if (threadIdx.x == 0) TRACE_GLOB(1, 2);
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tm, 128);
@@ -1046,7 +1079,9 @@ __global__ void __launch_bounds__(kScanThreads)
 gla_tc_scan_kernel(const float *__restrict__ E, const float *__restrict__ gam,
                    const float *__restrict__ h0, float *__restrict__ sstart, int splits) {
     pdl_launch_dependents();    // the output kernel may be scheduled now; it waits for us
+    if (threadIdx.x == 0 && blockIdx.y == 0) TRACE_GLOB(2, 0);
     pdl_wait_prerequisites();   // the end states of the state kernel
+    if (threadIdx.x == 0 && blockIdx.y == 0) TRACE_GLOB(2, 1);
     const size_t bh = blockIdx.x;
     const int e0 = blockIdx.y * (kScanThreads * kScanPer) + threadIdx.x;   // d * kD + v
     const int nseg = splits - 1;
@@ -1151,16 +1186,21 @@ cudaError_t launch_tc(const Problem &p, int splits, void *ws, size_t ws_bytes,
     const int nchunks = (int)((p.T + kC - 1) / kC);
     const int bh = (int)(p.B * p.H);
     float *E = nullptr, *gam = nullptr, *sstart = nullptr;
+    // State-pass reads kept in L2 for the output pass, as a fraction of all of them; the last
+    // segment (which gets none) is shortened by 15 % of that fraction.
+    const int64_t per_chunk = 2 * 16384 + 32768;   // k, v, g bytes of one chunk
+    const int64_t state_bytes = (int64_t)bh * (s - 1) * ((nchunks + s - 1) / s) * per_chunk;
+    const double kept = s > 1 ? std::min(1.0, (double)kL2KeepBytes / (double)state_bytes) : 0.0;
+    const int last16 = 16 - (int)(16.0 * 0.15 * kept + 0.5);
     if (s > 1) {
         if (!ws || ws_bytes < tc_workspace_bytes(p, s)) return cudaErrorInvalidValue;
         E = static_cast<float *>(ws);
         sstart = E + (size_t)bh * (s - 1) * kD * kD;
         gam = sstart + (size_t)bh * (s - 1) * kD * kD;
         // keep about kL2KeepBytes of the state pass's last reads for the output kernel
-        const int64_t per_chunk = 2 * 16384 + 32768;   // k, v, g bytes of one chunk
         const int retain = (int)std::min<int64_t>(
             (nchunks + s - 1) / s, kL2KeepBytes / ((int64_t)bh * (s - 1) * per_chunk));
-        StateArgs sa{E, gam, p.T, (int)p.H, nchunks, s, dev_err, retain};
+        StateArgs sa{E, gam, p.T, (int)p.H, nchunks, s, dev_err, retain, last16};
         gla_tc_state_kernel<<<bh * (s - 1), kStateThreads, sm_::ALLOC, stream>>>(mk, mv, mg, sa);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         // scan and output kernels are programmatic dependents: each may be scheduled while its
@@ -1187,7 +1227,8 @@ cudaError_t launch_tc(const Problem &p, int splits, void *ws, size_t ws_bytes,
     // GLA_ERR_DEVICE_TIMEOUT (after ~2 s per wait) with the context intact.
     const int stall = std::getenv("GLA_TEST_STALL_ONE_LOAD") ? std::min(1, nchunks / s - 1) : -1;
     OutArgs oa{static_cast<const __nv_bfloat16 *>(p.q), static_cast<const __nv_bfloat16 *>(p.k),
-               p.g, p.h0, p.hT, sstart, p.T, (int)p.H, nchunks, s, p.scale, dev_err, stall};
+               p.g, p.h0, p.hT, sstart, p.T, (int)p.H, nchunks, s, p.scale, dev_err, stall,
+               last16};
     if (s > 1) {
         cudaLaunchAttribute pdl[1];
         pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -75,6 +75,16 @@ def test_default_path_short_sequences_exact():
     assert path_for(1, 63, 16) == "exact" and path_for(1, 64, 16) == "tc"
 
 
+@pytest.mark.parametrize("B,T,H", [(1, 8192, 1), (1, 20000, 2), (3, 3000, 5)])
+def test_tc_auto_split_many_segments(B, T, H):
+    """Few heads: the automatic split gives many short segments (128 one-chunk segments at
+    B*H = 1), so the state pass, the scan over up to 127 segment states and the output pass
+    all run at their widest."""
+    from chunkwise_recurrent_prefill_gb300.gla import workspace_size
+    assert workspace_size(B, T, H) > 0
+    _check(_inputs(B=B, T=T, H=H, seed=T + H), seq_splits=0)
+
+
 def test_tc_no_h0():
     _check(_inputs(B=1, T=333, H=3, seed=8, with_h0=False), seq_splits=2)
 
