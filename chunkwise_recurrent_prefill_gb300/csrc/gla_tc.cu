@@ -131,8 +131,8 @@ constexpr uint32_t GAM = P + 8192;      // [NR][128] f32 exp(L_c): renormalisati
 constexpr uint32_t GAM2 = GAM + NR * 512; // [NR][128] f32 exp(Bc) (extreme chunks)
 constexpr uint32_t ENDS = GAM2 + NR * 512; // [128] f32 exp(L) after the latest chunk
 constexpr uint32_t XF = ENDS + 512;     // [NR] u32 chunk flags: 1 = extreme, 2 = renormalise
-constexpr uint32_t XCH = XF + 64;       // [2][128] f32 token-half totals of the gate warps
-constexpr uint32_t SCR = XCH + 1024;    // [4][64] f32 exact-path scratch
+constexpr uint32_t XCH = XF + 64;       // [3][128] f32 token-range totals of the gate warps
+constexpr uint32_t SCR = XCH + 1536;    // [4][64] f32 exact-path scratch
 constexpr uint32_t BAR = SCR + 1024;    // mbarriers
 constexpr uint32_t NBAR = 24;
 constexpr uint32_t TSLOT = BAR + NBAR * 8;
@@ -147,7 +147,10 @@ enum {
 };
 static_assert(FIN < (int)om::NBAR, "output kernel barrier map");
 
-constexpr int kOutThreads = 448;       // 14 warps (at most 4 per SM sub-partition: 128 registers)
+constexpr int kOutThreads = 512;       // 16 warps (4 per SM sub-partition: 128 registers)
+constexpr int kGateWarps = 6;          // warps 10..15
+constexpr int kGateThreads = kGateWarps * 32;
+constexpr int kGatePart = 24;          // tokens per gate thread (the last range has 16)
 constexpr int kStateThreads = 320;     // 10 warps
 
 struct OutArgs {
@@ -246,8 +249,8 @@ __device__ __forceinline__ void gate_cumsum(const float *gs, float *xch, int qq,
 __device__ __forceinline__ uint32_t par(int use) { return (uint32_t)use & 1u; }
 
 // ======================================================================= output kernel
-// Warp roles (14 warps): 0 TMA producer, 1 MMA scheduler (one thread), 2-5 epilogue,
-// 6-9 state + P conversion, 10-13 gate warps.
+// Warp roles (16 warps): 0 TMA producer, 1 MMA scheduler (one thread), 2-5 epilogue,
+// 6-9 state + P conversion, 10-15 gate warps.
 __global__ void __launch_bounds__(kOutThreads, 1)
 gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg,
@@ -274,11 +277,11 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         for (int i = 0; i < NQ; ++i) {
             mbar_init(&bars[QFULL + i], 1);
             mbar_init(&bars[QEMPTY + i], 1);
-            mbar_init(&bars[GDONE + i], 4);
+            mbar_init(&bars[GDONE + i], kGateWarps);
         }
         for (int i = 0; i < NG; ++i) {
             mbar_init(&bars[GFULL + i], 1);
-            mbar_init(&bars[GEMPTY + i], 4);
+            mbar_init(&bars[GEMPTY + i], kGateWarps);
         }
         mbar_init(&bars[PFULL], 1);
         mbar_init(&bars[PFREE], 4);
@@ -688,38 +691,40 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------------------ gate warps (4)
-        // Thread (hf, dp) owns the key-dimension pair d = 2 dp, 2 dp + 1 over the token half
-        // hf of a chunk (tokens 32 hf .. 32 hf + 31). Pass 1 sums the half's log2-gates and
-        // records the range of the running sums; the halves exchange totals, and the warps
-        // agree on the chunk's flags (extreme, renormalise). Pass 2 recomputes the running
-        // sums while scaling q and k in place, two dimensions per 32-bit access.
-        const int gt = (warp - 10) * 32 + lane;             // 0..127
-        const int dp = gt & 63, hf = gt >> 6;
+        // ------------------------------------------------------------ gate warps (6)
+        // Thread (part, dp) owns the key-dimension pair d = 2 dp, 2 dp + 1 over one of three
+        // token ranges of a chunk ([0,24), [24,48), [48,64)). Pass 1 sums the range's
+        // log2-gates and records the range of the running sums; the ranges exchange totals,
+        // and the warps agree on the chunk's flags (extreme, renormalise). Pass 2 recomputes
+        // the running sums while scaling q and k in place, two dimensions per 32-bit access.
+        const int gt = (warp - 10) * 32 + lane;             // 0..191
+        const int dp = gt & 63, part = gt >> 6;
+        const int tb = part * kGatePart;                    // first token of the range
+        const int tl = min(kGatePart, kC - tb);             // tokens in the range
         const int d = 2 * dp;
         const uint32_t boxo = (uint32_t)(d >> 6) * 8192;
         const uint32_t col = (uint32_t)(d & 63);
         // byte offsets of this thread's column within each row of an 8-row swizzle atom
         // (blocks start on multiples of 8 rows, so row % 8 is the index within the block)
-        static_assert(kGateBlock % 8 == 0, "gate blocks must cover whole swizzle atoms");
+        static_assert(kGateBlock % 8 == 0 && kGatePart % kGateBlock == 0,
+                      "gate blocks must cover whole swizzle atoms");
         uint32_t swz[kGateBlock];
 #pragma unroll
         for (int x = 0; x < kGateBlock; ++x) swz[x] = sw128_offset((uint32_t)x, col);
         const float sc = a.scale;
         const float lsc = log2f(sc);                        // folded into the q exponent
-        float *xch = reinterpret_cast<float *>(sm + XCH);   // [2][128] half totals
+        float *xch = reinterpret_cast<float *>(sm + XCH);   // [3][128] range totals
         float L0 = 0.f, L1 = 0.f;   // log2 decay of the normalised state (S = 2^L S~)
         for (int c = 0; c < n; ++c) {
             const int gs = c % NG, qs = c % NQ, slot = c & (NR - 1);
             bool w = mbar_wait(&bars[GFULL + gs], par(c / NG));
-            if (named_bar_or(1, 128, !w)) { ok = false; break; }
+            if (named_bar_or(1, kGateThreads, !w)) { ok = false; break; }
             if (gt == 0) TRACE_OUT(16, c);
-            const float *grow = reinterpret_cast<const float *>(sm + G + gs * GSLOT) +
-                                (32 * hf) * kD + d;
+            const float *grow = reinterpret_cast<const float *>(sm + G + gs * GSLOT) + tb * kD + d;
             float r0 = 0.f, r1 = 0.f;
             float lo0 = 0.f, hi0 = 0.f, lo1 = 0.f, hi1 = 0.f;   // range of the running sums
 #pragma unroll 1
-            for (int t0 = 0; t0 < 32; t0 += kGateBlock) {
+            for (int t0 = 0; t0 < tl; t0 += kGateBlock) {
                 float2 gv[kGateBlock];
 #pragma unroll
                 for (int x = 0; x < kGateBlock; ++x) gv[x] = *reinterpret_cast<const float2 *>(grow + (t0 + x) * kD);
@@ -731,17 +736,23 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     lo1 = fminf(lo1, r1); hi1 = fmaxf(hi1, r1);
                 }
             }
-            *reinterpret_cast<float2 *>(xch + hf * kD + d) = make_float2(r0, r1);
-            named_bar_sync(1, 128);
-            const float2 t0v = *reinterpret_cast<const float2 *>(xch + d);        // half 0 totals
-            const float2 t1v = *reinterpret_cast<const float2 *>(xch + kD + d);   // half 1 totals
-            const float off0 = hf ? t0v.x : 0.f, off1 = hf ? t0v.y : 0.f;
-            const float B0 = t0v.x + t1v.x, B1 = t0v.y + t1v.y;   // chunk totals
+            *reinterpret_cast<float2 *>(xch + part * kD + d) = make_float2(r0, r1);
+            named_bar_sync(1, kGateThreads);
+            const float2 tA = *reinterpret_cast<const float2 *>(xch + d);           // range totals
+            const float2 tB = *reinterpret_cast<const float2 *>(xch + kD + d);
+            const float2 tC = *reinterpret_cast<const float2 *>(xch + 2 * kD + d);
+            const float ab0 = tA.x + tB.x, ab1 = tA.y + tB.y;
+            // b = off + (running sum within the range); the chunk total is formed by the same
+            // additions, so that b of the last token equals it exactly
+            const float off0 = part == 0 ? 0.f : (part == 1 ? tA.x : ab0);
+            const float off1 = part == 0 ? 0.f : (part == 1 ? tA.y : ab1);
+            const float B0 = ab0 + tC.x, B1 = ab1 + tC.y;   // chunk totals
             // largest |b| over this thread's tokens (attained at an end of the range)
             const float mx = fmaxf(fmaxf(fabsf(off0 + lo0), fabsf(off0 + hi0)),
                                    fmaxf(fabsf(off1 + lo1), fabsf(off1 + hi1)));
-            const bool ext = named_bar_or(1, 128, mx > kExtreme2);
-            const bool ren = named_bar_or(1, 128, fabsf(L0) > kRenorm2 || fabsf(L1) > kRenorm2) || ext;
+            const bool ext = named_bar_or(1, kGateThreads, mx > kExtreme2);
+            const bool ren =
+                named_bar_or(1, kGateThreads, fabsf(L0) > kRenorm2 || fabsf(L1) > kRenorm2) || ext;
             if (gt == 0) TRACE_OUT(17, c);
             const float Lc0 = L0, Lc1 = L1;                     // before this chunk
             const float Lq0 = ren ? 0.f : L0, Lq1 = ren ? 0.f : L1;   // used by this chunk
@@ -749,10 +760,10 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             L1 = ext ? 0.f : Lq1 + B1;
             if (gt == 0) TRACE_OUT(18, c);
             w = mbar_wait(&bars[QFULL + qs], par(c / NQ));
-            if (named_bar_or(1, 128, !w)) { ok = false; break; }
+            if (named_bar_or(1, kGateThreads, !w)) { ok = false; break; }
             // ring entries of chunk c: written only now, after the stage of chunk c arrived
             // (which required the output of c - NQ stored, so pass c - NR has read the slot)
-            if (hf == 0) {
+            if (part == 0) {
                 *reinterpret_cast<float2 *>(gam_s + slot * 128 + d) = make_float2(ex2(Lc0), ex2(Lc1));
                 if (ext)
                     *reinterpret_cast<float2 *>(gam2_s + slot * 128 + d) = make_float2(ex2(B0), ex2(B1));
@@ -771,12 +782,12 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 const float eq0 = off0 + Lq0 + lsc, eq1 = off1 + Lq1 + lsc;
                 const float ek0 = -(off0 + Lq0), ek1 = -(off1 + Lq1);
 #pragma unroll 1
-                for (int t0 = 0; t0 < 32; t0 += kGateBlock) {
+                for (int t0 = 0; t0 < tl; t0 += kGateBlock) {
                     float2 gv[kGateBlock];
                     uint32_t qv[kGateBlock], kv[kGateBlock];
 #pragma unroll
                     for (int x = 0; x < kGateBlock; ++x) {
-                        const uint32_t off = (uint32_t)(32 * hf + t0) * 128u + swz[x];
+                        const uint32_t off = (uint32_t)(tb + t0) * 128u + swz[x];
                         gv[x] = *reinterpret_cast<const float2 *>(grow + (t0 + x) * kD);
                         qv[x] = *reinterpret_cast<const uint32_t *>(qt + off);
                         kv[x] = *reinterpret_cast<const uint32_t *>(kt + off);
@@ -791,7 +802,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     }
 #pragma unroll
                     for (int x = 0; x < kGateBlock; ++x) {
-                        const uint32_t off = (uint32_t)(32 * hf + t0) * 128u + swz[x];
+                        const uint32_t off = (uint32_t)(tb + t0) * 128u + swz[x];
                         *reinterpret_cast<uint32_t *>(qt + off) = qv[x];
                         *reinterpret_cast<uint32_t *>(kt + off) = kv[x];
                     }
@@ -800,12 +811,12 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 // extreme chunk: K^ = k 2^(Bc - b) with b = off + r formed exactly as the chunk
                 // total was, so that the last token's factor is exactly 1
 #pragma unroll 1
-                for (int t0 = 0; t0 < 32; t0 += kGateBlock) {
+                for (int t0 = 0; t0 < tl; t0 += kGateBlock) {
                     float2 gv[kGateBlock];
                     uint32_t qv[kGateBlock], kv[kGateBlock];
 #pragma unroll
                     for (int x = 0; x < kGateBlock; ++x) {
-                        const uint32_t off = (uint32_t)(32 * hf + t0) * 128u + swz[x];
+                        const uint32_t off = (uint32_t)(tb + t0) * 128u + swz[x];
                         gv[x] = *reinterpret_cast<const float2 *>(grow + (t0 + x) * kD);
                         qv[x] = *reinterpret_cast<const uint32_t *>(qt + off);
                         kv[x] = *reinterpret_cast<const uint32_t *>(kt + off);
@@ -821,7 +832,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     }
 #pragma unroll
                     for (int x = 0; x < kGateBlock; ++x) {
-                        const uint32_t off = (uint32_t)(32 * hf + t0) * 128u + swz[x];
+                        const uint32_t off = (uint32_t)(tb + t0) * 128u + swz[x];
                         *reinterpret_cast<uint32_t *>(qt + off) = qv[x];
                         *reinterpret_cast<uint32_t *>(kt + off) = kv[x];
                     }
