@@ -208,12 +208,10 @@ size_t gla_fwd_workspace_size(int64_t B, int64_t T, int64_t H, int64_t Dk, int64
     p.B = B; p.T = T; p.H = H; p.Dk = Dk; p.Dv = Dv; p.io = io;
     if (resolve_path(opt, p) != GLA_PATH_TC || !gla::tc_supported(p)) return 0;
     int splits = opt ? opt->seq_splits : 0;
-    if (splits <= 0) {
-        DeviceState *st = nullptr;
-        const int sms = current_device(&st) == GLA_OK ? st->num_sms : 152;
-        splits = gla::tc_auto_splits(p, sms);
-    }
-    return gla::tc_workspace_bytes(p, splits);
+    DeviceState *st = nullptr;
+    const int sms = current_device(&st) == GLA_OK ? st->num_sms : 152;
+    if (splits <= 0) splits = gla::tc_auto_splits(p, sms);
+    return gla::tc_workspace_bytes(p, splits, sms);
 }
 
 gla_status gla_fwd_ex(const void *q, const void *k, const void *v, const float *g_log,
@@ -244,7 +242,7 @@ gla_status gla_fwd_ex(const void *q, const void *k, const void *v, const float *
     } else {
         int splits = (opt && opt->seq_splits > 0) ? opt->seq_splits
                                                   : gla::tc_auto_splits(p, st->num_sms);
-        const size_t need = gla::tc_workspace_bytes(p, splits);
+        const size_t need = gla::tc_workspace_bytes(p, splits, st->num_sms);
         void *ws = nullptr;
         if (need > 0) {
             if (opt && opt->workspace) {
@@ -255,7 +253,7 @@ gla_status gla_fwd_ex(const void *q, const void *k, const void *v, const float *
                 if (rc != GLA_OK) return rc;
             }
         }
-        e = gla::launch_tc(p, splits, ws, need, st->err_word, s);
+        e = gla::launch_tc(p, splits, st->num_sms, ws, need, st->err_word, s);
     }
     if (e != cudaSuccess) {
         cudaGetLastError();

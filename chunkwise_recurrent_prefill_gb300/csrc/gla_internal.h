@@ -38,8 +38,9 @@ cudaError_t launch_exact(const Problem &p, unsigned int *dev_err, cudaStream_t s
 // tcgen05 path (bf16 io, Dk = Dv = 128).
 bool tc_supported(const Problem &p);
 int tc_auto_splits(const Problem &p, int num_sms);
-size_t tc_workspace_bytes(const Problem &p, int splits);
-cudaError_t launch_tc(const Problem &p, int splits, void *ws, size_t ws_bytes,
+int tc_state_pieces(const Problem &p, int splits, int num_sms);
+size_t tc_workspace_bytes(const Problem &p, int splits, int num_sms);
+cudaError_t launch_tc(const Problem &p, int splits, int num_sms, void *ws, size_t ws_bytes,
                       unsigned int *dev_err, cudaStream_t s);
 
 }  // namespace gla

@@ -52,6 +52,7 @@ using namespace tc;
 
 constexpr int kC = 64;                 // chunk length (tokens)
 constexpr int kMaxSplits = 256;        // sequence segments per head, at most
+constexpr int kMaxPieces = 8;          // state-pass pieces per segment, at most
 constexpr int kD = 128;                // Dk = Dv
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kExtreme2 = 50.f;      // |b| (log2 units) beyond which P takes the exact route
@@ -175,6 +176,7 @@ struct StateArgs {
     unsigned *err;
     int retain;                        // chunks per CTA (read last) loaded with evict_last
     int last16;                        // weight of the last segment in 16ths (see seg_bound)
+    int pieces;                        // consecutive pieces per segment, one CTA each
 };
 
 // Chunk range [cb, ce) of segment `seg`. Every segment weighs 16 except the last, which
@@ -894,12 +896,20 @@ gla_tc_state_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
     pdl_launch_dependents();   // the scan kernel may be scheduled now; it waits for us
     if (threadIdx.x == 0) TRACE_GLOB(1, 0);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nseg = a.splits - 1;
-    const int seg = blockIdx.x % nseg;
-    const int bh = blockIdx.x / nseg;
+    // CTA = piece `sub` of segment `seg` of head `bh`: E and Gamma of that piece
+    const int npc = (a.splits - 1) * a.pieces;   // pieces per head
+    const int pi = blockIdx.x % npc;
+    const int bh = blockIdx.x / npc;
+    const int seg = pi / a.pieces, sub = pi % a.pieces;
     const int bidx = bh / a.H, h = bh % a.H;
     int cb, ce;
     seg_range(seg, a.nchunks, a.splits, a.last16, cb, ce);
+    {
+        const int len = ce - cb;
+        const int c0 = cb + (int)((int64_t)sub * len / a.pieces);
+        ce = cb + (int)((int64_t)(sub + 1) * len / a.pieces);
+        cb = c0;
+    }
     const int n = ce - cb;
     constexpr int NGD = NKV;   // gate-done ring
 
@@ -1041,7 +1051,7 @@ gla_tc_state_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
             if (gt == 0) TRACE_ST(2, c);
         }
         if (ok && qq == 0) {
-            float *gp = a.gam + ((size_t)bh * (a.splits - 1) + seg) * kD;
+            float *gp = a.gam + ((size_t)bh * npc + pi) * kD;
             gp[d] = ex2(l0);
             gp[d + 1] = ex2(l1);
         }
@@ -1053,7 +1063,7 @@ gla_tc_state_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
                 ok = false;
             } else {
                 tc_fence_after();
-                float *ep = a.E + ((size_t)bh * (a.splits - 1) + seg) * (kD * kD) + v;
+                float *ep = a.E + ((size_t)bh * npc + pi) * (kD * kD) + v;
 #pragma unroll 1
                 for (int half = 0; half < 2; ++half) {
                     float ev[64];
@@ -1077,18 +1087,19 @@ gla_tc_state_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
 }
 
 // ======================================================================= scan kernel
-// S_start(s+1) = Gamma_s (.) S_start(s) + E_s, rows scaled by Gamma_s[d]; S_start(0) = h0.
-// Each thread carries kScanPer state elements (d, v) of one head, 256 apart; the loads of a
-// batch of segments are issued together so the chain costs one memory round trip per
-// batch, not per segment. The grid stays small (B*H x 16 CTAs) so that all of it can be
-// resident while it waits for the state kernel.
+// S_start(s+1) = fold over the pieces of segment s of (Gamma (.) S + E), rows scaled by
+// Gamma[d]; S_start(0) = h0. Each thread carries kScanPer state elements (d, v) of one head,
+// 256 apart; the loads of a batch of pieces are issued together so the chain costs one
+// memory round trip per batch, not per piece. The grid stays small (B*H x 16 CTAs) so that
+// all of it can be resident while it waits for the state kernel.
 constexpr int kScanThreads = 256;
 constexpr int kScanPer = 4;
 constexpr int kScanBatch = 4;
 
 __global__ void __launch_bounds__(kScanThreads)
 gla_tc_scan_kernel(const float *__restrict__ E, const float *__restrict__ gam,
-                   const float *__restrict__ h0, float *__restrict__ sstart, int splits) {
+                   const float *__restrict__ h0, float *__restrict__ sstart, int splits,
+                   int pieces) {
     pdl_launch_dependents();    // the output kernel may be scheduled now; it waits for us
     if (threadIdx.x == 0 && blockIdx.y == 0) TRACE_GLOB(2, 0);
     pdl_wait_prerequisites();   // the end states of the state kernel
@@ -1096,19 +1107,20 @@ gla_tc_scan_kernel(const float *__restrict__ E, const float *__restrict__ gam,
     const size_t bh = blockIdx.x;
     const int e0 = blockIdx.y * (kScanThreads * kScanPer) + threadIdx.x;   // d * kD + v
     const int nseg = splits - 1;
+    const int npc = nseg * pieces;
     constexpr size_t kDD = (size_t)kD * kD;
     float s[kScanPer];
 #pragma unroll
     for (int i = 0; i < kScanPer; ++i)
         s[i] = h0 ? h0[bh * kDD + e0 + i * kScanThreads] : 0.f;
-    const float *Eb = E + bh * nseg * kDD + e0;
-    const float *gb = gam + bh * nseg * kD;
+    const float *Eb = E + bh * npc * kDD + e0;
+    const float *gb = gam + bh * npc * kD;
     float *ob = sstart + bh * nseg * kDD + e0;
-    for (int r0 = 0; r0 < nseg; r0 += kScanBatch) {
+    for (int r0 = 0; r0 < npc; r0 += kScanBatch) {
         float ev[kScanBatch][kScanPer], gv[kScanBatch][kScanPer];
 #pragma unroll
         for (int j = 0; j < kScanBatch; ++j) {
-            if (r0 + j < nseg) {
+            if (r0 + j < npc) {
 #pragma unroll
                 for (int i = 0; i < kScanPer; ++i) {
                     const int e = e0 + i * kScanThreads;
@@ -1119,11 +1131,13 @@ gla_tc_scan_kernel(const float *__restrict__ E, const float *__restrict__ gam,
         }
 #pragma unroll
         for (int j = 0; j < kScanBatch; ++j) {
-            if (r0 + j < nseg) {
+            if (r0 + j < npc) {
+                const bool seg_end = (r0 + j + 1) % pieces == 0;
+                const size_t os = (size_t)((r0 + j + 1) / pieces - 1) * kDD;
 #pragma unroll
                 for (int i = 0; i < kScanPer; ++i) {
                     s[i] = gv[j][i] * s[i] + ev[j][i];
-                    ob[(size_t)(r0 + j) * kDD + i * kScanThreads] = s[i];
+                    if (seg_end) ob[os + i * kScanThreads] = s[i];
                 }
             }
         }
@@ -1169,14 +1183,28 @@ int tc_auto_splits(const Problem &p, int num_sms) {
     return (int)std::min<int64_t>(s, kMaxSplits);
 }
 
-size_t tc_workspace_bytes(const Problem &p, int splits) {
+int tc_state_pieces(const Problem &p, int splits, int num_sms) {
+    const int s = clamp_splits(p, splits);
+    if (s <= 1) return 1;
+    // Split each segment's state pass into consecutive pieces until its grid, like the output
+    // pass, fills the GPU in one wave; every piece keeps at least four chunks.
+    const int64_t bh = p.B * p.H;
+    const int64_t nchunks = (p.T + kC - 1) / kC;
+    int64_t k = num_sms / (bh * (s - 1));
+    k = std::min<int64_t>(k, nchunks / (4 * (int64_t)s));
+    return (int)std::max<int64_t>(1, std::min<int64_t>(k, kMaxPieces));
+}
+
+size_t tc_workspace_bytes(const Problem &p, int splits, int num_sms) {
     const int s = clamp_splits(p, splits);
     if (s <= 1) return 0;
     const size_t bh = (size_t)(p.B * p.H);
-    return bh * (size_t)(s - 1) * (2 * (size_t)kD * kD + kD) * sizeof(float);
+    const size_t k = (size_t)tc_state_pieces(p, splits, num_sms);
+    // E and Gamma of every piece, and the start state of every segment but the first
+    return bh * (size_t)(s - 1) * (k * ((size_t)kD * kD + kD) + (size_t)kD * kD) * sizeof(float);
 }
 
-cudaError_t launch_tc(const Problem &p, int splits, void *ws, size_t ws_bytes,
+cudaError_t launch_tc(const Problem &p, int splits, int num_sms, void *ws, size_t ws_bytes,
                       unsigned int *dev_err, cudaStream_t stream) {
     if (p.T == 0) return launch_exact(p, dev_err, stream);   // only hT = h0 to write
     const int s = clamp_splits(p, splits);
@@ -1197,6 +1225,7 @@ cudaError_t launch_tc(const Problem &p, int splits, void *ws, size_t ws_bytes,
     const int nchunks = (int)((p.T + kC - 1) / kC);
     const int bh = (int)(p.B * p.H);
     float *E = nullptr, *gam = nullptr, *sstart = nullptr;
+    const int pieces = tc_state_pieces(p, s, num_sms);
     // State-pass reads kept in L2 for the output pass, as a fraction of all of them; the last
     // segment (which gets none) is shortened by 15 % of that fraction.
     const int64_t per_chunk = 2 * 16384 + 32768;   // k, v, g bytes of one chunk
@@ -1204,15 +1233,17 @@ cudaError_t launch_tc(const Problem &p, int splits, void *ws, size_t ws_bytes,
     const double kept = s > 1 ? std::min(1.0, (double)kL2KeepBytes / (double)state_bytes) : 0.0;
     const int last16 = 16 - (int)(16.0 * 0.15 * kept + 0.5);
     if (s > 1) {
-        if (!ws || ws_bytes < tc_workspace_bytes(p, s)) return cudaErrorInvalidValue;
+        if (!ws || ws_bytes < tc_workspace_bytes(p, s, num_sms)) return cudaErrorInvalidValue;
         E = static_cast<float *>(ws);
-        sstart = E + (size_t)bh * (s - 1) * kD * kD;
-        gam = sstart + (size_t)bh * (s - 1) * kD * kD;
+        gam = E + (size_t)bh * (s - 1) * pieces * kD * kD;
+        sstart = gam + (size_t)bh * (s - 1) * pieces * kD;
         // keep about kL2KeepBytes of the state pass's last reads for the output kernel
         const int retain = (int)std::min<int64_t>(
-            (nchunks + s - 1) / s, kL2KeepBytes / ((int64_t)bh * (s - 1) * per_chunk));
-        StateArgs sa{E, gam, p.T, (int)p.H, nchunks, s, dev_err, retain, last16};
-        gla_tc_state_kernel<<<bh * (s - 1), kStateThreads, sm_::ALLOC, stream>>>(mk, mv, mg, sa);
+            ((nchunks + s - 1) / s + pieces - 1) / pieces,
+            kL2KeepBytes / ((int64_t)bh * (s - 1) * pieces * per_chunk));
+        StateArgs sa{E, gam, p.T, (int)p.H, nchunks, s, dev_err, retain, last16, pieces};
+        gla_tc_state_kernel<<<bh * (s - 1) * pieces, kStateThreads, sm_::ALLOC, stream>>>(mk, mv, mg,
+                                                                                      sa);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         // scan and output kernels are programmatic dependents: each may be scheduled while its
         // predecessor (one of ours) still runs, and waits for it in griddepcontrol.wait
@@ -1229,7 +1260,7 @@ cudaError_t launch_tc(const Problem &p, int splits, void *ws, size_t ws_bytes,
         cfg.attrs = pdl;
         cfg.numAttrs = 1;
         e = cudaLaunchKernelEx(&cfg, gla_tc_scan_kernel, (const float *)E, (const float *)gam,
-                               p.h0, sstart, s);
+                               p.h0, sstart, s, pieces);
         if (e != cudaSuccess) return e;
         count_launches(2);
     }
