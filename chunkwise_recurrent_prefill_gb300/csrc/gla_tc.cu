@@ -132,8 +132,8 @@ constexpr uint32_t GAM = P + 8192;      // [NR][128] f32 exp(L_c): renormalisati
 constexpr uint32_t GAM2 = GAM + NR * 512; // [NR][128] f32 exp(Bc) (extreme chunks)
 constexpr uint32_t ENDS = GAM2 + NR * 512; // [128] f32 exp(L) after the latest chunk
 constexpr uint32_t XF = ENDS + 512;     // [NR] u32 chunk flags: 1 = extreme, 2 = renormalise
-constexpr uint32_t XCH = XF + 64;       // [3][128] f32 token-range totals of the gate warps
-constexpr uint32_t SCR = XCH + 1536;    // [4][64] f32 exact-path scratch
+constexpr uint32_t XCH = XF + 64;       // [<=4][128] f32 token-range totals of the gate warps
+constexpr uint32_t SCR = XCH + 2048;    // [4][64] f32 exact-path scratch
 constexpr uint32_t BAR = SCR + 1024;    // mbarriers
 constexpr uint32_t NBAR = 24;
 constexpr uint32_t TSLOT = BAR + NBAR * 8;
@@ -148,10 +148,15 @@ enum {
 };
 static_assert(FIN < (int)om::NBAR, "output kernel barrier map");
 
-constexpr int kOutThreads = 512;       // 16 warps (4 per SM sub-partition: 128 registers)
-constexpr int kGateWarps = 6;          // warps 10..15
+constexpr int kGateWarps = 6;          // warps 10..15 (4 warps with kGatePart 32 measured
+                                       // 3-5% slower at B*H = 64 and 256, equal at 16)
+constexpr int kOutThreads = (10 + kGateWarps) * 32;   // at most 4 warps per SM
+                                                       // sub-partition: 128 registers
 constexpr int kGateThreads = kGateWarps * 32;
-constexpr int kGatePart = 24;          // tokens per gate thread (the last range has 16)
+constexpr int kGateParts = kGateThreads / 64;   // token ranges (one thread per key pair each)
+constexpr int kGatePart = 24;          // tokens per range (the last range takes the rest)
+static_assert(kGatePart * (kGateParts - 1) < 64 && kGatePart * kGateParts >= 64,
+              "gate token ranges must cover the chunk");
 constexpr int kStateThreads = 320;     // 10 warps
 
 struct OutArgs {
@@ -251,8 +256,8 @@ __device__ __forceinline__ void gate_cumsum(const float *gs, float *xch, int qq,
 __device__ __forceinline__ uint32_t par(int use) { return (uint32_t)use & 1u; }
 
 // ======================================================================= output kernel
-// Warp roles (16 warps): 0 TMA producer, 1 MMA scheduler (one thread), 2-5 epilogue,
-// 6-9 state + P conversion, 10-15 gate warps.
+// Warp roles (10 + kGateWarps warps): 0 TMA producer, 1 MMA scheduler (one thread), 2-5 epilogue,
+// 6-9 state + P conversion, the rest gate warps.
 __global__ void __launch_bounds__(kOutThreads, 1)
 gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg,
@@ -693,13 +698,13 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------------------ gate warps (6)
-        // Thread (part, dp) owns the key-dimension pair d = 2 dp, 2 dp + 1 over one of three
-        // token ranges of a chunk ([0,24), [24,48), [48,64)). Pass 1 sums the range's
+        // ------------------------------------------------------------ gate warps
+        // Thread (part, dp) owns the key-dimension pair d = 2 dp, 2 dp + 1 over one of the
+        // kGateParts token ranges of a chunk (kGatePart tokens each). Pass 1 sums the range's
         // log2-gates and records the range of the running sums; the ranges exchange totals,
         // and the warps agree on the chunk's flags (extreme, renormalise). Pass 2 recomputes
         // the running sums while scaling q and k in place, two dimensions per 32-bit access.
-        const int gt = (warp - 10) * 32 + lane;             // 0..191
+        const int gt = (warp - 10) * 32 + lane;             // 0 .. kGateThreads - 1
         const int dp = gt & 63, part = gt >> 6;
         const int tb = part * kGatePart;                    // first token of the range
         const int tl = min(kGatePart, kC - tb);             // tokens in the range
@@ -740,15 +745,17 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             }
             *reinterpret_cast<float2 *>(xch + part * kD + d) = make_float2(r0, r1);
             named_bar_sync(1, kGateThreads);
-            const float2 tA = *reinterpret_cast<const float2 *>(xch + d);           // range totals
-            const float2 tB = *reinterpret_cast<const float2 *>(xch + kD + d);
-            const float2 tC = *reinterpret_cast<const float2 *>(xch + 2 * kD + d);
-            const float ab0 = tA.x + tB.x, ab1 = tA.y + tB.y;
-            // b = off + (running sum within the range); the chunk total is formed by the same
-            // additions, so that b of the last token equals it exactly
-            const float off0 = part == 0 ? 0.f : (part == 1 ? tA.x : ab0);
-            const float off1 = part == 0 ? 0.f : (part == 1 ? tA.y : ab1);
-            const float B0 = ab0 + tC.x, B1 = ab1 + tC.y;   // chunk totals
+            // b = off + (running sum within the range), with off the left-to-right sum of the
+            // earlier ranges' totals; the chunk total is formed by the same additions, so that
+            // b of the last token equals it exactly
+            float off0 = 0.f, off1 = 0.f, B0 = 0.f, B1 = 0.f;
+#pragma unroll
+            for (int q = 0; q < kGateParts; ++q) {
+                const float2 t = *reinterpret_cast<const float2 *>(xch + q * kD + d);
+                if (q == part) { off0 = B0; off1 = B1; }
+                B0 = q == 0 ? t.x : B0 + t.x;
+                B1 = q == 0 ? t.y : B1 + t.y;
+            }
             // largest |b| over this thread's tokens (attained at an end of the range)
             const float mx = fmaxf(fmaxf(fabsf(off0 + lo0), fabsf(off0 + hi0)),
                                    fmaxf(fabsf(off1 + lo1), fabsf(off1 + hi1)));
