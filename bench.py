@@ -51,6 +51,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU work of the oracle baseline sample")
+    ap.add_argument("--op", default="prefill", choices=["prefill", "step"],
+                    help="prefill (the headline) or one decode step on a resident state")
     return ap.parse_args()
 
 
@@ -405,6 +407,78 @@ def run_e2e(args, w, x_cpu, dev, stream, gla, world, dist):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
 
 
+def run_step(args, rank, world, dist):
+    """One decode step per timed iteration on the decode workload: every step reads and
+    rewrites the whole fp32 state, so the bound is HBM bandwidth."""
+    import torch
+    from chunkwise_recurrent_prefill_gb300 import gla
+    from chunkwise_recurrent_prefill_gb300.workloads import STEP_WORKLOAD, make_step_inputs
+    sw = STEP_WORKLOAD
+    B, H, D = sw["B"], sw["H"], sw["D"]
+    gla.load_library()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    x = make_step_inputs(B, H, D, sw["io"], sw["seed"], dev)
+    o = torch.empty_like(x["v"])
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        gla.gla_step(x["q"], x["k"], x["v"], x["g"], x["scale"], x["S"], o=o, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert gla.last_device_status() == 0
+    gid = str(torch.cuda.get_device_properties(dev).uuid)
+    sampler = ClockSampler(gid if gid.startswith("GPU-") else "GPU-" + gid)
+    sampler.start()
+    time.sleep(0.3)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = gla.launch_counter()
+    t_lo = time.time()
+    for i in range(args.steps):
+        flush.zero_()
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    t_hi = time.time()
+    launches = gla.launch_counter() - launches0
+    time.sleep(0.2)
+    sampler.mark(t_lo, t_hi)
+    sampler.stop()
+    ms = sorted(a.elapsed_time(b) for a, b in evs)
+    total_s = max_over_ranks(sum(ms) / 1e3, dist, dev)
+    per = total_s / args.steps
+    es = 2
+    nbytes = B * H * (2 * D * D * 4 + 2 * D * es + 2 * D * es + D * 4)
+    hbm_gbs, _, peak_src = load_peaks()
+    achieved = nbytes / per / 1e9
+    if rank == 0:
+        print(json.dumps({
+            "metric": "GLA decode step tokens/s (one token for each of B=64 sequences, H=16, "
+                      "D=128, bf16 q/k/v/o, fp32 state)",
+            "value": weak_scaling_value(B, args.steps, world, total_s), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * per, "ms_p50": ms[len(ms) // 2],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded N(0,1) q/k/v, logsigmoid(N(0,1))/16 gates, 0.02 N(0,1) state)",
+            "config": {"workload": sw["name"], "B": B, "H": H, "Dk": D, "Dv": D, "io": sw["io"],
+                       "l2": "flushed by a 256 MiB device write before every timed step"},
+            "clocks": sampler.summary(), "gpu_launches": launches,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                         "frac": achieved / hbm_gbs, "traffic": None,
+                         "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst)",
+                         "algorithmic_bytes_per_launch": nbytes, "kernel": "step"},
+            "e2e": None, "cpu_baseline": None,
+        }), flush=True)
+
+
 def main():
     args = parse_args()
     from chunkwise_recurrent_prefill_gb300.workloads import BENCH_WORKLOAD, WORKLOADS
@@ -425,7 +499,10 @@ def main():
     else:
         torch.cuda.set_device(0)
     try:
-        run_ours(args, w, rank, world, dist)
+        if args.op == "step":
+            run_step(args, rank, world, dist)
+        else:
+            run_ours(args, w, rank, world, dist)
     finally:
         if dist:
             dist.destroy_process_group()

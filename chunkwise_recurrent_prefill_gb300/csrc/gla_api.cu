@@ -277,6 +277,43 @@ gla_status gla_fwd_f32(const float *q, const float *k, const float *v, const flo
                       stream);
 }
 
+gla_status gla_step(const void *q, const void *k, const void *v, const float *g_log, float scale,
+                    float *S, void *o, int64_t B, int64_t H, int64_t Dk, int64_t Dv, int io,
+                    gla_stream_t stream) {
+    // one token: the shapes of gla_fwd_ex with T = 1; S plays h0 (in) and hT (out)
+    Sizes sz;
+    gla_status rc = validate_shape(B, 1, H, Dk, Dv, io, &sz);
+    if (rc != GLA_OK) return rc;
+    if (!gla::step_supported(Dk, Dv)) return GLA_ERR_UNSUPPORTED_DIM;
+    const bool empty = (sz.nqk == 0);
+    if (!empty && (!q || !k || !v || !g_log || !S || !o)) return GLA_ERR_NULL_ARG;
+    if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(g_log) || misaligned(S) ||
+        misaligned(o))
+        return GLA_ERR_MISALIGNED;
+    const size_t es = io == GLA_IO_BF16 ? 2 : 4;
+    const size_t bqk = (size_t)sz.nqk * es, bv = (size_t)sz.nv * es;
+    const size_t bg = (size_t)sz.nqk * 4, bs = (size_t)sz.nstate * 4;
+    const void *ins[4] = {q, k, v, g_log};
+    const size_t nins[4] = {bqk, bqk, bv, bg};
+    for (int i = 0; i < 4; ++i) {
+        if (overlap(o, bv, ins[i], nins[i]) || overlap(S, bs, ins[i], nins[i]))
+            return GLA_ERR_ALIAS;
+    }
+    if (overlap(o, bv, S, bs)) return GLA_ERR_ALIAS;
+    DeviceState *st = nullptr;
+    rc = current_device(&st);
+    if (rc != GLA_OK) return rc;
+    if (empty) return GLA_OK;
+    const cudaError_t e = gla::launch_step(q, k, v, g_log, scale, S, o, B * H, Dk, Dv, io,
+                                           reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        set_detail("decode step launch", e);
+        return GLA_ERR_LAUNCH;
+    }
+    return GLA_OK;
+}
+
 gla_status gla_last_device_status(gla_stream_t stream) {
     DeviceState *st = nullptr;
     gla_status rc = current_device(&st);

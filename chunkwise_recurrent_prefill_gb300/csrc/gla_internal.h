@@ -35,6 +35,12 @@ void set_error_detail(const char *text);
 bool exact_supported(int64_t Dk, int64_t Dv);
 cudaError_t launch_exact(const Problem &p, unsigned int *dev_err, cudaStream_t s);
 
+// One decode step on a resident state (any io, 1 <= Dk <= 1024, Dv a multiple of 4 <= 1024).
+bool step_supported(int64_t Dk, int64_t Dv);
+cudaError_t launch_step(const void *q, const void *k, const void *v, const float *g, float scale,
+                        float *S, void *o, int64_t BH, int64_t Dk, int64_t Dv, int io,
+                        cudaStream_t stream);
+
 // tcgen05 path (bf16 io, Dk = Dv = 128).
 bool tc_supported(const Problem &p);
 int tc_auto_splits(const Problem &p, int num_sms);

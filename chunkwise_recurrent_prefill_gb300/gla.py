@@ -59,6 +59,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.gla_fwd_ex.argtypes = sig + [ctypes.c_int, ctypes.POINTER(_Options), vp]
             for f in (lib.gla_fwd, lib.gla_fwd_f32, lib.gla_fwd_ex):
                 f.restype = ctypes.c_int
+            lib.gla_step.argtypes = [vp, vp, vp, vp, f32, vp, vp, i64, i64, i64, i64,
+                                     ctypes.c_int, vp]
+            lib.gla_step.restype = ctypes.c_int
             lib.gla_fwd_noalloc.argtypes = sig + [ctypes.c_int, vp]
             lib.gla_fwd_noalloc.restype = ctypes.c_int
             lib.gla_fwd_workspace_size.argtypes = [i64, i64, i64, i64, i64, ctypes.c_int,
@@ -200,6 +203,36 @@ def gla_fwd_noalloc(q, k, v, g, scale: float, h0=None, *, o, hT=None, seq_splits
         detail = lib.gla_last_error_detail().decode() if rc in (6, 9) else ""
         raise GLAError(rc, "gla_fwd_noalloc", detail)
     return o, hT
+
+
+def gla_step(q, k, v, g, scale: float, S, *, o=None, stream=None):
+    """One decode step through ``gla_step``: q, k [B,H,Dk]; v [B,H,Dv] (all bf16, or all
+    float32); g [B,H,Dk] float32 log-gates; S [B,H,Dk,Dv] float32, updated in place
+    (S <- diag(exp(g)) S + k^T v). Returns o = scale q S [B,H,Dv] (same dtype as q)."""
+    lib = load_library()
+    if q.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("q/k/v must be bfloat16 or float32")
+    B, H, Dk = q.shape
+    Dv = v.shape[-1]
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("tensors must be on a CUDA device")
+    _check(k, "k", q.dtype, (B, H, Dk), dev)
+    _check(v, "v", q.dtype, (B, H, Dv), dev)
+    _check(g, "g", torch.float32, (B, H, Dk), dev)
+    _check(S, "S", torch.float32, (B, H, Dk, Dv), dev)
+    if o is None:
+        o = torch.empty((B, H, Dv), dtype=q.dtype, device=dev)
+    else:
+        _check(o, "o", q.dtype, (B, H, Dv), dev)
+    io = IO_BF16 if q.dtype == torch.bfloat16 else IO_F32
+    with torch.cuda.device(dev):
+        rc = lib.gla_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), ctypes.c_float(scale), _ptr(S),
+                          _ptr(o), B, H, Dk, Dv, io, _stream_handle(stream))
+    if rc != GLA_OK:
+        detail = lib.gla_last_error_detail().decode() if rc == 6 else ""
+        raise GLAError(rc, "gla_step", detail)
+    return o
 
 
 def launch_counter() -> int:

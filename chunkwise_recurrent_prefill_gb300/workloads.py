@@ -90,3 +90,23 @@ def small(name: str, B: int, T: int, H: int, io: str = "bf16", seed: int = 0,
     """An ad-hoc workload with the same distributions (tests use these for edge cases)."""
     return Workload(name, B=B, T=T, H=H, Dk=Dk, Dv=Dv, io=io, seed=seed, with_h0=with_h0,
                     want_hT=True)
+
+
+# Decode-step workload: one token for each of B sequences and H heads on a resident state
+# (the step after prefill). Same recipe: q, k, v, u, then the state S = 0.02 * N(0, 1).
+STEP_WORKLOAD = dict(name="decode_B64_H16_D128", B=64, H=16, D=128, io="bf16", seed=5)
+
+
+def make_step_inputs(B: int, H: int, D: int, io: str = "bf16", seed: int = 0,
+                     device: torch.device | str = "cpu") -> dict:
+    """q, k [B,H,D], v [B,H,D] (io dtype), g [B,H,D] float32, S [B,H,D,D] float32."""
+    gen = torch.Generator("cpu").manual_seed(seed)
+    dt = torch.bfloat16 if io == "bf16" else torch.float32
+    q = torch.randn(B, H, D, generator=gen).to(dt)
+    k = torch.randn(B, H, D, generator=gen).to(dt)
+    v = torch.randn(B, H, D, generator=gen).to(dt)
+    g = F.logsigmoid(torch.randn(B, H, D, generator=gen)) / 16
+    S = 0.02 * torch.randn(B, H, D, D, generator=gen)
+    x = dict(q=q, k=k, v=v, g=g, S=S, scale=D ** -0.5)
+    return {n: (t.to(device) if isinstance(t, torch.Tensor) else t) for n, t in x.items()}
+

@@ -107,6 +107,22 @@ gla_status gla_fwd_ex(const void *q, const void *k, const void *v, const float *
                       int64_t B, int64_t T, int64_t H, int64_t Dk, int64_t Dv,
                       int io, const gla_options *opt, gla_stream_t stream);
 
+/*
+ * gla_step — one decode step on a resident state: the token update of the recurrence above,
+ * applied once (update first, then the read), for every batch and head:
+ *     S <- diag(exp(g_log)) . S + k^T v,    o = scale . q . S
+ * It continues a prefill: pass the hT that gla_fwd wrote as S ("Linear Attention 在 GPU 上到底
+ * 慢在哪", section 学长的反馈, names decoding as the step that follows the prefill).
+ * Layouts (one token, contiguous): q, k, g_log [B, H, Dk]; v, o [B, H, Dv]; S [B, H, Dk, Dv]
+ * fp32, read and overwritten in place. io = GLA_IO_BF16 (bf16 q, k, v, o) or GLA_IO_F32;
+ * g_log and S are fp32 either way. 1 <= Dk <= 1024; 4 <= Dv <= 1024 with Dv a multiple of 4
+ * (GLA_ERR_UNSUPPORTED_DIM otherwise). Device pointers, 16-byte aligned; o
+ * and S must not overlap each other or any input. fp32 arithmetic; deterministic.
+ */
+gla_status gla_step(const void *q, const void *k, const void *v, const float *g_log, float scale,
+                    float *S, void *o, int64_t B, int64_t H, int64_t Dk, int64_t Dv, int io,
+                    gla_stream_t stream);
+
 /* Bytes of device workspace gla_fwd_ex needs for this shape and options (0 if none).
  * Returns 0 as well for arguments it would reject. */
 size_t gla_fwd_workspace_size(int64_t B, int64_t T, int64_t H, int64_t Dk, int64_t Dv,

@@ -96,3 +96,25 @@ def test_binding_refuses_cpu_tensors(lib):
     x = torch.zeros(1, 4, 1, 128)
     with pytest.raises(ValueError):
         gla_fwd(x, x, x, x, 1.0)
+
+
+def _step(lib, q=0x1000000000, k=0x2000000000, v=0x3000000000, g=0x4000000000,
+          S=0x5000000000, o=0x6000000000, B=1, H=2, Dk=128, Dv=128, io=0):
+    p = lambda x: None if x is None else ctypes.c_void_p(x)  # noqa: E731
+    return lib.gla_step(p(q), p(k), p(v), p(g), ctypes.c_float(1.0), p(S), p(o), B, H, Dk, Dv,
+                        io, None)
+
+
+def test_step_validation(lib):
+    from chunkwise_recurrent_prefill_gb300.gla import load_library
+    load_library()   # sets the argument types
+    assert _step(lib, q=None) == 1                      # GLA_ERR_NULL_ARG
+    assert _step(lib, S=None) == 1
+    assert _step(lib, B=-1) == 2                        # GLA_ERR_BAD_SHAPE
+    assert _step(lib, Dk=0) == 3                        # GLA_ERR_UNSUPPORTED_DIM
+    assert _step(lib, Dv=2048) == 3
+    assert _step(lib, Dv=6) == 3                        # not a multiple of 4
+    assert _step(lib, v=0x3000000008) == 4              # GLA_ERR_MISALIGNED
+    assert _step(lib, o=0x5000000000 + 256) == 5        # o inside S: GLA_ERR_ALIAS
+    assert _step(lib, S=0x4000000000) == 5              # S over g
+    assert _step(lib, io=7) == 10                       # GLA_ERR_BAD_OPTION
