@@ -62,7 +62,8 @@ def algorithmic_bytes(w) -> int:
     """Bytes a forward must move at least: q, k, v read, o written (io dtype), g read
     (fp32), plus h0 read / hT written when the workload carries them."""
     es = 2 if w.io == "bf16" else 4
-    per_token_head = 2 * w.Dk * es + w.Dv * es + w.Dv * es + w.Dk * 4
+    gate_bytes = w.Dk * 4 if getattr(w, "gate", "key") == "key" else 4
+    per_token_head = 2 * w.Dk * es + w.Dv * es + w.Dv * es + gate_bytes
     n = w.B * w.T * w.H * per_token_head
     state = w.B * w.H * w.Dk * w.Dv * 4
     return n + (state if w.with_h0 else 0) + (state if w.want_hT else 0)
@@ -175,6 +176,13 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ arms
 
+def per_key_gates(w, g):
+    """The oracle's gate layout [B,T,H,Dk]: a scalar gate is the same in every key dim."""
+    if getattr(w, "gate", "key") == "key":
+        return g.numpy()
+    return g[..., None].expand(*g.shape, w.Dk).contiguous().numpy()
+
+
 def cpu_oracle_sample(w, x_cpu, target_s: float):
     """Time the fp64 C oracle on a bounded sample of the workload: the first T_s tokens of
     every (batch, head) pair, repeated until ~target_s of CPU time has been spent (T_s is the
@@ -185,7 +193,7 @@ def cpu_oracle_sample(w, x_cpu, target_s: float):
     q = x_cpu["q"].float().numpy()
     k = x_cpu["k"].float().numpy()
     v = x_cpu["v"].float().numpy()
-    g = x_cpu["g"].numpy()
+    g = per_key_gates(w, x_cpu["g"])
     h0 = None if x_cpu["h0"] is None else x_cpu["h0"].numpy()
     cal_T = min(w.T, 256)
     t0 = time.perf_counter()
@@ -217,7 +225,7 @@ def run_reference(args, w, rank, world):
     q = x["q"].float().numpy()
     k = x["k"].float().numpy()
     v = x["v"].float().numpy()
-    g = x["g"].numpy()
+    g = per_key_gates(w, x["g"])
     h0 = None if x["h0"] is None else x["h0"].numpy()
     # size each step so that warmup + steps take ~150 s of CPU time in total
     cal_T = min(w.T, 128)
@@ -268,7 +276,9 @@ def workload_config(w, path):
     l2 = ("n/a (host CPU)" if path == "oracle"
           else "flushed by a 256 MiB device write before every timed step")
     return {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "Dk": w.Dk, "Dv": w.Dv,
-            "io": w.io, "gate": "fp32 log-gate logsigmoid(u)/16", "path": path,
+            "io": w.io, "gate": ("fp32 log-gate logsigmoid(u)/16, "
+                                 + ("one per key dim" if w.gate == "key" else "one per token and head")),
+            "path": path,
             "h0": w.with_h0, "hT": w.want_hT, "l2": l2}
 
 
@@ -290,7 +300,7 @@ def run_ours(args, w, rank, world, dist):
 
     def step():
         gla.gla_fwd(x["q"], x["k"], x["v"], x["g"], x["scale"], x["h0"], o=o, hT=hT,
-                    path=args.path, seq_splits=args.seq_splits, stream=stream)
+                    path=args.path, seq_splits=args.seq_splits, gate=w.gate, stream=stream)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -386,7 +396,8 @@ def run_e2e(args, w, x_cpu, dev, stream, gla, world, dist):
             if host[k_] is not None:
                 dbuf[k_].copy_(host[k_], non_blocking=True)
         gla.gla_fwd(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["g"], x_cpu["scale"], dbuf["h0"],
-                    o=o, hT=hT, path=args.path, seq_splits=args.seq_splits, stream=stream)
+                    o=o, hT=hT, path=args.path, seq_splits=args.seq_splits, gate=w.gate,
+                    stream=stream)
         o_host.copy_(o, non_blocking=True)
         if hT is not None:
             hT_host.copy_(hT, non_blocking=True)

@@ -102,7 +102,7 @@ gla_status validate_shape(int64_t B, int64_t T, int64_t H, int64_t Dk, int64_t D
 
 gla_status validate(const void *q, const void *k, const void *v, const float *g,
                     const float *h0, const void *o, const float *hT, int64_t B, int64_t T,
-                    int64_t H, int64_t Dk, int64_t Dv, int io, Sizes *sz) {
+                    int64_t H, int64_t Dk, int64_t Dv, int io, int gate, Sizes *sz) {
     gla_status rc = validate_shape(B, T, H, Dk, Dv, io, sz);
     if (rc != GLA_OK) return rc;
     const bool empty = (sz->nqk == 0);
@@ -112,7 +112,8 @@ gla_status validate(const void *q, const void *k, const void *v, const float *g,
         return GLA_ERR_MISALIGNED;
     const size_t es = io == GLA_IO_BF16 ? 2 : 4;
     const size_t bqk = (size_t)sz->nqk * es, bv = (size_t)sz->nv * es;
-    const size_t bg = (size_t)sz->nqk * 4, bs = (size_t)sz->nstate * 4;
+    const size_t bg = (size_t)(gate == GLA_GATE_SCALAR ? sz->nqk / Dk : sz->nqk) * 4;
+    const size_t bs = (size_t)sz->nstate * 4;
     const void *ins[5] = {q, k, v, g, h0};
     const size_t nins[5] = {bqk, bqk, bv, bg, bs};
     for (int i = 0; i < 5; ++i) {
@@ -219,9 +220,11 @@ gla_status gla_fwd_ex(const void *q, const void *k, const void *v, const float *
                       int64_t H, int64_t Dk, int64_t Dv, int io, const gla_options *opt,
                       gla_stream_t stream) {
     Sizes sz;
-    gla_status rc = validate(q, k, v, g_log, h0, o, hT, B, T, H, Dk, Dv, io, &sz);
+    const int gate = opt ? opt->gate : GLA_GATE_KEY;
+    if (gate != GLA_GATE_KEY && gate != GLA_GATE_SCALAR) return GLA_ERR_BAD_OPTION;
+    gla_status rc = validate(q, k, v, g_log, h0, o, hT, B, T, H, Dk, Dv, io, gate, &sz);
     if (rc != GLA_OK) return rc;
-    gla::Problem p{q, k, v, g_log, scale, h0, o, hT, B, T, H, Dk, Dv, io};
+    gla::Problem p{q, k, v, g_log, scale, h0, o, hT, B, T, H, Dk, Dv, io, gate};
     const int path = resolve_path(opt, p);
     if (path != GLA_PATH_EXACT && path != GLA_PATH_TC) return GLA_ERR_BAD_OPTION;
     if (opt && opt->seq_splits < 0) return GLA_ERR_BAD_OPTION;

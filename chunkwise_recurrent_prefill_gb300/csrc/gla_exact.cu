@@ -2,7 +2,7 @@
 //
 // The chunk steps of "线性注意力GPU算子库的定义与技术解析", section 四, in plain fp32:
 // per chunk of C = 64 tokens, b = in-chunk inclusive cumulative log-gate (a Dk vector
-// per token), then
+// per token; a scalar gate is the same value in every key dimension), then
 //     P_ij   = sum_d q_id k_jd exp(b_id - b_jd)   for j <= i    (decay-masked q.k^T)
 //     o_i    = scale * ( sum_{j<=i} P_ij v_j + (q_i * exp(b_i)) . S )
 //     S     <- diag(exp(b_last)) S + sum_j (k_j * exp(b_last - b_j))^T v_j
@@ -43,7 +43,8 @@ template <typename IO, int DK, int DV>
 __global__ void __launch_bounds__(kThreads)
 gla_exact_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO *__restrict__ v,
                  const float *__restrict__ g, float scale, const float *__restrict__ h0,
-                 IO *__restrict__ o, float *__restrict__ hT, int64_t T, int64_t H) {
+                 IO *__restrict__ o, float *__restrict__ hT, int64_t T, int64_t H,
+                 int gate_scalar) {
     constexpr int KS = DK + 1;
     extern __shared__ float sm[];
     float *qs = sm;                 // [C][KS]  q, later q * exp(b)
@@ -73,7 +74,7 @@ gla_exact_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO *_
                 const int64_t idx = ((b * T + t0 + t) * H + h) * DK + d;
                 qv = to_f(q[idx]);
                 kv = to_f(k[idx]);
-                gv = g[idx];
+                gv = gate_scalar ? g[(b * T + t0 + t) * H + h] : g[idx];
             }
             qs[t * KS + d] = qv;
             ks[t * KS + d] = kv;
@@ -148,7 +149,7 @@ cudaError_t launch_typed(const Problem &p, cudaStream_t s) {
     dim3 grid((unsigned)(p.B * p.H), DV / kVB);
     kern<<<grid, kThreads, smem, s>>>(static_cast<const IO *>(p.q), static_cast<const IO *>(p.k),
                                       static_cast<const IO *>(p.v), p.g, p.scale, p.h0,
-                                      static_cast<IO *>(p.o), p.hT, p.T, p.H);
+                                      static_cast<IO *>(p.o), p.hT, p.T, p.H, p.gate);
     e = cudaGetLastError();
     if (e == cudaSuccess) count_launches(1);
     return e;

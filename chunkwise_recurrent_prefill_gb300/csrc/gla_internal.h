@@ -17,6 +17,7 @@ struct Problem {
     float *hT;               // [B,H,Dk,Dv] or nullptr
     int64_t B, T, H, Dk, Dv;
     int io;                  // GLA_IO_BF16 / GLA_IO_F32
+    int gate;                // GLA_GATE_KEY: g [B,T,H,Dk]; GLA_GATE_SCALAR: g [B,T,H]
 };
 
 // Bits of the device error word kernels may raise (never trap).

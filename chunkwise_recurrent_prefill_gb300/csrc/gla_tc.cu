@@ -133,7 +133,8 @@ constexpr uint32_t GAM2 = GAM + NR * 512; // [NR][128] f32 exp(Bc) (extreme chun
 constexpr uint32_t ENDS = GAM2 + NR * 512; // [128] f32 exp(L) after the latest chunk
 constexpr uint32_t XF = ENDS + 512;     // [NR] u32 chunk flags: 1 = extreme, 2 = renormalise
 constexpr uint32_t XCH = XF + 64;       // [<=4][128] f32 token-range totals of the gate warps
-constexpr uint32_t SCR = XCH + 2048;    // [4][64] f32 exact-path scratch
+constexpr uint32_t GSC = XCH + 2048;    // [2][64] f32 scalar gates of two chunks (scalar mode)
+constexpr uint32_t SCR = GSC + 512;     // [4][64] f32 exact-path scratch
 constexpr uint32_t BAR = SCR + 1024;    // mbarriers
 constexpr uint32_t NBAR = 24;
 constexpr uint32_t TSLOT = BAR + NBAR * 8;
@@ -182,6 +183,7 @@ struct StateArgs {
     int retain;                        // chunks per CTA (read last) loaded with evict_last
     int last16;                        // weight of the last segment in 16ths (see seg_bound)
     int pieces;                        // consecutive pieces per segment, one CTA each
+    const float *g;                    // scalar log-gates [B,T,H] (scalar mode only)
 };
 
 // Chunk range [cb, ce) of segment `seg`. Every segment weighs 16 except the last, which
@@ -252,12 +254,38 @@ __device__ __forceinline__ void gate_cumsum(const float *gs, float *xch, int qq,
     }
 }
 
+// gate_cumsum for a scalar gate: gs holds the chunk's 64 per-token log-gates, the same in
+// every key dimension (so both columns of the pair see them).
+__device__ __forceinline__ void gate_cumsum_scalar(const float *gs, float *xch, int qq, int d,
+                                                   float (&b0)[16], float (&b1)[16],
+                                                   uint32_t bar) {
+    float a0 = 0.f;
+#pragma unroll
+    for (int x = 0; x < 16; ++x) {
+        a0 = fmaf(gs[16 * qq + x], kLog2e, a0);
+        b0[x] = a0;
+        b1[x] = a0;
+    }
+    *reinterpret_cast<float2 *>(xch + qq * kD + d) = make_float2(a0, a0);
+    named_bar_sync(bar, 256);
+    float o0 = 0.f;
+    for (int q2 = 0; q2 < qq; ++q2) o0 += xch[q2 * kD + d];
+#pragma unroll
+    for (int x = 0; x < 16; ++x) {
+        b0[x] += o0;
+        b1[x] += o0;
+    }
+}
+
 // Phase parity of the k-th use of a ring slot.
 __device__ __forceinline__ uint32_t par(int use) { return (uint32_t)use & 1u; }
 
 // ======================================================================= output kernel
 // Warp roles (10 + kGateWarps warps): 0 TMA producer, 1 MMA scheduler (one thread), 2-5 epilogue,
 // 6-9 state + P conversion, the rest gate warps.
+// kScalar: one log-gate per token and head (g [B,T,H]) instead of one per key dimension; the
+// gates are then read by the gate warps straight from global memory, a chunk ahead.
+template <bool kScalar>
 __global__ void __launch_bounds__(kOutThreads, 1)
 gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg,
@@ -324,7 +352,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             // every tile is read here for the last time: do not let it displace the chunks
             // the state kernel left in L2 for this kernel
             const uint64_t pol = l2_policy_evict_first();
-            int ng = 0, nq = 0;
+            int ng = kScalar ? n : 0, nq = 0;   // scalar gates are not staged by TMA
             uint32_t idle = 0;
             uint64_t t_idle = 0;
             while (ng < n || nq < n) {
@@ -375,7 +403,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 const int uses = nq > i ? (nq - 1 - i) / NQ + 1 : 0;
                 if (uses > 0 && !mbar_wait(&bars[QFULL + i], par(uses - 1))) ok = false;
             }
-            for (int i = 0; i < NG; ++i) {
+            for (int i = 0; i < NG && !kScalar; ++i) {
                 const int uses = ng > i ? (ng - 1 - i) / NG + 1 : 0;
                 if (uses > 0 && !mbar_wait(&bars[GFULL + i], par(uses - 1))) ok = false;
             }
@@ -638,7 +666,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                         const int64_t t = t0 + st_t;
                         const bool in = t < a.T;
                         const int64_t idx = (((int64_t)bidx * a.T + t) * a.H + h) * kD + d;
-                        gcol[st_t] = in ? a.g[idx] : 0.f;
+                        gcol[st_t] = in ? (kScalar ? a.g[idx / kD] : a.g[idx]) : 0.f;
                         qcol[st_t] = in ? __bfloat162float(a.q[idx]) : 0.f;
                         kcol[st_t] = in ? __bfloat162float(a.k[idx]) : 0.f;
                     }
@@ -722,19 +750,45 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         const float lsc = log2f(sc);                        // folded into the q exponent
         float *xch = reinterpret_cast<float *>(sm + XCH);   // [3][128] range totals
         float L0 = 0.f, L1 = 0.f;   // log2 decay of the normalised state (S = 2^L S~)
+        // scalar gates: thread gt < 64 fetches token gt of the next chunk into gpre; at the top
+        // of each chunk they are published in gsc[c & 1] (two buffers: no thread is ever more
+        // than one chunk behind another, the loop has several barriers per chunk)
+        float *gsc = reinterpret_cast<float *>(sm + GSC);
+        auto fetch_scalar = [&](int c) -> float {
+            const int64_t t = (int64_t)(cb + c) * kC + gt;
+            return t < a.T ? __ldg(a.g + ((int64_t)bidx * a.T + t) * a.H + h) : 0.f;
+        };
+        float gpre = (kScalar && gt < kC && n > 0) ? fetch_scalar(0) : 0.f;
         for (int c = 0; c < n; ++c) {
             const int gs = c % NG, qs = c % NQ, slot = c & (NR - 1);
-            bool w = mbar_wait(&bars[GFULL + gs], par(c / NG));
-            if (named_bar_or(1, kGateThreads, !w)) { ok = false; break; }
+            bool w = true;
+            if (kScalar) {
+                if (gt < kC) {
+                    gsc[(c & 1) * kC + gt] = gpre;
+                    if (c + 1 < n) gpre = fetch_scalar(c + 1);
+                }
+                named_bar_sync(1, kGateThreads);
+            } else {
+                w = mbar_wait(&bars[GFULL + gs], par(c / NG));
+                if (named_bar_or(1, kGateThreads, !w)) { ok = false; break; }
+            }
             if (gt == 0) TRACE_OUT(16, c);
             const float *grow = reinterpret_cast<const float *>(sm + G + gs * GSLOT) + tb * kD + d;
+            const float *gsrow = gsc + (c & 1) * kC + tb;   // scalar gates of this thread's range
+            auto gpair = [&](int t) -> float2 {
+                if (kScalar) {
+                    const float x = gsrow[t];
+                    return make_float2(x, x);
+                }
+                return *reinterpret_cast<const float2 *>(grow + t * kD);
+            };
             float r0 = 0.f, r1 = 0.f;
             float lo0 = 0.f, hi0 = 0.f, lo1 = 0.f, hi1 = 0.f;   // range of the running sums
 #pragma unroll 1
             for (int t0 = 0; t0 < tl; t0 += kGateBlock) {
                 float2 gv[kGateBlock];
 #pragma unroll
-                for (int x = 0; x < kGateBlock; ++x) gv[x] = *reinterpret_cast<const float2 *>(grow + (t0 + x) * kD);
+                for (int x = 0; x < kGateBlock; ++x) gv[x] = gpair(t0 + x);
 #pragma unroll
                 for (int x = 0; x < kGateBlock; ++x) {
                     r0 = fmaf(gv[x].x, kLog2e, r0);
@@ -797,7 +851,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
 #pragma unroll
                     for (int x = 0; x < kGateBlock; ++x) {
                         const uint32_t off = (uint32_t)(tb + t0) * 128u + swz[x];
-                        gv[x] = *reinterpret_cast<const float2 *>(grow + (t0 + x) * kD);
+                        gv[x] = gpair(t0 + x);
                         qv[x] = *reinterpret_cast<const uint32_t *>(qt + off);
                         kv[x] = *reinterpret_cast<const uint32_t *>(kt + off);
                     }
@@ -826,7 +880,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
 #pragma unroll
                     for (int x = 0; x < kGateBlock; ++x) {
                         const uint32_t off = (uint32_t)(tb + t0) * 128u + swz[x];
-                        gv[x] = *reinterpret_cast<const float2 *>(grow + (t0 + x) * kD);
+                        gv[x] = gpair(t0 + x);
                         qv[x] = *reinterpret_cast<const uint32_t *>(qt + off);
                         kv[x] = *reinterpret_cast<const uint32_t *>(kt + off);
                     }
@@ -848,7 +902,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[GEMPTY + gs]);   // the g slot may be refilled
+            if (!kScalar && lane == 0) mbar_arrive(&bars[GEMPTY + gs]);   // the g slot may be refilled
             if (gt == 0) xf[slot] = (ext ? 1u : 0u) | (ren ? 2u : 0u);
             fence_proxy_async_smem();
             __syncwarp();
@@ -878,7 +932,8 @@ constexpr uint32_t K = 0, V = 16384, KVSTAGE = 32768;
 constexpr uint32_t G = NKV * KVSTAGE, GSLOT = 32768;
 constexpr uint32_t BV = G + NG * GSLOT;  // [128] f32 chunk totals
 constexpr uint32_t XCH = BV + 512;       // [4][128] f32
-constexpr uint32_t BAR = XCH + 2048;
+constexpr uint32_t GSC = XCH + 2048;     // [2][64] f32 scalar gates of two chunks (scalar mode)
+constexpr uint32_t BAR = GSC + 512;
 constexpr uint32_t NBAR = 17;
 constexpr uint32_t TSLOT = BAR + NBAR * 8;
 constexpr uint32_t ALLOC = TSLOT + 16 + 1024;
@@ -890,6 +945,7 @@ constexpr uint32_t ALLOC = TSLOT + 16 + 1024;
 enum { SKFULL = 0, SKEMPTY = 4, SGFULL = 8, SGEMPTY = 10, SGDONE = 12, SEDONE = 16 };
 static_assert(SGDONE + sm_::NKV <= SEDONE, "state-kernel barrier map");
 
+template <bool kScalar>
 __global__ void __launch_bounds__(kStateThreads, 1)
 gla_tc_state_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                     const __grid_constant__ CUtensorMap tg, const StateArgs a) {
@@ -950,7 +1006,7 @@ gla_tc_state_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
             // The chunks this CTA reads last (the first ones of its segment) are the ones the
             // output kernel reads first: keep them in L2 ahead of the rest.
             const uint64_t keep = l2_policy_evict_last(), drop = l2_policy_evict_first();
-            int ng = 0, nk = 0;
+            int ng = kScalar ? n : 0, nk = 0;   // scalar gates are not staged by TMA
             uint32_t idle = 0;
             uint64_t t_idle = 0;
             while (ng < n || nk < n) {
@@ -990,7 +1046,7 @@ gla_tc_state_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
                     }
                 }
             }
-            for (int i = 0; i < NG; ++i) {
+            for (int i = 0; i < NG && !kScalar; ++i) {
                 const int uses = ng > i ? (ng - 1 - i) / NG + 1 : 0;
                 if (uses > 0 && !mbar_wait(&bars[SGFULL + i], par(uses - 1))) ok = false;
             }
@@ -1027,19 +1083,38 @@ gla_tc_state_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
         const uint32_t boxo = (uint32_t)(p >> 5) * 8192;
         const uint32_t col = (uint32_t)(d & 63);
         float l0 = 0.f, l1 = 0.f;   // log2 decay from this chunk's end to the segment end
+        // scalar gates: thread gt < 64 fetches token gt of the next chunk (chunks run last to
+        // first) and publishes it in gsc[c & 1] at the top of each chunk
+        float *gsc = reinterpret_cast<float *>(sm + GSC);
+        auto fetch_scalar = [&](int c) -> float {
+            const int64_t t = (int64_t)(ce - 1 - c) * kC + gt;
+            return t < a.T ? __ldg(a.g + ((int64_t)bidx * a.T + t) * a.H + h) : 0.f;
+        };
+        float gpre = (kScalar && gt < kC && n > 0) ? fetch_scalar(0) : 0.f;
         for (int c = 0; c < n; ++c) {
-            bool w = mbar_wait(&bars[SGFULL + c % NG], par(c / NG));
-            if (named_bar_or(1, 256, !w)) { ok = false; break; }
+            if (kScalar) {
+                if (gt < kC) {
+                    gsc[(c & 1) * kC + gt] = gpre;
+                    if (c + 1 < n) gpre = fetch_scalar(c + 1);
+                }
+                named_bar_sync(1, 256);
+            } else {
+                bool w = mbar_wait(&bars[SGFULL + c % NG], par(c / NG));
+                if (named_bar_or(1, 256, !w)) { ok = false; break; }
+            }
             if (gt == 0) TRACE_ST(1, c);
             float b0[16], b1[16];
-            gate_cumsum(reinterpret_cast<const float *>(sm + G + (c % NG) * GSLOT), xch, qq, d,
-                        b0, b1, 1);
-            if (gt == 0) mbar_arrive(&bars[SGEMPTY + c % NG]);
+            if (kScalar)
+                gate_cumsum_scalar(gsc + (c & 1) * kC, xch, qq, d, b0, b1, 1);
+            else
+                gate_cumsum(reinterpret_cast<const float *>(sm + G + (c % NG) * GSLOT), xch, qq, d,
+                            b0, b1, 1);
+            if (!kScalar && gt == 0) mbar_arrive(&bars[SGEMPTY + c % NG]);
             if (qq == 3) {
                 bv_s[d] = b0[15];
                 bv_s[d + 1] = b1[15];
             }
-            w = mbar_wait(&bars[SKFULL + c % NKV], par(c / NKV));
+            const bool w = mbar_wait(&bars[SKFULL + c % NKV], par(c / NKV));
             if (named_bar_or(1, 256, !w)) { ok = false; break; }   // also publishes bv_s
             const float s0 = bv_s[d] + l0, s1 = bv_s[d + 1] + l1;
             uint8_t *kt = sm + (c % NKV) * KVSTAGE + K + boxo;
@@ -1155,12 +1230,18 @@ bool g_attr_done = false;
 
 cudaError_t set_attrs() {
     if (g_attr_done) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(gla_tc_out_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, om::ALLOC);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(gla_tc_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             sm_::ALLOC);
-    if (e != cudaSuccess) return e;
+    const void *outs[2] = {(const void *)gla_tc_out_kernel<false>,
+                           (const void *)gla_tc_out_kernel<true>};
+    const void *states[2] = {(const void *)gla_tc_state_kernel<false>,
+                             (const void *)gla_tc_state_kernel<true>};
+    for (int i = 0; i < 2; ++i) {
+        cudaError_t e = cudaFuncSetAttribute(outs[i], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             om::ALLOC);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(states[i], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 sm_::ALLOC);
+        if (e != cudaSuccess) return e;
+    }
     g_attr_done = true;
     return cudaSuccess;
 }
@@ -1215,6 +1296,7 @@ cudaError_t launch_tc(const Problem &p, int splits, int num_sms, void *ws, size_
                       unsigned int *dev_err, cudaStream_t stream) {
     if (p.T == 0) return launch_exact(p, dev_err, stream);   // only hT = h0 to write
     const int s = clamp_splits(p, splits);
+    const bool scalar = p.gate == 1;
     cudaError_t e = set_attrs();
     if (e != cudaSuccess) return e;
     CUtensorMap mq, mk, mv, mg, mo;
@@ -1224,8 +1306,11 @@ cudaError_t launch_tc(const Problem &p, int splits, int num_sms, void *ws, size_
                        CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_bthd_map(&mv, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.B, p.T, p.H, kD, 64, kC,
                        CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_bthd_map(&mg, p.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.B, p.T, p.H, kD, kD, kC,
-                       CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        // per-key gates are staged by TMA; scalar gates are read directly (the map is unused)
+        !(scalar ? make_bthd_map(&mg, p.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.B, p.T, p.H, kD,
+                                 64, kC, CU_TENSOR_MAP_SWIZZLE_128B)
+                 : make_bthd_map(&mg, p.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.B, p.T, p.H, kD,
+                                 kD, kC, CU_TENSOR_MAP_SWIZZLE_NONE)) ||
         !make_bthd_map(&mo, p.o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.B, p.T, p.H, kD, 64, kC,
                        CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidResourceHandle;   // a tensor map could not be encoded
@@ -1235,7 +1320,7 @@ cudaError_t launch_tc(const Problem &p, int splits, int num_sms, void *ws, size_
     const int pieces = tc_state_pieces(p, s, num_sms);
     // State-pass reads kept in L2 for the output pass, as a fraction of all of them; the last
     // segment (which gets none) is shortened by 15 % of that fraction.
-    const int64_t per_chunk = 2 * 16384 + 32768;   // k, v, g bytes of one chunk
+    const int64_t per_chunk = 2 * 16384 + (scalar ? 0 : 32768);   // k, v, g bytes of a chunk
     const int64_t state_bytes = (int64_t)bh * (s - 1) * ((nchunks + s - 1) / s) * per_chunk;
     const double kept = s > 1 ? std::min(1.0, (double)kL2KeepBytes / (double)state_bytes) : 0.0;
     const int last16 = 16 - (int)(16.0 * 0.15 * kept + 0.5);
@@ -1248,9 +1333,13 @@ cudaError_t launch_tc(const Problem &p, int splits, int num_sms, void *ws, size_
         const int retain = (int)std::min<int64_t>(
             ((nchunks + s - 1) / s + pieces - 1) / pieces,
             kL2KeepBytes / ((int64_t)bh * (s - 1) * pieces * per_chunk));
-        StateArgs sa{E, gam, p.T, (int)p.H, nchunks, s, dev_err, retain, last16, pieces};
-        gla_tc_state_kernel<<<bh * (s - 1) * pieces, kStateThreads, sm_::ALLOC, stream>>>(mk, mv, mg,
-                                                                                      sa);
+        StateArgs sa{E, gam, p.T, (int)p.H, nchunks, s, dev_err, retain, last16, pieces, p.g};
+        if (scalar)
+            gla_tc_state_kernel<true><<<bh * (s - 1) * pieces, kStateThreads, sm_::ALLOC, stream>>>(
+                mk, mv, mg, sa);
+        else
+            gla_tc_state_kernel<false><<<bh * (s - 1) * pieces, kStateThreads, sm_::ALLOC, stream>>>(
+                mk, mv, mg, sa);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         // scan and output kernels are programmatic dependents: each may be scheduled while its
         // predecessor (one of ours) still runs, and waits for it in griddepcontrol.wait
@@ -1289,9 +1378,14 @@ cudaError_t launch_tc(const Problem &p, int splits, int num_sms, void *ws, size_
         cfg.stream = stream;
         cfg.attrs = pdl;
         cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, gla_tc_out_kernel, mq, mk, mv, mg, mo, oa);
+        e = scalar ? cudaLaunchKernelEx(&cfg, gla_tc_out_kernel<true>, mq, mk, mv, mg, mo, oa)
+                   : cudaLaunchKernelEx(&cfg, gla_tc_out_kernel<false>, mq, mk, mv, mg, mo, oa);
     } else {
-        gla_tc_out_kernel<<<bh * s, kOutThreads, om::ALLOC, stream>>>(mq, mk, mv, mg, mo, oa);
+        if (scalar)
+            gla_tc_out_kernel<true><<<bh * s, kOutThreads, om::ALLOC, stream>>>(mq, mk, mv, mg, mo, oa);
+        else
+            gla_tc_out_kernel<false><<<bh * s, kOutThreads, om::ALLOC, stream>>>(mq, mk, mv, mg, mo,
+                                                                                oa);
         e = cudaGetLastError();
     }
     if (e != cudaSuccess) return e;

@@ -25,6 +25,7 @@ STATUS = {
     10: "GLA_ERR_BAD_OPTION",
 }
 PATHS = {"auto": 0, "exact": 1, "tc": 2}
+GATES = {"key": 0, "scalar": 1}
 IO_BF16, IO_F32 = 0, 1
 
 
@@ -37,7 +38,8 @@ class GLAError(RuntimeError):
 
 class _Options(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("seq_splits", ctypes.c_int),
-                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+                ("gate", ctypes.c_int)]
 
 
 _lock = threading.Lock()
@@ -107,9 +109,11 @@ def _check(t, name, dtype, shape, device):
         raise ValueError(f"{name} must be contiguous")
 
 
-def options(path: str = "auto", seq_splits: int = 0, workspace: torch.Tensor | None = None):
+def options(path: str = "auto", seq_splits: int = 0, workspace: torch.Tensor | None = None,
+            gate: str = "key"):
     opt = _Options()
     opt.path = PATHS[path]
+    opt.gate = GATES[gate]
     opt.seq_splits = int(seq_splits)
     opt.workspace = None if workspace is None else workspace.data_ptr()
     opt.workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
@@ -132,13 +136,15 @@ def path_for(B, T, H, Dk=128, Dv=128, io="bf16", path="auto") -> str | None:
 
 
 def gla_fwd(q, k, v, g, scale: float, h0=None, *, o=None, hT=None, return_state: bool = False,
-            path: str = "auto", seq_splits: int = 0, workspace=None, stream=None):
+            path: str = "auto", seq_splits: int = 0, workspace=None, gate: str = "key",
+            stream=None):
     """GLA prefill forward through ``gla_fwd_ex``.
 
-    q, k: [B,T,H,Dk]; v: [B,T,H,Dv] (all bf16, or all float32); g: [B,T,H,Dk] float32
-    log-gates; h0: [B,H,Dk,Dv] float32 or None. Outputs o (same dtype as q) and, when
-    ``return_state`` or ``hT`` is given, the float32 final state. Returns (o, hT|None).
-    Asynchronous on ``stream`` (default: torch's current stream).
+    q, k: [B,T,H,Dk]; v: [B,T,H,Dv] (all bf16, or all float32); g: float32 log-gates,
+    [B,T,H,Dk] (``gate="key"``) or [B,T,H] (``gate="scalar"``: one gate per token and head);
+    h0: [B,H,Dk,Dv] float32 or None. Outputs o (same dtype as q) and, when ``return_state``
+    or ``hT`` is given, the float32 final state. Returns (o, hT|None). Asynchronous on
+    ``stream`` (default: torch's current stream).
     """
     lib = load_library()
     if q.dtype not in (torch.bfloat16, torch.float32):
@@ -151,7 +157,7 @@ def gla_fwd(q, k, v, g, scale: float, h0=None, *, o=None, hT=None, return_state:
     _check(q, "q", q.dtype, (B, T, H, Dk), dev)
     _check(k, "k", q.dtype, (B, T, H, Dk), dev)
     _check(v, "v", q.dtype, (B, T, H, Dv), dev)
-    _check(g, "g", torch.float32, (B, T, H, Dk), dev)
+    _check(g, "g", torch.float32, (B, T, H, Dk) if gate == "key" else (B, T, H), dev)
     if h0 is not None:
         _check(h0, "h0", torch.float32, (B, H, Dk, Dv), dev)
     if o is None:
@@ -162,7 +168,7 @@ def gla_fwd(q, k, v, g, scale: float, h0=None, *, o=None, hT=None, return_state:
         hT = torch.empty((B, H, Dk, Dv), dtype=torch.float32, device=dev)
     elif hT is not None:
         _check(hT, "hT", torch.float32, (B, H, Dk, Dv), dev)
-    opt = options(path, seq_splits, workspace)
+    opt = options(path, seq_splits, workspace, gate)
     io = IO_BF16 if q.dtype == torch.bfloat16 else IO_F32
     with torch.cuda.device(dev):
         rc = lib.gla_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(g), ctypes.c_float(scale), _ptr(h0),

@@ -11,7 +11,7 @@ dataset — "Linear Attention 在 GPU 上到底慢在哪", section 实验设计)
   float32 ``randn`` of its full shape.
 * q, k, v ~ N(0, 1), shapes [B, T, H, Dk] / [B, T, H, Dv].
 * log-gate g = logsigmoid(u) / 16 with u ~ N(0, 1), one value per token, head and key
-  dimension, kept in float32.
+  dimension (one per token and head for the scalar-gate workloads), kept in float32.
 * h0 = 0.02 * N(0, 1) (standard deviation 0.02) where a workload carries a state in.
 * scale = Dk ** -0.5.
 * bf16 workloads round q, k, v to bf16 after drawing; g and h0 stay float32.
@@ -36,6 +36,7 @@ class Workload:
     seed: int = 0
     with_h0: bool = False     # draw a nonzero initial state
     want_hT: bool = False     # the workload returns the final state
+    gate: str = "key"         # "key": g [B,T,H,Dk]; "scalar": g [B,T,H] (one gate per token/head)
 
     @property
     def tokens(self) -> int:
@@ -54,6 +55,9 @@ WORKLOADS = {
     "bf16_B16_H16_T4096": Workload("bf16_B16_H16_T4096", B=16, T=4096, H=16, seed=3),
     "bf16_B1_H16_T131072_h0": Workload("bf16_B1_H16_T131072_h0", B=1, T=131072, H=16, seed=4,
                                        with_h0=True, want_hT=True),
+    # the scalar-per-head gate variant on the bench shape (one log-gate per token and head)
+    "bf16_B1_H16_T16384_scalar": Workload("bf16_B1_H16_T16384_scalar", B=1, T=16384, H=16,
+                                          seed=6, gate="scalar"),
 }
 
 # The workload the throughput metric is quoted on (B=1, H=16, T=16K, D=128, bf16).
@@ -75,7 +79,7 @@ def make_inputs(w: Workload, device: str | torch.device = "cpu") -> dict:
     q = draw(w.B, w.T, w.H, w.Dk).to(io)
     k = draw(w.B, w.T, w.H, w.Dk).to(io)
     v = draw(w.B, w.T, w.H, w.Dv).to(io)
-    g = F.logsigmoid(draw(w.B, w.T, w.H, w.Dk)) / 16.0
+    g = F.logsigmoid(draw(w.B, w.T, w.H, w.Dk) if w.gate == "key" else draw(w.B, w.T, w.H)) / 16.0
     h0 = draw(w.B, w.H, w.Dk, w.Dv) * 0.02 if w.with_h0 else None
     out = dict(q=q, k=k, v=v, g=g, h0=h0, scale=float(w.Dk) ** -0.5)
     if str(device) != "cpu":
@@ -86,10 +90,10 @@ def make_inputs(w: Workload, device: str | torch.device = "cpu") -> dict:
 
 
 def small(name: str, B: int, T: int, H: int, io: str = "bf16", seed: int = 0,
-          with_h0: bool = False, Dk: int = 128, Dv: int = 128) -> Workload:
+          with_h0: bool = False, Dk: int = 128, Dv: int = 128, gate: str = "key") -> Workload:
     """An ad-hoc workload with the same distributions (tests use these for edge cases)."""
     return Workload(name, B=B, T=T, H=H, Dk=Dk, Dv=Dv, io=io, seed=seed, with_h0=with_h0,
-                    want_hT=True)
+                    want_hT=True, gate=gate)
 
 
 # Decode-step workload: one token for each of B sequences and H heads on a resident state

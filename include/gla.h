@@ -71,6 +71,13 @@ typedef enum {
 
 typedef enum { GLA_IO_BF16 = 0, GLA_IO_F32 = 1 } gla_io;
 
+/* Shape of the log-gate. GLA_GATE_KEY: g_log [B, T, H, Dk], one gate per key dimension (the
+ * default, and what gla_fwd / gla_fwd_f32 take). GLA_GATE_SCALAR: g_log [B, T, H], one gate
+ * per token and head applied to every key row, S_t = exp(g_t) S_{t-1} + k_t^T v_t (the
+ * scalar-decay (SSD-style) variant, "Linear Attention 在 GPU 上到底慢在哪", section
+ * 正确的 baseline 和下一步). */
+typedef enum { GLA_GATE_KEY = 0, GLA_GATE_SCALAR = 1 } gla_gate;
+
 typedef struct {
     int path;               /* gla_path                                                */
     int seq_splits;         /* tensor-core path: sequence segments per head; 0 = auto  */
@@ -78,6 +85,7 @@ typedef struct {
                                keeps one per device (allocated on first need, grown
                                when a larger problem arrives)                          */
     size_t workspace_bytes; /* size of `workspace` in bytes                            */
+    int gate;               /* gla_gate (0 = GLA_GATE_KEY)                             */
 } gla_options;
 
 /*
@@ -99,8 +107,8 @@ gla_status gla_fwd_f32(const float *q, const float *k, const float *v, const flo
 
 /*
  * gla_fwd_ex — the general entry: io selects bf16 or fp32 q/k/v/o, opt (may be NULL)
- * selects the path, the sequence split and the workspace. The tensor-core path needs
- * bf16 I/O and Dk = Dv = 128.
+ * selects the path, the sequence split, the workspace and the gate shape. The tensor-core
+ * path needs bf16 I/O and Dk = Dv = 128.
  */
 gla_status gla_fwd_ex(const void *q, const void *k, const void *v, const float *g_log,
                       float scale, const float *h0, void *o, float *hT,

@@ -188,3 +188,75 @@ def test_tc_default_path_is_tensor_cores():
     from chunkwise_recurrent_prefill_gb300.gla import path_for
     assert path_for(1, 16384, 16) == "tc"
     assert path_for(1, 512, 2, io="f32") == "exact"
+
+
+# ---------------------------------------------------------------- scalar-per-head gate
+
+def _oracle_scalar(x):
+    """The oracle takes per-key gates: a scalar gate is the same in every key dimension."""
+    import oracle
+    cpu = lambda t: None if t is None else t.cpu()  # noqa: E731
+    g = x["g"].cpu()
+    gk = g[..., None].expand(*g.shape, x["q"].shape[-1]).contiguous()
+    return oracle.recurrent(cpu(x["q"]), cpu(x["k"]), cpu(x["v"]), gk, x["scale"], cpu(x["h0"]))
+
+
+def _scalar_inputs(B, T, H, io="bf16", seed=0, with_h0=True):
+    from chunkwise_recurrent_prefill_gb300.workloads import make_inputs, small
+    return make_inputs(small("scalar", B=B, T=T, H=H, io=io, seed=seed, with_h0=with_h0,
+                             gate="scalar"), DEV)
+
+
+@pytest.mark.parametrize("T", [64, 65, 200, 1000])
+@pytest.mark.parametrize("splits", [1, 3])
+def test_tc_scalar_gate(T, splits):
+    from chunkwise_recurrent_prefill_gb300 import gla_fwd, last_device_status
+    x = _scalar_inputs(B=2, T=T, H=3, seed=T + 5 * splits)
+    o, hT = gla_fwd(x["q"], x["k"], x["v"], x["g"], x["scale"], x["h0"], return_state=True,
+                    path="tc", seq_splits=splits, gate="scalar")
+    torch.cuda.synchronize()
+    assert last_device_status() == 0
+    o_ref, h_ref = _oracle_scalar(x)
+    assert_close(o.float().cpu().numpy(), o_ref, "bf16", f"o(scalar, splits={splits})")
+    assert_close(hT.cpu().numpy(), h_ref, "bf16", f"hT(scalar, splits={splits})")
+
+
+@pytest.mark.parametrize("kind", ["forget", "strong", "renorm"])
+def test_tc_scalar_gate_extremes(kind):
+    from chunkwise_recurrent_prefill_gb300 import gla_fwd
+    x = _scalar_inputs(B=1, T=700, H=2, seed=9)
+    g = x["g"]
+    x["g"] = {"forget": torch.full_like(g, -1e4), "strong": -5.0 * torch.rand_like(g),
+              "renorm": -0.5 * torch.rand_like(g)}[kind]
+    o, hT = gla_fwd(x["q"], x["k"], x["v"], x["g"], x["scale"], x["h0"], return_state=True,
+                    path="tc", seq_splits=2, gate="scalar")
+    torch.cuda.synchronize()
+    assert torch.isfinite(o.float()).all() and torch.isfinite(hT).all()
+    o_ref, h_ref = _oracle_scalar(x)
+    assert_close(o.float().cpu().numpy(), o_ref, "bf16", f"o[scalar {kind}]")
+    assert_close(hT.cpu().numpy(), h_ref, "bf16", f"hT[scalar {kind}]")
+
+
+def test_exact_scalar_gate_f32():
+    from chunkwise_recurrent_prefill_gb300 import gla_fwd
+    x = _scalar_inputs(B=1, T=333, H=2, io="f32", seed=12)
+    o, hT = gla_fwd(x["q"], x["k"], x["v"], x["g"], x["scale"], x["h0"], return_state=True,
+                    gate="scalar")
+    torch.cuda.synchronize()
+    o_ref, h_ref = _oracle_scalar(x)
+    assert_close(o.cpu().numpy(), o_ref, "f32", "o(exact scalar)")
+    assert_close(hT.cpu().numpy(), h_ref, "f32", "hT(exact scalar)")
+
+
+def test_tc_scalar_gate_workload():
+    """The scalar-gate bench shape (B=1, H=16, T=16384), every output, automatic split."""
+    from chunkwise_recurrent_prefill_gb300 import gla_fwd
+    from chunkwise_recurrent_prefill_gb300.workloads import WORKLOADS, make_inputs
+    w = WORKLOADS["bf16_B1_H16_T16384_scalar"]
+    x = make_inputs(w, DEV)
+    o, _ = gla_fwd(x["q"], x["k"], x["v"], x["g"], x["scale"], x["h0"], return_state=True,
+                   gate="scalar")
+    torch.cuda.synchronize()
+    o_ref, _ = _oracle_scalar(x)
+    eo = assert_close(o.float().cpu().numpy(), o_ref, "bf16", "scalar workload o")
+    print(f"\nparity {w.name}: o max/mean rel {eo[0]:.3e}/{eo[1]:.3e}")
