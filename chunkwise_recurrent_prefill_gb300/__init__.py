@@ -7,6 +7,7 @@ from .gla import (  # noqa: F401
     GLAError,
     gla_fwd,
     gla_fwd_noalloc,
+    gla_fwd_varlen,
     gla_step,
     last_device_status,
     load_library,

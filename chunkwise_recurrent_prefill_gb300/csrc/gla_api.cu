@@ -185,6 +185,7 @@ const char *gla_status_string(gla_status s) {
         case GLA_ERR_UNSUPPORTED_DEVICE: return "GLA_ERR_UNSUPPORTED_DEVICE";
         case GLA_ERR_WORKSPACE: return "GLA_ERR_WORKSPACE";
         case GLA_ERR_BAD_OPTION: return "GLA_ERR_BAD_OPTION";
+        case GLA_ERR_BAD_SEQLENS: return "GLA_ERR_BAD_SEQLENS";
     }
     return "GLA_ERR_UNKNOWN";
 }
@@ -266,6 +267,57 @@ gla_status gla_fwd_ex(const void *q, const void *k, const void *v, const float *
     return GLA_OK;
 }
 
+gla_status gla_fwd_varlen(const void *q, const void *k, const void *v, const float *g_log,
+                          float scale, const float *h0, void *o, float *hT,
+                          const int32_t *cu_seqlens, int64_t N, int64_t T, int64_t H,
+                          int64_t Dk, int64_t Dv, int io, const gla_options *opt,
+                          gla_stream_t stream) {
+    // the token tensors are one batch of T tokens; the states are N per head
+    Sizes sz;
+    const int gate = opt ? opt->gate : GLA_GATE_KEY;
+    if (gate != GLA_GATE_KEY && gate != GLA_GATE_SCALAR) return GLA_ERR_BAD_OPTION;
+    if (N < 0) return GLA_ERR_BAD_SHAPE;
+    gla_status rc = validate(q, k, v, g_log, nullptr, o, nullptr, 1, T, H, Dk, Dv, io, gate, &sz);
+    if (rc != GLA_OK) return rc;
+    int64_t nstate;
+    if (!mul_ok(N, H, &nstate) || !mul_ok(nstate, Dk * Dv, &nstate) || N * H > (int64_t(1) << 24))
+        return GLA_ERR_BAD_SHAPE;
+    if (N > 0 && !cu_seqlens) return GLA_ERR_NULL_ARG;
+    if (misaligned(h0) || misaligned(hT) || (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u))
+        return GLA_ERR_MISALIGNED;
+    const size_t es = io == GLA_IO_BF16 ? 2 : 4;
+    const size_t bqk = (size_t)sz.nqk * es, bv = (size_t)sz.nv * es;
+    const size_t bg = (size_t)(gate == GLA_GATE_SCALAR ? sz.nqk / Dk : sz.nqk) * 4;
+    const size_t bs = (size_t)nstate * 4, bcu = (size_t)(N + 1) * 4;
+    const void *ins[6] = {q, k, v, g_log, h0, cu_seqlens};
+    const size_t nins[6] = {bqk, bqk, bv, bg, bs, bcu};
+    for (int i = 0; i < 6; ++i) {
+        if (overlap(o, bv, ins[i], nins[i]) || overlap(hT, bs, ins[i], nins[i]))
+            return GLA_ERR_ALIAS;
+    }
+    if (overlap(o, bv, hT, bs)) return GLA_ERR_ALIAS;
+    gla::Problem p{q, k, v, g_log, scale, h0, o, hT, N, T, H, Dk, Dv, io, gate, cu_seqlens};
+    const int path = resolve_path(opt, p);
+    if (path != GLA_PATH_EXACT && path != GLA_PATH_TC) return GLA_ERR_BAD_OPTION;
+    if (path == GLA_PATH_EXACT && !gla::exact_supported(Dk, Dv)) return GLA_ERR_UNSUPPORTED_DIM;
+    if (path == GLA_PATH_TC && (io != GLA_IO_BF16 || !gla::tc_supported(p)))
+        return GLA_ERR_UNSUPPORTED_DIM;
+    DeviceState *st = nullptr;
+    rc = current_device(&st);
+    if (rc != GLA_OK) return rc;
+    if (N * H == 0) return GLA_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const cudaError_t e = path == GLA_PATH_EXACT
+                              ? gla::launch_exact(p, st->err_word, s)
+                              : gla::launch_tc(p, 1, st->num_sms, nullptr, 0, st->err_word, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        set_detail(path == GLA_PATH_EXACT ? "exact path launch" : "tensor-core path launch", e);
+        return GLA_ERR_LAUNCH;
+    }
+    return GLA_OK;
+}
+
 gla_status gla_fwd(const void *q, const void *k, const void *v, const float *g_log, float scale,
                    const float *h0, void *o, float *hT, int64_t B, int64_t T, int64_t H,
                    int64_t Dk, int64_t Dv, gla_stream_t stream) {
@@ -336,7 +388,7 @@ gla_status gla_last_device_status(gla_stream_t stream) {
             cudaGetLastError();
             return GLA_ERR_LAUNCH;
         }
-        return GLA_ERR_DEVICE_TIMEOUT;
+        return (word & gla::kDevErrTimeout) ? GLA_ERR_DEVICE_TIMEOUT : GLA_ERR_BAD_SEQLENS;
     }
     return GLA_OK;
 }

@@ -12,7 +12,8 @@
 // path for fp32 I/O; it is also a slow exact reference for bf16 I/O.
 //
 // One CTA per (batch*head, Dv slice of VB columns); the state slice lives in shared
-// memory for the whole sequence. The tail chunk is zero-padded: a padded token has
+// memory for the whole sequence. Packed sequences (cu offsets) are the batches of a single
+// [T] token axis. The tail chunk is zero-padded: a padded token has
 // k = v = 0 and g = 0, so it neither adds to nor decays the state.
 #include <cuda_bf16.h>
 
@@ -44,7 +45,7 @@ __global__ void __launch_bounds__(kThreads)
 gla_exact_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO *__restrict__ v,
                  const float *__restrict__ g, float scale, const float *__restrict__ h0,
                  IO *__restrict__ o, float *__restrict__ hT, int64_t T, int64_t H,
-                 int gate_scalar) {
+                 int gate_scalar, const int *__restrict__ cu, unsigned *__restrict__ err) {
     constexpr int KS = DK + 1;
     extern __shared__ float sm[];
     float *qs = sm;                 // [C][KS]  q, later q * exp(b)
@@ -58,23 +59,33 @@ gla_exact_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO *_
     const int64_t bh = blockIdx.x;
     const int64_t b = bh / H, h = bh % H;
     const int v0 = blockIdx.y * kVB;
+    // token rows [r0, r0 + Tb) of the flattened [B*T] (or packed) token axis
+    int64_t r0 = b * T, Tb = T;
+    if (cu) {
+        const int s0 = cu[b], s1 = cu[b + 1];
+        const bool bad = s0 < 0 || s1 < s0 || s1 > T;
+        if (bad && tid == 0 && err) atomicOr(err, kDevErrInternal);
+        r0 = bad ? 0 : s0;
+        Tb = bad ? 0 : s1 - s0;
+        if (bad) return;   // uniform across the block: nothing is written
+    }
 
     for (int i = tid; i < DK * kVB; i += kThreads) {
         const int d = i / kVB, e = i % kVB;
         Ss[i] = h0 ? h0[(bh * DK + d) * DV + v0 + e] : 0.f;
     }
 
-    for (int64_t t0 = 0; t0 < T; t0 += kC) {
-        const int L = (int)((T - t0) < kC ? (T - t0) : kC);
+    for (int64_t t0 = 0; t0 < Tb; t0 += kC) {
+        const int L = (int)((Tb - t0) < kC ? (Tb - t0) : kC);
         __syncthreads();
         for (int i = tid; i < kC * DK; i += kThreads) {
             const int t = i / DK, d = i % DK;
             float qv = 0.f, kv = 0.f, gv = 0.f;
             if (t < L) {
-                const int64_t idx = ((b * T + t0 + t) * H + h) * DK + d;
+                const int64_t idx = ((r0 + t0 + t) * H + h) * DK + d;
                 qv = to_f(q[idx]);
                 kv = to_f(k[idx]);
-                gv = gate_scalar ? g[(b * T + t0 + t) * H + h] : g[idx];
+                gv = gate_scalar ? g[(r0 + t0 + t) * H + h] : g[idx];
             }
             qs[t * KS + d] = qv;
             ks[t * KS + d] = kv;
@@ -82,7 +93,7 @@ gla_exact_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO *_
         }
         for (int i = tid; i < kC * kVB; i += kThreads) {
             const int t = i / kVB, e = i % kVB;
-            vs[i] = t < L ? to_f(v[((b * T + t0 + t) * H + h) * DV + v0 + e]) : 0.f;
+            vs[i] = t < L ? to_f(v[((r0 + t0 + t) * H + h) * DV + v0 + e]) : 0.f;
         }
         __syncthreads();
         if (tid < DK) {  // inclusive cumulative log-gate along the chunk, per key dim
@@ -119,7 +130,7 @@ gla_exact_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO *_
             const float *qi = qs + i * KS;
 #pragma unroll 8
             for (int d = 0; d < DK; ++d) acc += qi[d] * Ss[d * kVB + e];
-            if (i < L) o[((b * T + t0 + i) * H + h) * DV + v0 + e] = from_f<IO>(scale * acc);
+            if (i < L) o[((r0 + t0 + i) * H + h) * DV + v0 + e] = from_f<IO>(scale * acc);
         }
         __syncthreads();
         for (int p = tid; p < DK * kVB; p += kThreads) {  // state scan step
@@ -140,7 +151,7 @@ gla_exact_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO *_
 }
 
 template <typename IO, int DK, int DV>
-cudaError_t launch_typed(const Problem &p, cudaStream_t s) {
+cudaError_t launch_typed(const Problem &p, unsigned *err, cudaStream_t s) {
     auto kern = gla_exact_kernel<IO, DK, DV>;
     const size_t smem = exact_smem_bytes<DK, DV>();
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -149,18 +160,19 @@ cudaError_t launch_typed(const Problem &p, cudaStream_t s) {
     dim3 grid((unsigned)(p.B * p.H), DV / kVB);
     kern<<<grid, kThreads, smem, s>>>(static_cast<const IO *>(p.q), static_cast<const IO *>(p.k),
                                       static_cast<const IO *>(p.v), p.g, p.scale, p.h0,
-                                      static_cast<IO *>(p.o), p.hT, p.T, p.H, p.gate);
+                                      static_cast<IO *>(p.o), p.hT, p.T, p.H, p.gate, p.cu,
+                                      err);
     e = cudaGetLastError();
     if (e == cudaSuccess) count_launches(1);
     return e;
 }
 
 template <typename IO>
-cudaError_t launch_io(const Problem &p, cudaStream_t s) {
-    if (p.Dk == 128 && p.Dv == 128) return launch_typed<IO, 128, 128>(p, s);
-    if (p.Dk == 128 && p.Dv == 64) return launch_typed<IO, 128, 64>(p, s);
-    if (p.Dk == 64 && p.Dv == 128) return launch_typed<IO, 64, 128>(p, s);
-    if (p.Dk == 64 && p.Dv == 64) return launch_typed<IO, 64, 64>(p, s);
+cudaError_t launch_io(const Problem &p, unsigned *err, cudaStream_t s) {
+    if (p.Dk == 128 && p.Dv == 128) return launch_typed<IO, 128, 128>(p, err, s);
+    if (p.Dk == 128 && p.Dv == 64) return launch_typed<IO, 128, 64>(p, err, s);
+    if (p.Dk == 64 && p.Dv == 128) return launch_typed<IO, 64, 128>(p, err, s);
+    if (p.Dk == 64 && p.Dv == 64) return launch_typed<IO, 64, 64>(p, err, s);
     return cudaErrorInvalidValue;
 }
 
@@ -170,10 +182,10 @@ bool exact_supported(int64_t Dk, int64_t Dv) {
     return (Dk == 64 || Dk == 128) && (Dv == 64 || Dv == 128);
 }
 
-cudaError_t launch_exact(const Problem &p, unsigned int * /*dev_err*/, cudaStream_t s) {
+cudaError_t launch_exact(const Problem &p, unsigned int *dev_err, cudaStream_t s) {
     if (p.B * p.H == 0) return cudaSuccess;
-    if (p.io == 1) return launch_io<float>(p, s);
-    return launch_io<__nv_bfloat16>(p, s);
+    if (p.io == 1) return launch_io<float>(p, dev_err, s);
+    return launch_io<__nv_bfloat16>(p, dev_err, s);
 }
 
 }  // namespace gla

@@ -18,12 +18,15 @@ struct Problem {
     int64_t B, T, H, Dk, Dv;
     int io;                  // GLA_IO_BF16 / GLA_IO_F32
     int gate;                // GLA_GATE_KEY: g [B,T,H,Dk]; GLA_GATE_SCALAR: g [B,T,H]
+    const int *cu;           // packed sequences: B sequences at offsets cu[0..B] along a
+                             // single batch of T tokens (device), or null
 };
 
 // Bits of the device error word kernels may raise (never trap).
 enum : unsigned int {
     kDevErrTimeout = 1u,     // a bounded mbarrier / flag wait ran out
-    kDevErrInternal = 2u,    // an internal consistency check failed
+    kDevErrInternal = 2u,    // an input the host could not check was inconsistent (packed-
+                             // sequence offsets not non-decreasing from 0 to T)
 };
 
 // Host-side count of kernel launches issued by the library (gla_launch_counter).

@@ -172,6 +172,8 @@ struct OutArgs {
     unsigned *err;
     int stall_chunk;                   // test hook: chunk whose q/k/v load is never issued (-1)
     int last16;                        // weight of the last segment in 16ths (see seg_bound)
+    const int *cu;                     // packed sequences: offsets [B+1] along T, or null
+    __nv_bfloat16 *o;                  // output (rows a TMA store may not cover)
 };
 
 struct StateArgs {
@@ -304,11 +306,35 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     const int seg = blockIdx.x % a.splits;
     const int bh = blockIdx.x / a.splits;
     const int bidx = bh / a.H, h = bh % a.H;
+    // Tokens of this CTA's sequence: [tbase, tend) along the T axis of the tensors, in batch
+    // bmap. Packed sequences (a.cu) all live in batch 0 and are not split.
+    int64_t tbase = 0, tend = a.T;
+    int bmap = bidx;
+    bool bad_seq = false;
+    if (a.cu) {
+        const int s0 = a.cu[bidx], s1 = a.cu[bidx + 1];
+        bad_seq = s0 < 0 || s1 < s0 || s1 > a.T;
+        tbase = bad_seq ? 0 : s0;
+        tend = bad_seq ? 0 : s1;
+        bmap = 0;
+    }
     int cb, ce;
-    seg_range(seg, a.nchunks, a.splits, a.last16, cb, ce);
+    if (a.cu) {
+        cb = 0;
+        ce = (int)((tend - tbase + kC - 1) / kC);
+    } else {
+        seg_range(seg, a.nchunks, a.splits, a.last16, cb, ce);
+    }
     const int n = ce - cb;
+    // valid rows of chunk c (64 except at the end of a sequence)
+    auto valid_rows = [&](int c) -> int {
+        const int64_t left = tend - tbase - (int64_t)(cb + c) * kC;
+        return left >= kC ? kC : (int)left;
+    };
 
+    if (threadIdx.x < kD) reinterpret_cast<float *>(sm + ENDS)[threadIdx.x] = 1.f;  // L = 0
     if (threadIdx.x == 0) {
+        if (bad_seq) atomicOr(a.err, kDevErrInternal);
         for (int i = 0; i < NQ; ++i) {
             mbar_init(&bars[QFULL + i], 1);
             mbar_init(&bars[QEMPTY + i], 1);
@@ -360,8 +386,8 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 if (ng < n && (ng < NG || mbar_test(&bars[GEMPTY + ng % NG], par(ng / NG - 1)))) {
                     uint64_t *fb = &bars[GFULL + ng % NG];
                     mbar_arrive_expect_tx(fb, GSLOT);
-                    tma_load_4d_hint(sm + G + (ng % NG) * GSLOT, &tg, fb, 0, h, (cb + ng) * kC,
-                                     bidx, pol);
+                    tma_load_4d_hint(sm + G + (ng % NG) * GSLOT, &tg, fb, 0, h,
+                                     (int)(tbase + (cb + ng) * kC), bmap, pol);
                     ++ng;
                     prog = true;
                 }
@@ -369,19 +395,19 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     uint8_t *base = sm + (nq % NQ) * QSTAGE;
                     uint64_t *fb = &bars[QFULL + nq % NQ];
                     TRACE_OUT(0, nq);
-                    const int t = (cb + nq) * kC;
+                    const int t = (int)(tbase + (cb + nq) * kC);
                     mbar_arrive_expect_tx(fb, 3 * 16384);
                     if (nq == a.stall_chunk) {   // test hook: the stage never fills
                         ++nq;
                         prog = true;
                         continue;
                     }
-                    tma_load_4d_hint(base + Q, &tq, fb, 0, h, t, bidx, pol);
-                    tma_load_4d_hint(base + Q + 8192, &tq, fb, 64, h, t, bidx, pol);
-                    tma_load_4d_hint(base + K, &tk, fb, 0, h, t, bidx, pol);
-                    tma_load_4d_hint(base + K + 8192, &tk, fb, 64, h, t, bidx, pol);
-                    tma_load_4d_hint(base + V, &tv, fb, 0, h, t, bidx, pol);
-                    tma_load_4d_hint(base + V + 8192, &tv, fb, 64, h, t, bidx, pol);
+                    tma_load_4d_hint(base + Q, &tq, fb, 0, h, t, bmap, pol);
+                    tma_load_4d_hint(base + Q + 8192, &tq, fb, 64, h, t, bmap, pol);
+                    tma_load_4d_hint(base + K, &tk, fb, 0, h, t, bmap, pol);
+                    tma_load_4d_hint(base + K + 8192, &tk, fb, 64, h, t, bmap, pol);
+                    tma_load_4d_hint(base + V, &tv, fb, 0, h, t, bmap, pol);
+                    tma_load_4d_hint(base + V + 8192, &tv, fb, 64, h, t, bmap, pol);
                     ++nq;
                     prog = true;
                 }
@@ -547,12 +573,27 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             }
             fence_proxy_async_smem();
             named_bar_sync(2, 128);
-            if (et == 0) {
-                const int t0 = (cb + c) * kC;
+            const int vr = valid_rows(c);
+            if (a.cu && vr < kC) {
+                // the last chunk of a packed sequence: the rows past its end belong to the next
+                // one, so only the valid rows are written, from registers
+                const int64_t t0 = tbase + (int64_t)(cb + c) * kC;
+                __nv_bfloat16 *op = a.o + (t0 * a.H + h) * kD + v;
+                const int64_t rs = (int64_t)a.H * kD;   // row stride of o
+#pragma unroll
+                for (int x = 0; x < 32; ++x)
+                    if (x < vr) op[x * rs] = __float2bfloat16_rn(o0[x]);
+#pragma unroll
+                for (int x = 0; x < 32; ++x)
+                    if (32 + x < vr) op[(32 + x) * rs] = __float2bfloat16_rn(o1[x]);
+                named_bar_sync(2, 128);
+                if (et == 0) mbar_arrive(&bars[QEMPTY + c % NQ]);
+            } else if (et == 0) {
+                const int t0 = (int)(tbase + (cb + c) * kC);
                 uint8_t *qt = sm + (c % NQ) * QSTAGE + Q;
                 const uint64_t pol = l2_policy_evict_first();
-                tma_store_4d_hint(&to, qt, 0, h, t0, bidx, pol);
-                tma_store_4d_hint(&to, qt + 8192, 64, h, t0, bidx, pol);
+                tma_store_4d_hint(&to, qt, 0, h, t0, bmap, pol);
+                tma_store_4d_hint(&to, qt + 8192, 64, h, t0, bmap, pol);
                 bulk_commit();
                 bulk_wait_read_all();
                 mbar_arrive(&bars[QEMPTY + c % NQ]);   // the stage may be refilled
@@ -660,12 +701,12 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
 #pragma unroll
                 for (int x = 0; x < 64; ++x) prow[x] = 0.f;
                 float *gcol = scr, *qcol = scr + 64, *kcol = scr + 128, *bcol = scr + 192;
-                const int64_t t0 = (int64_t)(cb + c) * kC;
+                const int64_t t0 = tbase + (int64_t)(cb + c) * kC;
                 for (int d = 0; d < kD; ++d) {
                     if (st_t < 64) {
                         const int64_t t = t0 + st_t;
-                        const bool in = t < a.T;
-                        const int64_t idx = (((int64_t)bidx * a.T + t) * a.H + h) * kD + d;
+                        const bool in = t < tend;
+                        const int64_t idx = (((int64_t)bmap * a.T + t) * a.H + h) * kD + d;
                         gcol[st_t] = in ? (kScalar ? a.g[idx / kD] : a.g[idx]) : 0.f;
                         qcol[st_t] = in ? __bfloat162float(a.q[idx]) : 0.f;
                         kcol[st_t] = in ? __bfloat162float(a.k[idx]) : 0.f;
@@ -708,8 +749,8 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             if (lane == 0) mbar_arrive(&bars[PBF]);
             if (v == 0) TRACE_OUT(11, c);
         }
-        if (ok && a.hT && seg == a.splits - 1) {
-            if (!mbar_wait(&bars[UDONE], par(n - 1))) {
+        if (ok && !bad_seq && a.hT && seg == a.splits - 1) {
+            if (n > 0 && !mbar_wait(&bars[UDONE], par(n - 1))) {
                 ok = false;
             } else {
                 tc_fence_after();
@@ -755,8 +796,8 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         // than one chunk behind another, the loop has several barriers per chunk)
         float *gsc = reinterpret_cast<float *>(sm + GSC);
         auto fetch_scalar = [&](int c) -> float {
-            const int64_t t = (int64_t)(cb + c) * kC + gt;
-            return t < a.T ? __ldg(a.g + ((int64_t)bidx * a.T + t) * a.H + h) : 0.f;
+            const int64_t t = tbase + (int64_t)(cb + c) * kC + gt;
+            return t < tend ? __ldg(a.g + ((int64_t)bmap * a.T + t) * a.H + h) : 0.f;
         };
         float gpre = (kScalar && gt < kC && n > 0) ? fetch_scalar(0) : 0.f;
         for (int c = 0; c < n; ++c) {
@@ -775,6 +816,14 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             if (gt == 0) TRACE_OUT(16, c);
             const float *grow = reinterpret_cast<const float *>(sm + G + gs * GSLOT) + tb * kD + d;
             const float *gsrow = gsc + (c & 1) * kC + tb;   // scalar gates of this thread's range
+            const int vr = valid_rows(c);
+            if (!kScalar && vr < kC) {
+                // rows past the sequence end hold another sequence's gates (packed sequences):
+                // this thread's own elements of them become 0 (no decay) before it reads them
+                for (int t = max(vr - tb, 0); t < tl; ++t)
+                    *reinterpret_cast<float2 *>(const_cast<float *>(grow) + t * kD) =
+                        make_float2(0.f, 0.f);
+            }
             auto gpair = [&](int t) -> float2 {
                 if (kScalar) {
                     const float x = gsrow[t];
@@ -835,6 +884,11 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             if (gt == 0) TRACE_OUT(1, c);
             uint8_t *qt = sm + qs * QSTAGE + Q + boxo;
             uint8_t *kt = sm + qs * QSTAGE + K + boxo;
+            if (vr < kC) {
+                // and their keys become 0: they add nothing to P or to the state
+                for (int t = max(vr - tb, 0); t < tl; ++t)
+                    *reinterpret_cast<uint32_t *>(kt + sw128_offset((uint32_t)(tb + t), col)) = 0u;
+            }
             r0 = 0.f;
             r1 = 0.f;
             // blocks of kGateBlock tokens: all loads of a block are issued before its stores, so a
@@ -1295,23 +1349,24 @@ size_t tc_workspace_bytes(const Problem &p, int splits, int num_sms) {
 cudaError_t launch_tc(const Problem &p, int splits, int num_sms, void *ws, size_t ws_bytes,
                       unsigned int *dev_err, cudaStream_t stream) {
     if (p.T == 0) return launch_exact(p, dev_err, stream);   // only hT = h0 to write
-    const int s = clamp_splits(p, splits);
+    const int s = p.cu ? 1 : clamp_splits(p, splits);   // packed sequences are not split
+    const int64_t mB = p.cu ? 1 : p.B;                   // batch extent of the tensor maps
     const bool scalar = p.gate == 1;
     cudaError_t e = set_attrs();
     if (e != cudaSuccess) return e;
     CUtensorMap mq, mk, mv, mg, mo;
-    if (!make_bthd_map(&mq, p.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.B, p.T, p.H, kD, 64, kC,
+    if (!make_bthd_map(&mq, p.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, mB, p.T, p.H, kD, 64, kC,
                        CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_bthd_map(&mk, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.B, p.T, p.H, kD, 64, kC,
+        !make_bthd_map(&mk, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, mB, p.T, p.H, kD, 64, kC,
                        CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_bthd_map(&mv, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.B, p.T, p.H, kD, 64, kC,
+        !make_bthd_map(&mv, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, mB, p.T, p.H, kD, 64, kC,
                        CU_TENSOR_MAP_SWIZZLE_128B) ||
         // per-key gates are staged by TMA; scalar gates are read directly (the map is unused)
-        !(scalar ? make_bthd_map(&mg, p.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.B, p.T, p.H, kD,
+        !(scalar ? make_bthd_map(&mg, p.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, mB, p.T, p.H, kD,
                                  64, kC, CU_TENSOR_MAP_SWIZZLE_128B)
-                 : make_bthd_map(&mg, p.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.B, p.T, p.H, kD,
+                 : make_bthd_map(&mg, p.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, mB, p.T, p.H, kD,
                                  kD, kC, CU_TENSOR_MAP_SWIZZLE_NONE)) ||
-        !make_bthd_map(&mo, p.o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.B, p.T, p.H, kD, 64, kC,
+        !make_bthd_map(&mo, p.o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, mB, p.T, p.H, kD, 64, kC,
                        CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidResourceHandle;   // a tensor map could not be encoded
     const int nchunks = (int)((p.T + kC - 1) / kC);
@@ -1363,10 +1418,11 @@ cudaError_t launch_tc(const Problem &p, int splits, int num_sms, void *ws, size_
     // Test hook for the bounded waits: with GLA_TEST_STALL_ONE_LOAD set, every output CTA
     // skips the q/k/v load of one chunk, so the waits for it run out and the call reports
     // GLA_ERR_DEVICE_TIMEOUT (after ~2 s per wait) with the context intact.
-    const int stall = std::getenv("GLA_TEST_STALL_ONE_LOAD") ? std::min(1, nchunks / s - 1) : -1;
+    const int stall = (std::getenv("GLA_TEST_STALL_ONE_LOAD") && !p.cu)
+                          ? std::min(1, nchunks / s - 1) : -1;
     OutArgs oa{static_cast<const __nv_bfloat16 *>(p.q), static_cast<const __nv_bfloat16 *>(p.k),
                p.g, p.h0, p.hT, sstart, p.T, (int)p.H, nchunks, s, p.scale, dev_err, stall,
-               last16};
+               last16, p.cu, static_cast<__nv_bfloat16 *>(p.o)};
     if (s > 1) {
         cudaLaunchAttribute pdl[1];
         pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

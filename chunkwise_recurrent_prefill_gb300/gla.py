@@ -22,7 +22,7 @@ STATUS = {
     0: "GLA_OK", 1: "GLA_ERR_NULL_ARG", 2: "GLA_ERR_BAD_SHAPE", 3: "GLA_ERR_UNSUPPORTED_DIM",
     4: "GLA_ERR_MISALIGNED", 5: "GLA_ERR_ALIAS", 6: "GLA_ERR_LAUNCH",
     7: "GLA_ERR_DEVICE_TIMEOUT", 8: "GLA_ERR_UNSUPPORTED_DEVICE", 9: "GLA_ERR_WORKSPACE",
-    10: "GLA_ERR_BAD_OPTION",
+    10: "GLA_ERR_BAD_OPTION", 11: "GLA_ERR_BAD_SEQLENS",
 }
 PATHS = {"auto": 0, "exact": 1, "tc": 2}
 GATES = {"key": 0, "scalar": 1}
@@ -63,6 +63,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                 f.restype = ctypes.c_int
             lib.gla_step.argtypes = [vp, vp, vp, vp, f32, vp, vp, i64, i64, i64, i64,
                                      ctypes.c_int, vp]
+            lib.gla_fwd_varlen.argtypes = [vp, vp, vp, vp, f32, vp, vp, vp, vp, i64, i64, i64,
+                                           i64, i64, ctypes.c_int, ctypes.POINTER(_Options), vp]
+            lib.gla_fwd_varlen.restype = ctypes.c_int
             lib.gla_step.restype = ctypes.c_int
             lib.gla_fwd_noalloc.argtypes = sig + [ctypes.c_int, vp]
             lib.gla_fwd_noalloc.restype = ctypes.c_int
@@ -208,6 +211,50 @@ def gla_fwd_noalloc(q, k, v, g, scale: float, h0=None, *, o, hT=None, seq_splits
     if rc != GLA_OK:
         detail = lib.gla_last_error_detail().decode() if rc in (6, 9) else ""
         raise GLAError(rc, "gla_fwd_noalloc", detail)
+    return o, hT
+
+
+def gla_fwd_varlen(q, k, v, g, scale: float, cu_seqlens, h0=None, *, o=None, hT=None,
+                   return_state: bool = False, path: str = "auto", gate: str = "key",
+                   stream=None):
+    """GLA prefill over packed sequences through ``gla_fwd_varlen``.
+
+    q, k: [T,H,Dk]; v: [T,H,Dv] (all bf16, or all float32); g: float32 [T,H,Dk] (or [T,H]
+    with ``gate="scalar"``); cu_seqlens: int32 [N+1] on the device (sequence i is tokens
+    cu_seqlens[i] .. cu_seqlens[i+1]-1); h0: [N,H,Dk,Dv] float32 or None. Returns (o, hT|None).
+    """
+    lib = load_library()
+    if q.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("q/k/v must be bfloat16 or float32")
+    T, H, Dk = q.shape
+    Dv = v.shape[-1]
+    N = cu_seqlens.numel() - 1
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("tensors must be on a CUDA device")
+    _check(k, "k", q.dtype, (T, H, Dk), dev)
+    _check(v, "v", q.dtype, (T, H, Dv), dev)
+    _check(g, "g", torch.float32, (T, H, Dk) if gate == "key" else (T, H), dev)
+    _check(cu_seqlens, "cu_seqlens", torch.int32, (N + 1,), dev)
+    if h0 is not None:
+        _check(h0, "h0", torch.float32, (N, H, Dk, Dv), dev)
+    if o is None:
+        o = torch.empty((T, H, Dv), dtype=q.dtype, device=dev)
+    else:
+        _check(o, "o", q.dtype, (T, H, Dv), dev)
+    if hT is None and return_state:
+        hT = torch.empty((N, H, Dk, Dv), dtype=torch.float32, device=dev)
+    elif hT is not None:
+        _check(hT, "hT", torch.float32, (N, H, Dk, Dv), dev)
+    opt = options(path, 0, None, gate)
+    io = IO_BF16 if q.dtype == torch.bfloat16 else IO_F32
+    with torch.cuda.device(dev):
+        rc = lib.gla_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(g), ctypes.c_float(scale),
+                                _ptr(h0), _ptr(o), _ptr(hT), _ptr(cu_seqlens), N, T, H, Dk, Dv,
+                                io, ctypes.byref(opt), _stream_handle(stream))
+    if rc != GLA_OK:
+        detail = lib.gla_last_error_detail().decode() if rc == 6 else ""
+        raise GLAError(rc, "gla_fwd_varlen", detail)
     return o, hT
 
 

@@ -59,7 +59,9 @@ typedef enum {
     GLA_ERR_DEVICE_TIMEOUT = 7,    /* a kernel gave up waiting on a pipeline barrier  */
     GLA_ERR_UNSUPPORTED_DEVICE = 8,/* the current device is not sm_103                */
     GLA_ERR_WORKSPACE = 9,         /* caller workspace too small or misaligned        */
-    GLA_ERR_BAD_OPTION = 10        /* an option value is out of range                 */
+    GLA_ERR_BAD_OPTION = 10,       /* an option value is out of range                 */
+    GLA_ERR_BAD_SEQLENS = 11       /* packed-sequence offsets were found inconsistent on
+                                      the device (reported by gla_last_device_status)   */
 } gla_status;
 
 /* Which arithmetic path runs. */
@@ -131,6 +133,25 @@ gla_status gla_step(const void *q, const void *k, const void *v, const float *g_
                     float *S, void *o, int64_t B, int64_t H, int64_t Dk, int64_t Dv, int io,
                     gla_stream_t stream);
 
+/*
+ * gla_fwd_varlen — gla_fwd_ex over N sequences of different lengths packed along one token
+ * axis (a T-ragged batch). Sequence i is tokens cu_seqlens[i] .. cu_seqlens[i+1]-1; each
+ * runs the recurrence independently from h0[i] (or zero) and writes hT[i].
+ * Layouts: q, k, g_log [T, H, Dk] (g_log [T, H] with GLA_GATE_SCALAR); v, o [T, H, Dv];
+ * h0, hT [N, H, Dk, Dv] fp32; cu_seqlens: DEVICE int32 [N + 1], non-decreasing, cu_seqlens[0]
+ * = 0 and cu_seqlens[N] = T. The offsets are read on the device only: violations are
+ * reported by gla_last_device_status as GLA_ERR_BAD_SEQLENS. Sequences are not split
+ * (opt->seq_splits is ignored): the tensor-core path runs one CTA per sequence and head.
+ * Other arguments, options and errors as gla_fwd_ex. This serves the batch-efficiency concern
+ * of "面向长序列大模型的线性注意力算子性能评测方法与优化实践", section 四、评测维度设计 (no
+ * padding to the longest sequence of a batch); the pages define no varlen interface.
+ */
+gla_status gla_fwd_varlen(const void *q, const void *k, const void *v, const float *g_log,
+                          float scale, const float *h0, void *o, float *hT,
+                          const int32_t *cu_seqlens, int64_t N, int64_t T, int64_t H,
+                          int64_t Dk, int64_t Dv, int io, const gla_options *opt,
+                          gla_stream_t stream);
+
 /* Bytes of device workspace gla_fwd_ex needs for this shape and options (0 if none).
  * Returns 0 as well for arguments it would reject. */
 size_t gla_fwd_workspace_size(int64_t B, int64_t T, int64_t H, int64_t Dk, int64_t Dv,
@@ -145,7 +166,9 @@ int gla_path_for(int64_t B, int64_t T, int64_t H, int64_t Dk, int64_t Dv, int io
  * gla_last_device_status — synchronises `stream`, then reads and clears the library's
  * device error word on the current device. Returns GLA_OK, GLA_ERR_DEVICE_TIMEOUT when
  * a kernel abandoned a bounded pipeline wait (its outputs are then undefined, the
- * context stays usable), or GLA_ERR_LAUNCH when the synchronisation itself failed.
+ * context stays usable), GLA_ERR_BAD_SEQLENS when gla_fwd_varlen found offsets that are
+ * not non-decreasing within [0, T] (the affected sequences are left unwritten), or
+ * GLA_ERR_LAUNCH when the synchronisation itself failed.
  */
 gla_status gla_last_device_status(gla_stream_t stream);
 
