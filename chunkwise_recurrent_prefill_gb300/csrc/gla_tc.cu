@@ -287,7 +287,10 @@ __device__ __forceinline__ uint32_t par(int use) { return (uint32_t)use & 1u; }
 // 6-9 state + P conversion, the rest gate warps.
 // kScalar: one log-gate per token and head (g [B,T,H]) instead of one per key dimension; the
 // gates are then read by the gate warps straight from global memory, a chunk ahead.
-template <bool kScalar>
+// kPacked: the batches are sequences packed along one token axis at offsets a.cu; the rows
+// of a sequence's last chunk past its end are masked (batched tensors need no masking: the
+// rows past T are zero-filled by the tensor copies and clipped by the stores).
+template <bool kScalar, bool kPacked>
 __global__ void __launch_bounds__(kOutThreads, 1)
 gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg,
@@ -311,7 +314,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     int64_t tbase = 0, tend = a.T;
     int bmap = bidx;
     bool bad_seq = false;
-    if (a.cu) {
+    if (kPacked) {
         const int s0 = a.cu[bidx], s1 = a.cu[bidx + 1];
         bad_seq = s0 < 0 || s1 < s0 || s1 > a.T;
         tbase = bad_seq ? 0 : s0;
@@ -319,7 +322,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         bmap = 0;
     }
     int cb, ce;
-    if (a.cu) {
+    if (kPacked) {
         cb = 0;
         ce = (int)((tend - tbase + kC - 1) / kC);
     } else {
@@ -573,8 +576,8 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             }
             fence_proxy_async_smem();
             named_bar_sync(2, 128);
-            const int vr = valid_rows(c);
-            if (a.cu && vr < kC) {
+            const int vr = kPacked ? valid_rows(c) : kC;
+            if (kPacked && vr < kC) {
                 // the last chunk of a packed sequence: the rows past its end belong to the next
                 // one, so only the valid rows are written, from registers
                 const int64_t t0 = tbase + (int64_t)(cb + c) * kC;
@@ -816,8 +819,8 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             if (gt == 0) TRACE_OUT(16, c);
             const float *grow = reinterpret_cast<const float *>(sm + G + gs * GSLOT) + tb * kD + d;
             const float *gsrow = gsc + (c & 1) * kC + tb;   // scalar gates of this thread's range
-            const int vr = valid_rows(c);
-            if (!kScalar && vr < kC) {
+            const int vr = kPacked ? valid_rows(c) : kC;
+            if (!kScalar && kPacked && vr < kC) {
                 // rows past the sequence end hold another sequence's gates (packed sequences):
                 // this thread's own elements of them become 0 (no decay) before it reads them
                 for (int t = max(vr - tb, 0); t < tl; ++t)
@@ -884,7 +887,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             if (gt == 0) TRACE_OUT(1, c);
             uint8_t *qt = sm + qs * QSTAGE + Q + boxo;
             uint8_t *kt = sm + qs * QSTAGE + K + boxo;
-            if (vr < kC) {
+            if (kPacked && vr < kC) {
                 // and their keys become 0: they add nothing to P or to the state
                 for (int t = max(vr - tb, 0); t < tl; ++t)
                     *reinterpret_cast<uint32_t *>(kt + sw128_offset((uint32_t)(tb + t), col)) = 0u;
@@ -1284,17 +1287,21 @@ bool g_attr_done = false;
 
 cudaError_t set_attrs() {
     if (g_attr_done) return cudaSuccess;
-    const void *outs[2] = {(const void *)gla_tc_out_kernel<false>,
-                           (const void *)gla_tc_out_kernel<true>};
+    const void *outs[4] = {(const void *)gla_tc_out_kernel<false, false>,
+                           (const void *)gla_tc_out_kernel<true, false>,
+                           (const void *)gla_tc_out_kernel<false, true>,
+                           (const void *)gla_tc_out_kernel<true, true>};
     const void *states[2] = {(const void *)gla_tc_state_kernel<false>,
                              (const void *)gla_tc_state_kernel<true>};
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 4; ++i) {
         cudaError_t e = cudaFuncSetAttribute(outs[i], cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              om::ALLOC);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(states[i], cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 sm_::ALLOC);
-        if (e != cudaSuccess) return e;
+        if (i < 2) {
+            e = cudaFuncSetAttribute(states[i], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     sm_::ALLOC);
+            if (e != cudaSuccess) return e;
+        }
     }
     g_attr_done = true;
     return cudaSuccess;
@@ -1434,14 +1441,13 @@ cudaError_t launch_tc(const Problem &p, int splits, int num_sms, void *ws, size_
         cfg.stream = stream;
         cfg.attrs = pdl;
         cfg.numAttrs = 1;
-        e = scalar ? cudaLaunchKernelEx(&cfg, gla_tc_out_kernel<true>, mq, mk, mv, mg, mo, oa)
-                   : cudaLaunchKernelEx(&cfg, gla_tc_out_kernel<false>, mq, mk, mv, mg, mo, oa);
+        e = scalar
+                ? cudaLaunchKernelEx(&cfg, gla_tc_out_kernel<true, false>, mq, mk, mv, mg, mo, oa)
+                : cudaLaunchKernelEx(&cfg, gla_tc_out_kernel<false, false>, mq, mk, mv, mg, mo, oa);
     } else {
-        if (scalar)
-            gla_tc_out_kernel<true><<<bh * s, kOutThreads, om::ALLOC, stream>>>(mq, mk, mv, mg, mo, oa);
-        else
-            gla_tc_out_kernel<false><<<bh * s, kOutThreads, om::ALLOC, stream>>>(mq, mk, mv, mg, mo,
-                                                                                oa);
+        auto kern = p.cu ? (scalar ? gla_tc_out_kernel<true, true> : gla_tc_out_kernel<false, true>)
+                         : (scalar ? gla_tc_out_kernel<true, false> : gla_tc_out_kernel<false, false>);
+        kern<<<bh * s, kOutThreads, om::ALLOC, stream>>>(mq, mk, mv, mg, mo, oa);
         e = cudaGetLastError();
     }
     if (e != cudaSuccess) return e;
