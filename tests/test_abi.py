@@ -118,3 +118,26 @@ def test_step_validation(lib):
     assert _step(lib, o=0x5000000000 + 256) == 5        # o inside S: GLA_ERR_ALIAS
     assert _step(lib, S=0x4000000000) == 5              # S over g
     assert _step(lib, io=7) == 10                       # GLA_ERR_BAD_OPTION
+
+
+def _varlen(lib, cu=0x7000000000, N=2, T=128, H=2, Dk=128, Dv=128, io=0, gate=0, h0=None,
+            hT=None, o=0x5000000000):
+    from chunkwise_recurrent_prefill_gb300.gla import _Options
+    p = lambda x: None if x is None else ctypes.c_void_p(x)  # noqa: E731
+    opt = _Options()
+    opt.gate = gate
+    return lib.gla_fwd_varlen(p(A["q"]), p(A["k"]), p(A["v"]), p(A["g"]), ctypes.c_float(1.0),
+                              p(h0), p(o), p(hT), p(cu), N, T, H, Dk, Dv, io,
+                              ctypes.byref(opt), None)
+
+
+def test_varlen_validation(lib):
+    from chunkwise_recurrent_prefill_gb300.gla import load_library
+    load_library()   # sets the argument types
+    assert _varlen(lib, cu=None) == 1                    # offsets required when N > 0
+    assert _varlen(lib, N=-1) == 2
+    assert _varlen(lib, cu=0x7000000002) == 4            # int32 offsets: 4-byte aligned
+    assert _varlen(lib, gate=5) == 10
+    assert _varlen(lib, Dk=64, Dv=64, io=0) in (0, 3, 6, 8)   # valid shape: exact path or no GPU
+    assert _varlen(lib, hT=0x1000000000) == 5            # hT over q
+    assert _varlen(lib, o=0x7000000000 - 64) == 5        # o over the offsets
