@@ -914,11 +914,18 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     }
 #pragma unroll
                     for (int x = 0; x < kGateBlock; ++x) {
-                        r0 = fmaf(gv[x].x, kLog2e, r0);
-                        r1 = fmaf(gv[x].y, kLog2e, r1);
                         const float2 qf = unpack_bf16(qv[x]), kf = unpack_bf16(kv[x]);
-                        qv[x] = pack_bf16(qf.x * ex2(r0 + eq0), qf.y * ex2(r1 + eq1));
-                        kv[x] = pack_bf16(kf.x * ex2(ek0 - r0), kf.y * ex2(ek1 - r1));
+                        r0 = fmaf(gv[x].x, kLog2e, r0);
+                        if (kScalar) {
+                            // one gate for every key dimension: both columns share the factors
+                            const float fq = ex2(r0 + eq0), fk = ex2(ek0 - r0);
+                            qv[x] = pack_bf16(qf.x * fq, qf.y * fq);
+                            kv[x] = pack_bf16(kf.x * fk, kf.y * fk);
+                        } else {
+                            r1 = fmaf(gv[x].y, kLog2e, r1);
+                            qv[x] = pack_bf16(qf.x * ex2(r0 + eq0), qf.y * ex2(r1 + eq1));
+                            kv[x] = pack_bf16(kf.x * ex2(ek0 - r0), kf.y * ex2(ek1 - r1));
+                        }
                     }
 #pragma unroll
                     for (int x = 0; x < kGateBlock; ++x) {
@@ -1179,8 +1186,13 @@ gla_tc_state_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
             for (int x = 0; x < 16; ++x) {
                 const uint32_t off = sw128_offset(16 * qq + x, col);
                 const float2 kv = unpack_bf16(*reinterpret_cast<const uint32_t *>(kt + off));
-                *reinterpret_cast<uint32_t *>(kt + off) =
-                    pack_bf16(kv.x * ex2(s0 - b0[x]), kv.y * ex2(s1 - b1[x]));
+                if (kScalar) {   // one gate for every key dimension: one factor per token
+                    const float f = ex2(s0 - b0[x]);
+                    *reinterpret_cast<uint32_t *>(kt + off) = pack_bf16(kv.x * f, kv.y * f);
+                } else {
+                    *reinterpret_cast<uint32_t *>(kt + off) =
+                        pack_bf16(kv.x * ex2(s0 - b0[x]), kv.y * ex2(s1 - b1[x]));
+                }
             }
             l0 = s0;
             l1 = s1;
