@@ -45,7 +45,7 @@ cudaError_t launch_step(const void *q, const void *k, const void *v, const float
                         float *S, void *o, int64_t BH, int64_t Dk, int64_t Dv, int io,
                         cudaStream_t stream);
 
-// tcgen05 path (bf16 io, Dk = Dv = 128).
+// tcgen05 path (bf16 io, Dk and Dv in {64, 128}).
 bool tc_supported(const Problem &p);
 int tc_auto_splits(const Problem &p, int num_sms);
 int tc_state_pieces(const Problem &p, int splits, int num_sms);

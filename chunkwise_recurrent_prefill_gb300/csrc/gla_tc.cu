@@ -174,6 +174,8 @@ struct OutArgs {
     int last16;                        // weight of the last segment in 16ths (see seg_bound)
     const int *cu;                     // packed sequences: offsets [B+1] along T, or null
     __nv_bfloat16 *o;                  // output (rows a TMA store may not cover)
+    int Dk, Dv;                        // head dims of the caller's tensors (64 or 128); the
+                                       // kernels work at 128, padding with zeros
 };
 
 struct StateArgs {
@@ -581,14 +583,16 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 // the last chunk of a packed sequence: the rows past its end belong to the next
                 // one, so only the valid rows are written, from registers
                 const int64_t t0 = tbase + (int64_t)(cb + c) * kC;
-                __nv_bfloat16 *op = a.o + (t0 * a.H + h) * kD + v;
-                const int64_t rs = (int64_t)a.H * kD;   // row stride of o
+                __nv_bfloat16 *op = a.o + (t0 * a.H + h) * a.Dv + v;
+                const int64_t rs = (int64_t)a.H * a.Dv;   // row stride of o
+                if (v < a.Dv) {
 #pragma unroll
-                for (int x = 0; x < 32; ++x)
-                    if (x < vr) op[x * rs] = __float2bfloat16_rn(o0[x]);
+                    for (int x = 0; x < 32; ++x)
+                        if (x < vr) op[x * rs] = __float2bfloat16_rn(o0[x]);
 #pragma unroll
-                for (int x = 0; x < 32; ++x)
-                    if (32 + x < vr) op[(32 + x) * rs] = __float2bfloat16_rn(o1[x]);
+                    for (int x = 0; x < 32; ++x)
+                        if (32 + x < vr) op[(32 + x) * rs] = __float2bfloat16_rn(o1[x]);
+                }
                 named_bar_sync(2, 128);
                 if (et == 0) mbar_arrive(&bars[QEMPTY + c % NQ]);
             } else if (et == 0) {
@@ -596,7 +600,8 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 uint8_t *qt = sm + (c % NQ) * QSTAGE + Q;
                 const uint64_t pol = l2_policy_evict_first();
                 tma_store_4d_hint(&to, qt, 0, h, t0, bmap, pol);
-                tma_store_4d_hint(&to, qt + 8192, 64, h, t0, bmap, pol);
+                if (a.Dv > 64)   // no store is issued past the caller's last value column
+                    tma_store_4d_hint(&to, qt + 8192, 64, h, t0, bmap, pol);
                 bulk_commit();
                 bulk_wait_read_all();
                 mbar_arrive(&bars[QEMPTY + c % NQ]);   // the stage may be refilled
@@ -623,13 +628,16 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             if (threadIdx.x == 6 * 32) TRACE_GLOB(0, 1);
             init = a.sstart + ((size_t)bh * (a.splits - 1) + (seg - 1)) * (kD * kD);
         } else if (a.h0)
-            init = a.h0 + (size_t)bh * (kD * kD);
+            init = a.h0 + (size_t)bh * a.Dk * a.Dv;
+        // start states are 128 x 128 internally; h0 has the caller's Dk x Dv (zero padded)
+        const int irows = seg > 0 ? kD : a.Dk, icols = seg > 0 ? kD : a.Dv;
 #pragma unroll 1
         for (int d0 = 0; d0 < kD; d0 += 16) {
             uint32_t r[16];
 #pragma unroll
             for (int x = 0; x < 16; ++x)
-                r[x] = init ? __float_as_uint(init[(d0 + x) * kD + v]) : 0u;
+                r[x] = (init && d0 + x < irows && v < icols)
+                           ? __float_as_uint(init[(d0 + x) * icols + v]) : 0u;
             tmem_st16(tmem_addr(tm, j, kColS + d0), r);
         }
         tmem_wait_st();
@@ -705,12 +713,12 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 for (int x = 0; x < 64; ++x) prow[x] = 0.f;
                 float *gcol = scr, *qcol = scr + 64, *kcol = scr + 128, *bcol = scr + 192;
                 const int64_t t0 = tbase + (int64_t)(cb + c) * kC;
-                for (int d = 0; d < kD; ++d) {
+                for (int d = 0; d < a.Dk; ++d) {   // padded key dims add nothing
                     if (st_t < 64) {
                         const int64_t t = t0 + st_t;
                         const bool in = t < tend;
-                        const int64_t idx = (((int64_t)bmap * a.T + t) * a.H + h) * kD + d;
-                        gcol[st_t] = in ? (kScalar ? a.g[idx / kD] : a.g[idx]) : 0.f;
+                        const int64_t idx = (((int64_t)bmap * a.T + t) * a.H + h) * a.Dk + d;
+                        gcol[st_t] = in ? (kScalar ? a.g[idx / a.Dk] : a.g[idx]) : 0.f;
                         qcol[st_t] = in ? __bfloat162float(a.q[idx]) : 0.f;
                         kcol[st_t] = in ? __bfloat162float(a.k[idx]) : 0.f;
                     }
@@ -757,14 +765,16 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 ok = false;
             } else {
                 tc_fence_after();
-                float *hp = a.hT + (size_t)bh * (kD * kD) + v;
+                float *hp = a.hT + (size_t)bh * a.Dk * a.Dv + v;
 #pragma unroll 1
-                for (int half = 0; half < 2; ++half) {
+                for (int half = 0; half < a.Dk / 64; ++half) {
                     float sv[64];
                     tmem_ld64(tmem_addr(tm, j, kColS + half * 64), sv);
+                    if (v < a.Dv) {
 #pragma unroll
-                    for (int x = 0; x < 64; ++x)
-                        hp[(half * 64 + x) * kD] = sv[x] * ends_s[half * 64 + x];
+                        for (int x = 0; x < 64; ++x)
+                            hp[(half * 64 + x) * a.Dv] = sv[x] * ends_s[half * 64 + x];
+                    }
                 }
             }
         }
@@ -1250,7 +1260,7 @@ constexpr int kScanBatch = 4;
 __global__ void __launch_bounds__(kScanThreads)
 gla_tc_scan_kernel(const float *__restrict__ E, const float *__restrict__ gam,
                    const float *__restrict__ h0, float *__restrict__ sstart, int splits,
-                   int pieces) {
+                   int pieces, int Dk, int Dv) {
     pdl_launch_dependents();    // the output kernel may be scheduled now; it waits for us
     if (threadIdx.x == 0 && blockIdx.y == 0) TRACE_GLOB(2, 0);
     pdl_wait_prerequisites();   // the end states of the state kernel
@@ -1262,8 +1272,10 @@ gla_tc_scan_kernel(const float *__restrict__ E, const float *__restrict__ gam,
     constexpr size_t kDD = (size_t)kD * kD;
     float s[kScanPer];
 #pragma unroll
-    for (int i = 0; i < kScanPer; ++i)
-        s[i] = h0 ? h0[bh * kDD + e0 + i * kScanThreads] : 0.f;
+    for (int i = 0; i < kScanPer; ++i) {
+        const int e = e0 + i * kScanThreads, d = e / kD, v = e % kD;   // h0 is Dk x Dv
+        s[i] = (h0 && d < Dk && v < Dv) ? h0[bh * (size_t)Dk * Dv + (size_t)d * Dv + v] : 0.f;
+    }
     const float *Eb = E + bh * npc * kDD + e0;
     const float *gb = gam + bh * npc * kD;
     float *ob = sstart + bh * nseg * kDD + e0;
@@ -1328,7 +1340,10 @@ int clamp_splits(const Problem &p, int splits) {
 }  // namespace
 
 bool tc_supported(const Problem &p) {
-    return p.io == 0 && p.Dk == kD && p.Dv == kD && p.T < (int64_t(1) << 30) &&
+    // head dims 64 run on the 128-wide kernels: the tensor copies read zeros past the
+    // caller's last dimension, and zero keys and gates add nothing and decay nothing
+    const auto dim_ok = [](int64_t d) { return d == kD || d == 64; };
+    return p.io == 0 && dim_ok(p.Dk) && dim_ok(p.Dv) && p.T < (int64_t(1) << 30) &&
            p.B * p.H < (int64_t(1) << 24);
 }
 
@@ -1374,18 +1389,18 @@ cudaError_t launch_tc(const Problem &p, int splits, int num_sms, void *ws, size_
     cudaError_t e = set_attrs();
     if (e != cudaSuccess) return e;
     CUtensorMap mq, mk, mv, mg, mo;
-    if (!make_bthd_map(&mq, p.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, mB, p.T, p.H, kD, 64, kC,
+    if (!make_bthd_map(&mq, p.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, mB, p.T, p.H, p.Dk, 64, kC,
                        CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_bthd_map(&mk, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, mB, p.T, p.H, kD, 64, kC,
+        !make_bthd_map(&mk, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, mB, p.T, p.H, p.Dk, 64, kC,
                        CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_bthd_map(&mv, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, mB, p.T, p.H, kD, 64, kC,
+        !make_bthd_map(&mv, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, mB, p.T, p.H, p.Dv, 64, kC,
                        CU_TENSOR_MAP_SWIZZLE_128B) ||
         // per-key gates are staged by TMA; scalar gates are read directly (the map is unused)
-        !(scalar ? make_bthd_map(&mg, p.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, mB, p.T, p.H, kD,
-                                 64, kC, CU_TENSOR_MAP_SWIZZLE_128B)
-                 : make_bthd_map(&mg, p.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, mB, p.T, p.H, kD,
-                                 kD, kC, CU_TENSOR_MAP_SWIZZLE_NONE)) ||
-        !make_bthd_map(&mo, p.o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, mB, p.T, p.H, kD, 64, kC,
+        !(scalar ? make_bthd_map(&mg, p.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, mB, p.T, p.H,
+                                 p.Dk, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B)
+                 : make_bthd_map(&mg, p.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, mB, p.T, p.H,
+                                 p.Dk, kD, kC, CU_TENSOR_MAP_SWIZZLE_NONE)) ||
+        !make_bthd_map(&mo, p.o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, mB, p.T, p.H, p.Dv, 64, kC,
                        CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidResourceHandle;   // a tensor map could not be encoded
     const int nchunks = (int)((p.T + kC - 1) / kC);
@@ -1430,7 +1445,7 @@ cudaError_t launch_tc(const Problem &p, int splits, int num_sms, void *ws, size_
         cfg.attrs = pdl;
         cfg.numAttrs = 1;
         e = cudaLaunchKernelEx(&cfg, gla_tc_scan_kernel, (const float *)E, (const float *)gam,
-                               p.h0, sstart, s, pieces);
+                               p.h0, sstart, s, pieces, (int)p.Dk, (int)p.Dv);
         if (e != cudaSuccess) return e;
         count_launches(2);
     }
@@ -1441,7 +1456,7 @@ cudaError_t launch_tc(const Problem &p, int splits, int num_sms, void *ws, size_
                           ? std::min(1, nchunks / s - 1) : -1;
     OutArgs oa{static_cast<const __nv_bfloat16 *>(p.q), static_cast<const __nv_bfloat16 *>(p.k),
                p.g, p.h0, p.hT, sstart, p.T, (int)p.H, nchunks, s, p.scale, dev_err, stall,
-               last16, p.cu, static_cast<__nv_bfloat16 *>(p.o)};
+               last16, p.cu, static_cast<__nv_bfloat16 *>(p.o), (int)p.Dk, (int)p.Dv};
     if (s > 1) {
         cudaLaunchAttribute pdl[1];
         pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

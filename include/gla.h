@@ -22,8 +22,8 @@
  *     q, k, g_log : [B, T, H, Dk]
  *     v, o        : [B, T, H, Dv]
  *     h0, hT      : [B, H, Dk, Dv]   float32
- * Supported head dims: Dk = Dv = 128 on the tensor-core path; the exact CUDA-core path
- * also takes Dk, Dv in {64, 128}. Any T >= 0 (a partial last chunk is handled).
+ * Supported head dims: Dk, Dv in {64, 128} on both paths (the tensor-core kernels work at
+ * 128 and pad a head dim of 64 with zeros). Any T >= 0 (a partial last chunk is handled).
  *
  * Ownership and memory: every tensor pointer is a DEVICE pointer owned by the caller
  * and must be 16-byte aligned. o and hT must not overlap any input. The library never
@@ -110,7 +110,7 @@ gla_status gla_fwd_f32(const float *q, const float *k, const float *v, const flo
 /*
  * gla_fwd_ex — the general entry: io selects bf16 or fp32 q/k/v/o, opt (may be NULL)
  * selects the path, the sequence split, the workspace and the gate shape. The tensor-core
- * path needs bf16 I/O and Dk = Dv = 128.
+ * path needs bf16 I/O and Dk, Dv in {64, 128}.
  */
 gla_status gla_fwd_ex(const void *q, const void *k, const void *v, const float *g_log,
                       float scale, const float *h0, void *o, float *hT,

@@ -87,7 +87,7 @@ def test_unsupported_dims(lib):
     assert _call(lib, **A, Dk=96, opt=options("exact")) == 3
     assert _call(lib, **A, Dk=0) == 3
     assert _call(lib, **A, io=1, opt=options("tc")) == 3       # tensor cores need bf16 I/O
-    assert _call(lib, **A, Dk=64, Dv=64, opt=options("tc")) == 3
+    assert _call(lib, **A, Dk=96, Dv=96, opt=options("tc")) == 3      # 64 or 128 only
 
 
 def test_binding_refuses_cpu_tensors(lib):

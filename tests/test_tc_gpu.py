@@ -260,3 +260,25 @@ def test_tc_scalar_gate_workload():
     o_ref, _ = _oracle_scalar(x)
     eo = assert_close(o.float().cpu().numpy(), o_ref, "bf16", "scalar workload o")
     print(f"\nparity {w.name}: o max/mean rel {eo[0]:.3e}/{eo[1]:.3e}")
+
+
+# ---------------------------------------------------------------- head dim 64
+
+@pytest.mark.parametrize("Dk,Dv", [(64, 64), (64, 128), (128, 64)])
+@pytest.mark.parametrize("splits", [1, 3])
+@pytest.mark.parametrize("gate", ["key", "scalar"])
+def test_tc_head_dim_64(Dk, Dv, splits, gate):
+    """Head dims of 64 on the tensor-core path (the kernels pad to 128 with zeros)."""
+    from chunkwise_recurrent_prefill_gb300 import gla_fwd, last_device_status
+    from chunkwise_recurrent_prefill_gb300.gla import path_for
+    from chunkwise_recurrent_prefill_gb300.workloads import make_inputs, small
+    assert path_for(1, 512, 2, Dk=Dk, Dv=Dv) == "tc"
+    x = make_inputs(small("d64", B=2, T=700, H=3, seed=Dk + Dv + splits, with_h0=True, Dk=Dk,
+                          Dv=Dv, gate=gate), DEV)
+    o, hT = gla_fwd(x["q"], x["k"], x["v"], x["g"], x["scale"], x["h0"], return_state=True,
+                    path="tc", seq_splits=splits, gate=gate)
+    torch.cuda.synchronize()
+    assert last_device_status() == 0
+    o_ref, h_ref = _oracle_scalar(x) if gate == "scalar" else _oracle(x)
+    assert_close(o.float().cpu().numpy(), o_ref, "bf16", f"o(D={Dk}x{Dv})")
+    assert_close(hT.cpu().numpy(), h_ref, "bf16", f"hT(D={Dk}x{Dv})")
