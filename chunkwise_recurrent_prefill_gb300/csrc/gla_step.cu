@@ -13,7 +13,7 @@ namespace {
 
 constexpr int kStepWarps = 8;
 constexpr int kStepCols = 128;  // state columns (value dims) per CTA: four per lane
-constexpr int kStepBatch = 8;   // state rows a warp loads before it stores them
+constexpr int kStepBatch = 16;  // state rows a warp loads before it stores them
 
 template <typename T>
 __device__ __forceinline__ float ld_io(const T *p, size_t i);
@@ -36,7 +36,7 @@ __device__ __forceinline__ void st_io(__nv_bfloat16 *p, size_t i, float x) {
 // per-column dot products q . S[:, v] are summed across warps in shared memory in a fixed
 // order (no atomics: the result is deterministic). Dv is a multiple of 4.
 template <typename T>
-__global__ void __launch_bounds__(kStepWarps * 32, 3)
+__global__ void __launch_bounds__(kStepWarps * 32, 2)
 gla_step_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
                 const float *__restrict__ g, float scale, float *__restrict__ S,
                 T *__restrict__ o, int Dk, int Dv) {
