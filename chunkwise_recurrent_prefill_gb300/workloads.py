@@ -96,6 +96,47 @@ def small(name: str, B: int, T: int, H: int, io: str = "bf16", seed: int = 0,
                     want_hT=True, gate=gate)
 
 
+# Gated-delta-rule workloads (same shapes as the GLA bench and parity cases). Recipe:
+# ``torch.Generator('cpu').manual_seed(seed)``; draw order q, k, v, u (gate), w (write
+# strength), then h0. q and k ~ N(0, 1) rows divided by their L2 norm (unit-norm queries
+# and keys, the regime the delta write assumes), v ~ N(0, 1), g = logsigmoid(u) / 16 and
+# beta = sigmoid(w) with u, w ~ N(0, 1), one value each per token and head; h0 as above.
+GDN_WORKLOADS = {
+    "gdn_f32_B1_H2_T512": Workload("gdn_f32_B1_H2_T512", B=1, T=512, H=2, io="f32", seed=10),
+    "gdn_bf16_B1_H16_T4096": Workload("gdn_bf16_B1_H16_T4096", B=1, T=4096, H=16, seed=11),
+    "gdn_bf16_B1_H16_T16384": Workload("gdn_bf16_B1_H16_T16384", B=1, T=16384, H=16, seed=12),
+    "gdn_bf16_B16_H16_T4096_h0": Workload("gdn_bf16_B16_H16_T4096_h0", B=16, T=4096, H=16,
+                                          seed=13, with_h0=True, want_hT=True),
+}
+GDN_BENCH_WORKLOAD = "gdn_bf16_B1_H16_T16384"
+
+
+def make_gdn_inputs(w: Workload, device: str | torch.device = "cpu") -> dict:
+    """Inputs of a gated-delta-rule workload: q, k, v (io dtype), g, beta [B,T,H] float32,
+    h0 (float32 or None), scale."""
+    gen = torch.Generator("cpu").manual_seed(w.seed)
+    io = torch.bfloat16 if w.io == "bf16" else torch.float32
+
+    def draw(*shape):
+        return torch.randn(*shape, generator=gen, dtype=torch.float32)
+
+    def unit(x):
+        return x / x.norm(dim=-1, keepdim=True)
+
+    q = unit(draw(w.B, w.T, w.H, w.Dk)).to(io)
+    k = unit(draw(w.B, w.T, w.H, w.Dk)).to(io)
+    v = draw(w.B, w.T, w.H, w.Dv).to(io)
+    g = F.logsigmoid(draw(w.B, w.T, w.H)) / 16.0
+    beta = torch.sigmoid(draw(w.B, w.T, w.H))
+    h0 = draw(w.B, w.H, w.Dk, w.Dv) * 0.02 if w.with_h0 else None
+    out = dict(q=q, k=k, v=v, g=g, beta=beta, h0=h0, scale=float(w.Dk) ** -0.5)
+    if str(device) != "cpu":
+        for key in ("q", "k", "v", "g", "beta", "h0"):
+            if out[key] is not None:
+                out[key] = out[key].to(device)
+    return out
+
+
 # Decode-step workload: one token for each of B sequences and H heads on a resident state
 # (the step after prefill). Same recipe: q, k, v, u, then the state S = 0.02 * N(0, 1).
 STEP_WORKLOAD = dict(name="decode_B64_H16_D128", B=64, H=16, D=128, io="bf16", seed=5)
