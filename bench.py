@@ -51,8 +51,9 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU work of the oracle baseline sample")
-    ap.add_argument("--op", default="prefill", choices=["prefill", "step"],
-                    help="prefill (the headline) or one decode step on a resident state")
+    ap.add_argument("--op", default="prefill", choices=["prefill", "step", "gdn"],
+                    help="prefill (the headline), one decode step on a resident state, or the "
+                         "gated delta rule forward")
     return ap.parse_args()
 
 
@@ -516,14 +517,138 @@ def run_step(args, rank, world, dist):
         }), flush=True)
 
 
+def gdn_flops_per_token_head(Dk: int, Dv: int, C: int = 64) -> int:
+    """fp32 flops of the gated-delta-rule chunk algebra per token and head (causal halves
+    of the in-chunk products): K K^T and Q K^T 2*C*Dk, the triangular solves C*(Dk+Dv),
+    W S, Qh S and Kh^T U 6*Dk*Dv, P U C*Dv."""
+    return 2 * C * Dk + C * (Dk + Dv) + 6 * Dk * Dv + C * Dv
+
+
+def fp32_alu_peak_tflops(sm_mhz: float | None) -> tuple[float, str]:
+    """CUDA-core fp32 FMA peak: 152 SMs x 128 fp32 lanes x 2 flops x SM clock (the median
+    clock sampled in the timed region, else the 2070 MHz maximum)."""
+    mhz = sm_mhz or 2070.0
+    return 152 * 128 * 2 * mhz * 1e6 / 1e12, f"152 SMs x 128 fp32 lanes x 2 x {mhz:.0f} MHz"
+
+
+def run_gdn(args, rank, world, dist):
+    """The gated delta rule forward on its bench workload (B=1, H=16, T=16384, D=128, bf16)."""
+    import torch
+    from chunkwise_recurrent_prefill_gb300 import gla
+    from chunkwise_recurrent_prefill_gb300.workloads import (GDN_BENCH_WORKLOAD, GDN_WORKLOADS,
+                                                             make_gdn_inputs)
+    w = GDN_WORKLOADS[args.workload or GDN_BENCH_WORKLOAD]
+    import __graft_entry__
+    __graft_entry__.build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    x_cpu = make_gdn_inputs(w)
+    x = {k_: (v_.to(dev) if hasattr(v_, "to") else v_) for k_, v_ in x_cpu.items()}
+    o = torch.empty((w.B, w.T, w.H, w.Dv), dtype=x["q"].dtype, device=dev)
+    hT = torch.empty((w.B, w.H, w.Dk, w.Dv), dtype=torch.float32, device=dev) \
+        if w.want_hT else None
+    ws = torch.empty(gla.gdn_workspace_size(w.B, w.T, w.H, w.Dk, w.Dv), dtype=torch.uint8,
+                     device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        gla.gdn_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], x["h0"], o=o, hT=hT,
+                    workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert gla.last_device_status() == 0
+    gid = str(torch.cuda.get_device_properties(dev).uuid)
+    sampler = ClockSampler(gid if gid.startswith("GPU-") else "GPU-" + gid)
+    sampler.start()
+    time.sleep(0.3)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = gla.launch_counter()
+    t_lo = time.time()
+    for i in range(args.steps):
+        flush.zero_()
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    t_hi = time.time()
+    if dist:
+        dist.barrier()
+    launches = gla.launch_counter() - launches0
+    time.sleep(0.2)
+    sampler.mark(t_lo, t_hi)
+    sampler.stop()
+    assert gla.last_device_status() == 0
+    ms = sorted(a.elapsed_time(b) for a, b in evs)
+    total_s = max_over_ranks(sum(ms) / 1e3, dist, dev)
+    per = total_s / args.steps
+    clocks = sampler.summary()
+    flops = w.B * w.T * w.H * gdn_flops_per_token_head(w.Dk, w.Dv)
+    peak, peak_src = fp32_alu_peak_tflops(clocks.get("sm_mhz"))
+    achieved = flops / per / 1e12
+    es = 2 if w.io == "bf16" else 4
+    nbytes = w.B * w.T * w.H * ((2 * w.Dk + 2 * w.Dv) * es + 8)
+    hbm_gbs, _, _ = load_peaks()
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = gdn_cpu_oracle_sample(w, x_cpu, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps({
+            "metric": "gated delta rule prefill fwd tokens/s (B·T, H=16 D=128 bf16)",
+            "value": weak_scaling_value(w.B * w.T, args.steps, world, total_s),
+            "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * per, "ms_p50": ms[len(ms) // 2],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded unit-norm q/k, N(0,1) v, logsigmoid(N(0,1))/16 gates, "
+                    "sigmoid(N(0,1)) write strengths)",
+            "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "Dk": w.Dk, "Dv": w.Dv,
+                       "io": w.io, "h0": w.with_h0, "hT": w.want_hT, "path": "gdn (fp32 CUDA cores)",
+                       "l2": "flushed by a 256 MiB device write before every timed step"},
+            "clocks": clocks, "gpu_launches": launches,
+            "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": None,
+                         "peak_source": f"derived: {peak_src}",
+                         "algorithmic_flops_per_launch": flops,
+                         "algorithmic_bytes_per_launch": nbytes,
+                         "hbm_frac": nbytes / per / 1e9 / hbm_gbs,
+                         "kernel": "gdn_prep + gdn_scan (one call)"},
+            "e2e": None, "cpu_baseline": cpu,
+        }), flush=True)
+
+
+def gdn_cpu_oracle_sample(w, x_cpu, target_s: float):
+    """The fp64 numpy token loop of the gated delta rule on the first T_s tokens of every
+    (batch, head) pair, T_s sized for about target_s of host time."""
+    from oracle import gdn_ref
+    cut = lambda t, n: None if t is None else t[:, :n]   # noqa: E731
+    args_ = lambda n: [cut(x_cpu[k_], n) for k_ in ("q", "k", "v", "g", "beta")]   # noqa: E731
+    cal = min(w.T, 64)
+    t0 = time.perf_counter()
+    gdn_ref.recurrent(*args_(cal), x_cpu["scale"], x_cpu["h0"])
+    rate = w.B * cal / max(time.perf_counter() - t0, 1e-6)
+    T_s = int(min(w.T, max(64, target_s * rate / w.B)))
+    t0 = time.perf_counter()
+    gdn_ref.recurrent(*args_(T_s), x_cpu["scale"], x_cpu["h0"])
+    dt = time.perf_counter() - t0
+    return {"value": w.B * T_s / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {T_s} of {w.T} tokens of all {w.B}x{w.H} (batch, head) pairs, "
+                      f"fp64 numpy token loop (single-threaded einsum), {dt:.2f} s"}
+
+
 def main():
     args = parse_args()
     from chunkwise_recurrent_prefill_gb300.workloads import BENCH_WORKLOAD, WORKLOADS
-    w = WORKLOADS[args.workload or BENCH_WORKLOAD]
+    w = WORKLOADS[args.workload or BENCH_WORKLOAD] if args.op != "gdn" else None
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
-        run_reference(args, w, rank, world)
+        run_reference(args, w or WORKLOADS[BENCH_WORKLOAD], rank, world)
         return
     import torch
     dist = None
@@ -538,6 +663,8 @@ def main():
     try:
         if args.op == "step":
             run_step(args, rank, world, dist)
+        elif args.op == "gdn":
+            run_gdn(args, rank, world, dist)
         else:
             run_ours(args, w, rank, world, dist)
     finally:

@@ -1,0 +1,518 @@
+// Gated delta rule forward (prefill), chunkwise, fp32 CUDA cores.
+//
+// Per batch and head, with one log-gate g_t and one write strength beta_t per token:
+//     S_t = exp(g_t) (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T,   o_t = scale q_t S_t
+// (the gated-delta-network family named in "面向长序列大模型的线性注意力算子性能评测方法与
+// 优化实践", section 三.3, and "线性注意力GPU算子库的定义与技术解析", section 三; the formula is
+// the published gated delta rule, which the pages do not print).
+//
+// Chunk algebra (C = 64 tokens, start state S0, b_i the inclusive in-chunk cumulative
+// log-gate): the new values the chunk writes are U = Ut - W S0, where (I + A) Ut = diag(beta) V,
+// (I + A) W = diag(beta exp(b)) K and A_jm = beta_j exp(b_j - b_m) k_j.k_m for m < j. Then
+//     O   = scale (diag(exp(b)) Q S0 + P U),   P_ij = exp(b_i - b_j) q_i.k_j for j <= i
+//     S1  = exp(b_63) S0 + Kh^T U,             Kh_j = exp(b_63 - b_j) k_j.
+// Everything that does not depend on S0 (A, the triangular solves, P, the decay factors) is
+// computed for all chunks at once by gdn_prep_kernel and written to a workspace; the state
+// then runs through the chunks in gdn_scan_kernel, one CTA per (batch, head, block of state
+// columns): the columns of S are independent under this recurrence (the transition acts on
+// the key axis only), which is what lets B = 1 spread over many SMs.
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "gla_internal.h"
+
+namespace gla {
+namespace {
+
+constexpr int kC = 64;          // tokens per chunk
+constexpr int kMaxD = 128;      // largest head dim
+constexpr int kThreads = 256;
+constexpr int kPrepStride = kC + 4;   // padded row of the transposed q/k tiles (see the loads)
+
+template <typename T>
+__device__ __forceinline__ float ld_io(const T *p, int64_t i);
+template <>
+__device__ __forceinline__ float ld_io<float>(const float *p, int64_t i) {
+    return p[i];
+}
+template <>
+__device__ __forceinline__ float ld_io<__nv_bfloat16>(const __nv_bfloat16 *p, int64_t i) {
+    return __bfloat162float(p[i]);
+}
+__device__ __forceinline__ void st_io(float *p, int64_t i, float x) { p[i] = x; }
+__device__ __forceinline__ void st_io(__nv_bfloat16 *p, int64_t i, float x) {
+    p[i] = __float2bfloat16_rn(x);
+}
+
+// Workspace of one (batch, head, chunk), in floats (every offset a multiple of 4):
+//   Wt [Dk][64]  W transposed       Ut [64][Dv] the solved values
+//   Pt [64][64]  P transposed (scale folded in, zero above the diagonal)
+//   Qh [Dk][64]  scale exp(b_i) q_i, transposed
+//   Kh [64][Dk]  exp(b_63 - b_j) k_j
+//   gc [4]       exp(b_63), 0, 0, 0
+struct WsLayout {
+    int64_t oW, oU, oP, oQ, oK, oG, total;
+    __host__ __device__ WsLayout(int Dk, int Dv) {
+        oW = 0;
+        oU = oW + (int64_t)Dk * kC;
+        oP = oU + (int64_t)kC * Dv;
+        oQ = oP + kC * kC;
+        oK = oQ + (int64_t)Dk * kC;
+        oG = oK + (int64_t)kC * Dk;
+        total = oG + 4;
+    }
+};
+
+struct GdnArgs {
+    const void *q, *k, *v;
+    const float *g, *beta;
+    float scale;
+    const float *h0;
+    void *o;
+    float *hT;
+    int64_t T;
+    int H, Dk, Dv, nchunks;
+    float *ws;
+};
+
+// ---------------------------------------------------------------------------------------
+// Chunk-parallel part: one CTA per (batch, head, chunk).
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 2) gdn_prep_kernel(GdnArgs a) {
+    extern __shared__ __align__(16) float smp[];
+    float *Qt = smp;                                  // [Dk][kPrepStride]
+    float *Kt = Qt + kMaxD * kPrepStride;             // [Dk][kPrepStride]
+    float *As = Kt + kMaxD * kPrepStride;             // [64][64] strictly lower A
+    float *bs = As + kC * kC;                         // [64] cumulative log-gate b_j
+    float *be = bs + kC;                              // [64] beta_j
+    float *eb = be + kC;                              // [64] exp(b_j)
+    float *bg = eb + kC;                              // [64] beta_j exp(b_j)
+    float *ek = bg + kC;                              // [64] exp(b_63 - b_j)
+    const int tid = threadIdx.x;
+    const int64_t blk = blockIdx.x;
+    const int c = (int)(blk % a.nchunks);
+    const int64_t bh = blk / a.nchunks;
+    const int64_t bb = bh / a.H, h = bh % a.H;
+    const int Dk = a.Dk, Dv = a.Dv;
+    const int64_t t0 = (int64_t)c * kC;
+    const int nval = (int)(a.T - t0 < kC ? a.T - t0 : kC);   // valid tokens of this chunk
+    const T *q = static_cast<const T *>(a.q), *k = static_cast<const T *>(a.k);
+    const T *v = static_cast<const T *>(a.v);
+    auto row = [&](int j) -> int64_t { return (bb * a.T + t0 + j) * a.H + h; };   // token row
+
+    // q, k transposed into [d][j] (rows past the sequence end are zero). A warp covers 8
+    // consecutive d and 4 consecutive j, so with the padded stride its 32 stores hit 32
+    // different banks.
+    const int dk8 = (Dk + 7) & ~7;
+    for (int idx = tid; idx < kC * dk8; idx += kThreads) {
+        const int dlo = idx & 7, j = (idx >> 3) & (kC - 1), d = (idx >> 9) * 8 + dlo;
+        if (d < Dk) {
+            const bool in = j < nval;
+            Qt[d * kPrepStride + j] = in ? ld_io(q, row(j) * Dk + d) : 0.f;
+            Kt[d * kPrepStride + j] = in ? ld_io(k, row(j) * Dk + d) : 0.f;
+        }
+    }
+    if (tid < kC) {
+        const bool in = tid < nval;
+        bs[tid] = in ? a.g[row(tid)] : 0.f;
+        be[tid] = in ? a.beta[row(tid)] : 0.f;
+    }
+    __syncthreads();
+    if (tid == 0) {   // inclusive cumulative sum, left to right
+        float s = 0.f;
+        for (int j = 0; j < kC; ++j) {
+            s += bs[j];
+            bs[j] = s;
+        }
+    }
+    __syncthreads();
+    if (tid < kC) {
+        eb[tid] = expf(bs[tid]);
+        bg[tid] = be[tid] * eb[tid];
+        ek[tid] = expf(bs[kC - 1] - bs[tid]);
+    }
+    __syncthreads();
+
+    float *ws = a.ws + blk * WsLayout(Dk, Dv).total;
+    const WsLayout L(Dk, Dv);
+
+    // K K^T and Q K^T, one 4 x 4 tile of each per thread: rows 4 mg .., columns 4 ng ..
+    {
+        const int mg = tid >> 4, ng = tid & 15;
+        float kk[16], qk[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x) kk[x] = qk[x] = 0.f;
+#pragma unroll 4
+        for (int d = 0; d < Dk; ++d) {
+            const float4 ka = *reinterpret_cast<const float4 *>(Kt + d * kPrepStride + 4 * mg);
+            const float4 qa = *reinterpret_cast<const float4 *>(Qt + d * kPrepStride + 4 * mg);
+            const float4 kb = *reinterpret_cast<const float4 *>(Kt + d * kPrepStride + 4 * ng);
+            const float ar[4] = {ka.x, ka.y, ka.z, ka.w}, qr[4] = {qa.x, qa.y, qa.z, qa.w};
+            const float bc[4] = {kb.x, kb.y, kb.z, kb.w};
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    kk[r * 4 + cc] = fmaf(ar[r], bc[cc], kk[r * 4 + cc]);
+                    qk[r * 4 + cc] = fmaf(qr[r], bc[cc], qk[r * 4 + cc]);
+                }
+        }
+        // A_jm = beta_j exp(b_j - b_m) k_j.k_m for m < j
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int j = 4 * mg + r;
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                const int m = 4 * ng + cc;
+                As[j * kC + m] = m < j ? be[j] * expf(bs[j] - bs[m]) * kk[r * 4 + cc] : 0.f;
+            }
+        }
+        // P^T: Pt[j][i] = scale exp(b_i - b_j) q_i.k_j for j <= i
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+            const int j = 4 * ng + cc;
+            float pr[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int i = 4 * mg + r;
+                pr[r] = j <= i ? a.scale * expf(bs[i] - bs[j]) * qk[r * 4 + cc] : 0.f;
+            }
+            *reinterpret_cast<float4 *>(ws + L.oP + j * kC + 4 * mg) =
+                make_float4(pr[0], pr[1], pr[2], pr[3]);
+        }
+    }
+    __syncthreads();
+
+    // Forward substitution, one right-hand-side column per thread:
+    //   x_j = r_j - sum_{m<j} A_jm x_m,  r_j = beta_j exp(b_j) k_j[col]  (col < Dk: W)
+    //                                     r_j = beta_j v_j[col - Dk]    (otherwise: Ut)
+    const int col = tid;
+    if (col < Dk + Dv) {
+        const bool isk = col < Dk;
+        const int cv = col - Dk;
+        float x[kC];
+#pragma unroll
+        for (int j = 0; j < kC; ++j) {
+            float r;
+            if (isk) r = bg[j] * Kt[col * kPrepStride + j];
+            else r = j < nval ? be[j] * ld_io(v, row(j) * Dv + cv) : 0.f;
+            float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+            for (int m = 0; m + 3 < j; m += 4) {
+                const float4 av = *reinterpret_cast<const float4 *>(As + j * kC + m);
+                s0 = fmaf(av.x, x[m], s0);
+                s1 = fmaf(av.y, x[m + 1], s1);
+                s0 = fmaf(av.z, x[m + 2], s0);
+                s1 = fmaf(av.w, x[m + 3], s1);
+            }
+#pragma unroll
+            for (int m = j & ~3; m < j; ++m) s0 = fmaf(As[j * kC + m], x[m], s0);
+            x[j] = r - (s0 + s1);
+        }
+        if (isk) {
+            float *wt = ws + L.oW + (int64_t)col * kC;
+#pragma unroll
+            for (int j = 0; j < kC; j += 4)
+                *reinterpret_cast<float4 *>(wt + j) = make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
+        } else {
+            float *ut = ws + L.oU + cv;
+#pragma unroll
+            for (int j = 0; j < kC; ++j) ut[(int64_t)j * Dv] = x[j];
+        }
+    }
+
+    // Qh (transposed, scale exp(b_i) q_i), Kh (exp(b_63 - b_j) k_j, rows), exp(b_63)
+    for (int idx = tid; idx < Dk * kC; idx += kThreads) {
+        const int d = idx / kC, i = idx % kC;
+        ws[L.oQ + idx] = a.scale * eb[i] * Qt[d * kPrepStride + i];
+    }
+    for (int idx = tid; idx < kC * Dk; idx += kThreads) {
+        const int j = idx / Dk, d = idx % Dk;
+        ws[L.oK + idx] = j < nval ? ek[j] * ld_io(k, row(j) * Dk + d) : 0.f;
+    }
+    if (tid < 4) ws[L.oG + tid] = tid == 0 ? eb[kC - 1] : 0.f;
+}
+
+// ---------------------------------------------------------------------------------------
+// Serial part: one CTA per (batch, head, block of NV state columns), through all chunks.
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void cp16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(dst)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_wait2() { asm volatile("cp.async.wait_group 2;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_wait0() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
+
+// acc[r][c] += sum_{k in [k0,k1)} A[k][m0 + r] B[k][n0 + c]: every lane of a warp reads the
+// same k row, so both float4 loads are conflict-free.
+__device__ __forceinline__ void outer_acc(float acc[16], const float *A, int lda, const float *B,
+                                          int ldb, int m0, int n0, int k0, int k1) {
+#pragma unroll 4
+    for (int kk = k0; kk < k1; ++kk) {
+        const float4 av = *reinterpret_cast<const float4 *>(A + kk * lda + m0);
+        const float4 bv = *reinterpret_cast<const float4 *>(B + kk * ldb + n0);
+        const float ar[4] = {av.x, av.y, av.z, av.w}, br[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[r * 4 + c] = fmaf(ar[r], br[c], acc[r * 4 + c]);
+    }
+}
+
+// Sums the k-split partial tiles into the threads of split 0 (fixed order: deterministic).
+// Every thread of the CTA calls it.
+__device__ __forceinline__ void reduce_splits(float acc[16], float *red, int ks, int KS, int nt,
+                                              int tile) {
+    if (KS == 1) return;
+    if (ks > 0 && ks < KS) {
+        float4 *dst = reinterpret_cast<float4 *>(red + ((int64_t)(ks - 1) * nt + tile) * 16);
+#pragma unroll
+        for (int x = 0; x < 4; ++x)
+            dst[x] = make_float4(acc[4 * x], acc[4 * x + 1], acc[4 * x + 2], acc[4 * x + 3]);
+    }
+    __syncthreads();
+    if (ks == 0) {
+        for (int s = 1; s < KS; ++s) {
+            const float4 *src = reinterpret_cast<const float4 *>(red + ((int64_t)(s - 1) * nt + tile) * 16);
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+                const float4 p = src[x];
+                acc[4 * x] += p.x;
+                acc[4 * x + 1] += p.y;
+                acc[4 * x + 2] += p.z;
+                acc[4 * x + 3] += p.w;
+            }
+        }
+    }
+}
+
+template <int NV>
+struct ScanSmem {
+    static constexpr int S = 0;                          // [Dk][NV] state block
+    static constexpr int U = S + kMaxD * NV;             // [64][NV] new values
+    static constexpr int W = U + kC * NV;                // [Dk][64]   group A
+    static constexpr int UT = W + kMaxD * kC;            // [64][NV]   group A
+    static constexpr int Q = UT + kC * NV;               // [Dk][64]   group B
+    static constexpr int P = Q + kMaxD * kC;             // [64][64]   group B
+    static constexpr int K = P + kC * kC;                // [64][Dk]   group C
+    static constexpr int G = K + kC * kMaxD;             // [4]        group C
+    static constexpr int RED = G + 4;                    // k-split partial tiles
+    static constexpr int kRedFloats = 3 * 64 * 16;
+    static constexpr int kFloats = RED + kRedFloats;
+};
+
+template <typename T, int NV>
+__global__ void __launch_bounds__(kThreads, 1) gdn_scan_kernel(GdnArgs a) {
+    using SM = ScanSmem<NV>;
+    extern __shared__ __align__(16) float sm[];
+    float *S = sm + SM::S, *U = sm + SM::U, *Wt = sm + SM::W, *Ut = sm + SM::UT;
+    float *Qh = sm + SM::Q, *Pt = sm + SM::P, *Kh = sm + SM::K, *gc = sm + SM::G;
+    float *red = sm + SM::RED;
+    const int tid = threadIdx.x;
+    const int nvb = a.Dv / NV;
+    const int64_t bh = blockIdx.x / nvb;
+    const int v0 = (int)(blockIdx.x % nvb) * NV;
+    const int64_t bb = bh / a.H, h = bh % a.H;
+    const int Dk = a.Dk, Dv = a.Dv, n = a.nchunks;
+    const WsLayout L(Dk, Dv);
+    const float *wsh = a.ws + bh * n * L.total;   // this head's chunks
+    T *o = static_cast<T *>(a.o);
+
+    auto issue_a = [&](int c) {
+        if (c < n) {
+            const float *src = wsh + (int64_t)c * L.total;
+            for (int i = tid; i < Dk * kC / 4; i += kThreads) cp16(Wt + 4 * i, src + L.oW + 4 * i);
+            for (int i = tid; i < kC * NV / 4; i += kThreads) {
+                const int j = i / (NV / 4), x = i % (NV / 4);
+                cp16(Ut + j * NV + 4 * x, src + L.oU + (int64_t)j * Dv + v0 + 4 * x);
+            }
+        }
+        cp_commit();
+    };
+    auto issue_b = [&](int c) {
+        if (c < n) {
+            const float *src = wsh + (int64_t)c * L.total;
+            for (int i = tid; i < Dk * kC / 4; i += kThreads) cp16(Qh + 4 * i, src + L.oQ + 4 * i);
+            for (int i = tid; i < kC * kC / 4; i += kThreads) cp16(Pt + 4 * i, src + L.oP + 4 * i);
+        }
+        cp_commit();
+    };
+    auto issue_c = [&](int c) {
+        if (c < n) {
+            const float *src = wsh + (int64_t)c * L.total;
+            for (int i = tid; i < kC * Dk / 4; i += kThreads) cp16(Kh + 4 * i, src + L.oK + 4 * i);
+            if (tid == 0) cp16(gc, src + L.oG);
+        }
+        cp_commit();
+    };
+
+    // state block from h0 (or zero)
+    for (int i = tid; i < Dk * NV; i += kThreads) {
+        const int d = i / NV, x = i % NV;
+        S[i] = a.h0 ? a.h0[(bh * Dk + d) * Dv + v0 + x] : 0.f;
+    }
+    issue_a(0);
+    issue_b(0);
+    issue_c(0);
+
+    // tile maps: U and O are [64][NV] (nt1 tiles), the state is [Dk][NV] (nt3 tiles)
+    // k-split: ks splits of the contraction per tile, at most 4 (the partial-tile buffer)
+    const int nt1 = 16 * (NV / 4), ks1n = min(kThreads / nt1, 4);
+    const int ks1 = tid / nt1, tile1 = tid % nt1;
+    const int m1 = 4 * (tile1 / (NV / 4)), n1 = 4 * (tile1 % (NV / 4));
+    const int nt3 = (Dk / 4) * (NV / 4), ks3n = min(kThreads / nt3, 4);
+    const int ks3 = tid / nt3, tile3 = tid % nt3;
+    const int m3 = 4 * (tile3 / (NV / 4)), n3 = 4 * (tile3 % (NV / 4));
+
+    for (int c = 0; c < n; ++c) {
+        // ---- U = Ut - W S   (W S: k over the key dims)
+        cp_wait2();
+        __syncthreads();
+        {
+            float acc[16];
+#pragma unroll
+            for (int x = 0; x < 16; ++x) acc[x] = 0.f;
+            if (ks1 < ks1n)
+                outer_acc(acc, Wt, kC, S, NV, m1, n1, ks1 * Dk / ks1n, (ks1 + 1) * Dk / ks1n);
+            reduce_splits(acc, red, ks1, ks1n, nt1, tile1);
+            if (ks1 == 0) {
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const float4 ut = *reinterpret_cast<const float4 *>(Ut + (m1 + r) * NV + n1);
+                    *reinterpret_cast<float4 *>(U + (m1 + r) * NV + n1) =
+                        make_float4(ut.x - acc[4 * r], ut.y - acc[4 * r + 1], ut.z - acc[4 * r + 2],
+                                    ut.w - acc[4 * r + 3]);
+                }
+            }
+        }
+        __syncthreads();
+        issue_a(c + 1);
+        // ---- O = Qh S + P U
+        cp_wait2();
+        __syncthreads();
+        {
+            float acc[16];
+#pragma unroll
+            for (int x = 0; x < 16; ++x) acc[x] = 0.f;
+            if (ks1 < ks1n) {
+                outer_acc(acc, Qh, kC, S, NV, m1, n1, ks1 * Dk / ks1n, (ks1 + 1) * Dk / ks1n);
+                outer_acc(acc, Pt, kC, U, NV, m1, n1, ks1 * kC / ks1n, (ks1 + 1) * kC / ks1n);
+            }
+            reduce_splits(acc, red, ks1, ks1n, nt1, tile1);
+            if (ks1 == 0) {
+                const int64_t tbase = (int64_t)c * kC;
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int64_t t = tbase + m1 + r;
+                    if (t < a.T) {
+                        const int64_t off = ((bb * a.T + t) * a.H + h) * Dv + v0 + n1;
+#pragma unroll
+                        for (int x = 0; x < 4; ++x) st_io(o, off + x, acc[4 * r + x]);
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        issue_b(c + 1);
+        // ---- S = exp(b_63) S + Kh^T U
+        cp_wait2();
+        __syncthreads();
+        {
+            float acc[16];
+#pragma unroll
+            for (int x = 0; x < 16; ++x) acc[x] = 0.f;
+            if (ks3 < ks3n)
+                outer_acc(acc, Kh, Dk, U, NV, m3, n3, ks3 * kC / ks3n, (ks3 + 1) * kC / ks3n);
+            reduce_splits(acc, red, ks3, ks3n, nt3, tile3);
+            if (ks3 == 0) {
+                const float dec = gc[0];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    float4 *sp = reinterpret_cast<float4 *>(S + (m3 + r) * NV + n3);
+                    const float4 s = *sp;
+                    *sp = make_float4(fmaf(dec, s.x, acc[4 * r]), fmaf(dec, s.y, acc[4 * r + 1]),
+                                      fmaf(dec, s.z, acc[4 * r + 2]), fmaf(dec, s.w, acc[4 * r + 3]));
+                }
+            }
+        }
+        __syncthreads();
+        issue_c(c + 1);
+    }
+    cp_wait0();
+    if (a.hT) {
+        for (int i = tid; i < Dk * NV; i += kThreads) {
+            const int d = i / NV, x = i % NV;
+            a.hT[(bh * Dk + d) * Dv + v0 + x] = S[i];
+        }
+    }
+}
+
+constexpr size_t kPrepSmem = (size_t)(2 * kMaxD * kPrepStride + kC * kC + 5 * kC) * sizeof(float);
+
+template <typename T>
+cudaError_t launch_typed(const GdnArgs &a, int64_t BH, int num_sms, cudaStream_t s) {
+    const int64_t nprep = BH * a.nchunks;
+    cudaError_t e = cudaFuncSetAttribute(gdn_prep_kernel<T>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem);
+    if (e != cudaSuccess) return e;
+    gdn_prep_kernel<T><<<(unsigned)nprep, kThreads, kPrepSmem, s>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // 16 state columns per CTA where 32 would leave SMs idle
+    const bool narrow = BH * (a.Dv / 32) < num_sms || a.Dv % 32 != 0;
+    if (narrow) {
+        const size_t smem = ScanSmem<16>::kFloats * sizeof(float);
+        e = cudaFuncSetAttribute(gdn_scan_kernel<T, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+        if (e != cudaSuccess) return e;
+        gdn_scan_kernel<T, 16><<<(unsigned)(BH * (a.Dv / 16)), kThreads, smem, s>>>(a);
+    } else {
+        const size_t smem = ScanSmem<32>::kFloats * sizeof(float);
+        e = cudaFuncSetAttribute(gdn_scan_kernel<T, 32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+        if (e != cudaSuccess) return e;
+        gdn_scan_kernel<T, 32><<<(unsigned)(BH * (a.Dv / 32)), kThreads, smem, s>>>(a);
+    }
+    e = cudaGetLastError();
+    if (e == cudaSuccess) count_launches(2);
+    return e;
+}
+
+}  // namespace
+
+bool gdn_supported(int64_t Dk, int64_t Dv) {
+    return Dk >= 4 && Dk <= kMaxD && Dk % 4 == 0 && Dv >= 16 && Dv <= kMaxD && Dv % 16 == 0;
+}
+
+size_t gdn_workspace_bytes(int64_t B, int64_t T, int64_t H, int64_t Dk, int64_t Dv) {
+    const int64_t nchunks = (T + kC - 1) / kC;
+    return (size_t)(B * H * nchunks) * (size_t)WsLayout((int)Dk, (int)Dv).total * sizeof(float);
+}
+
+cudaError_t launch_gdn(const GdnProblem &p, void *ws, int num_sms, cudaStream_t s) {
+    GdnArgs a;
+    a.q = p.q;
+    a.k = p.k;
+    a.v = p.v;
+    a.g = p.g;
+    a.beta = p.beta;
+    a.scale = p.scale;
+    a.h0 = p.h0;
+    a.o = p.o;
+    a.hT = p.hT;
+    a.T = p.T;
+    a.H = (int)p.H;
+    a.Dk = (int)p.Dk;
+    a.Dv = (int)p.Dv;
+    a.nchunks = (int)((p.T + kC - 1) / kC);
+    a.ws = static_cast<float *>(ws);
+    const int64_t BH = p.B * p.H;
+    return p.io == 0 /* bf16 */ ? launch_typed<__nv_bfloat16>(a, BH, num_sms, s)
+                     : launch_typed<float>(a, BH, num_sms, s);
+}
+
+}  // namespace gla

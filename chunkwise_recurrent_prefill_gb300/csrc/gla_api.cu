@@ -369,6 +369,63 @@ gla_status gla_step(const void *q, const void *k, const void *v, const float *g_
     return GLA_OK;
 }
 
+size_t gdn_fwd_workspace_size(int64_t B, int64_t T, int64_t H, int64_t Dk, int64_t Dv) {
+    Sizes sz;
+    if (validate_shape(B, T, H, Dk, Dv, GLA_IO_BF16, &sz) != GLA_OK) return 0;
+    if (!gla::gdn_supported(Dk, Dv) || sz.nqk == 0) return 0;
+    return gla::gdn_workspace_bytes(B, T, H, Dk, Dv);
+}
+
+gla_status gdn_fwd(const void *q, const void *k, const void *v, const float *g_log,
+                   const float *beta, float scale, const float *h0, void *o, float *hT,
+                   int64_t B, int64_t T, int64_t H, int64_t Dk, int64_t Dv, int io,
+                   void *workspace, size_t workspace_bytes, gla_stream_t stream) {
+    Sizes sz;
+    gla_status rc = validate_shape(B, T, H, Dk, Dv, io, &sz);
+    if (rc != GLA_OK) return rc;
+    if (!gla::gdn_supported(Dk, Dv)) return GLA_ERR_UNSUPPORTED_DIM;
+    const bool empty = (sz.nqk == 0);
+    if (!empty && (!q || !k || !v || !g_log || !beta || !o)) return GLA_ERR_NULL_ARG;
+    if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(g_log) || misaligned(beta) ||
+        misaligned(h0) || misaligned(o) || misaligned(hT))
+        return GLA_ERR_MISALIGNED;
+    const size_t es = io == GLA_IO_BF16 ? 2 : 4;
+    const size_t bqk = (size_t)sz.nqk * es, bv = (size_t)sz.nv * es;
+    const size_t bg = (size_t)(sz.nqk / Dk) * 4, bs = (size_t)sz.nstate * 4;
+    const void *ins[6] = {q, k, v, g_log, beta, h0};
+    const size_t nins[6] = {bqk, bqk, bv, bg, bg, bs};
+    for (int i = 0; i < 6; ++i) {
+        if (overlap(o, bv, ins[i], nins[i]) || overlap(hT, bs, ins[i], nins[i]))
+            return GLA_ERR_ALIAS;
+    }
+    if (overlap(o, bv, hT, bs)) return GLA_ERR_ALIAS;
+    const size_t need = empty ? 0 : gla::gdn_workspace_bytes(B, T, H, Dk, Dv);
+    if (workspace) {
+        if (misaligned(workspace) || workspace_bytes < need) return GLA_ERR_WORKSPACE;
+        for (int i = 0; i < 6; ++i)
+            if (overlap(workspace, need, ins[i], nins[i])) return GLA_ERR_WORKSPACE;
+        if (overlap(workspace, need, o, bv) || overlap(workspace, need, hT, bs))
+            return GLA_ERR_WORKSPACE;
+    }
+    DeviceState *st = nullptr;
+    rc = current_device(&st);
+    if (rc != GLA_OK) return rc;
+    if (empty) return GLA_OK;
+    void *ws = workspace;
+    if (!ws) {
+        rc = library_workspace(st, need, &ws);
+        if (rc != GLA_OK) return rc;
+    }
+    gla::GdnProblem p{q, k, v, g_log, beta, scale, h0, o, hT, B, T, H, Dk, Dv, io};
+    const cudaError_t e = gla::launch_gdn(p, ws, st->num_sms, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        set_detail("gated delta rule launch", e);
+        return GLA_ERR_LAUNCH;
+    }
+    return GLA_OK;
+}
+
 gla_status gla_last_device_status(gla_stream_t stream) {
     DeviceState *st = nullptr;
     gla_status rc = current_device(&st);

@@ -53,4 +53,19 @@ size_t tc_workspace_bytes(const Problem &p, int splits, int num_sms);
 cudaError_t launch_tc(const Problem &p, int splits, int num_sms, void *ws, size_t ws_bytes,
                       unsigned int *dev_err, cudaStream_t s);
 
+// Gated delta rule forward (fp32 CUDA cores): chunk-parallel prep, then the state scan.
+struct GdnProblem {
+    const void *q, *k, *v;   // [B,T,H,Dk] / [B,T,H,Dv], bf16 or fp32 (io)
+    const float *g, *beta;   // [B,T,H] log-gates and write strengths
+    float scale;
+    const float *h0;         // [B,H,Dk,Dv] or nullptr
+    void *o;                 // [B,T,H,Dv]
+    float *hT;               // [B,H,Dk,Dv] or nullptr
+    int64_t B, T, H, Dk, Dv;
+    int io;
+};
+bool gdn_supported(int64_t Dk, int64_t Dv);
+size_t gdn_workspace_bytes(int64_t B, int64_t T, int64_t H, int64_t Dk, int64_t Dv);
+cudaError_t launch_gdn(const GdnProblem &p, void *ws, int num_sms, cudaStream_t s);
+
 }  // namespace gla

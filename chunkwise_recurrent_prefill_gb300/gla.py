@@ -85,6 +85,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.gla_launch_counter.restype = ctypes.c_uint64
             lib.gla_version.argtypes = []
             lib.gla_version.restype = ctypes.c_int
+            lib.gdn_fwd.argtypes = [vp, vp, vp, vp, vp, f32, vp, vp, vp, i64, i64, i64, i64, i64,
+                                    ctypes.c_int, vp, ctypes.c_size_t, vp]
+            lib.gdn_fwd.restype = ctypes.c_int
+            lib.gdn_fwd_workspace_size.argtypes = [i64, i64, i64, i64, i64]
+            lib.gdn_fwd_workspace_size.restype = ctypes.c_size_t
             _lib = lib
     return _lib
 
@@ -286,6 +291,58 @@ def gla_step(q, k, v, g, scale: float, S, *, o=None, stream=None):
         detail = lib.gla_last_error_detail().decode() if rc == 6 else ""
         raise GLAError(rc, "gla_step", detail)
     return o
+
+
+def gdn_workspace_size(B: int, T: int, H: int, Dk: int, Dv: int) -> int:
+    """Bytes of device workspace ``gdn_fwd`` needs for this shape (0 if unsupported)."""
+    return int(load_library().gdn_fwd_workspace_size(B, T, H, Dk, Dv))
+
+
+def gdn_fwd(q, k, v, g, beta, scale: float, h0=None, *, o=None, hT=None,
+            return_state: bool = False, workspace: torch.Tensor | None = None, stream=None):
+    """Gated delta rule forward through ``gdn_fwd``.
+
+    q, k: [B,T,H,Dk]; v: [B,T,H,Dv] (all bf16, or all float32); g (log-gates) and beta
+    (write strengths): float32 [B,T,H]; h0: [B,H,Dk,Dv] float32 or None. ``workspace``: a
+    CUDA tensor of at least ``gdn_workspace_size`` bytes, or None for the library's own.
+    Returns (o, hT|None).
+    """
+    lib = load_library()
+    if q.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("q/k/v must be bfloat16 or float32")
+    B, T, H, Dk = q.shape
+    Dv = v.shape[-1]
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("tensors must be on a CUDA device")
+    _check(k, "k", q.dtype, (B, T, H, Dk), dev)
+    _check(v, "v", q.dtype, (B, T, H, Dv), dev)
+    _check(g, "g", torch.float32, (B, T, H), dev)
+    _check(beta, "beta", torch.float32, (B, T, H), dev)
+    if h0 is not None:
+        _check(h0, "h0", torch.float32, (B, H, Dk, Dv), dev)
+    if o is None:
+        o = torch.empty((B, T, H, Dv), dtype=q.dtype, device=dev)
+    else:
+        _check(o, "o", q.dtype, (B, T, H, Dv), dev)
+    if hT is None and return_state:
+        hT = torch.empty((B, H, Dk, Dv), dtype=torch.float32, device=dev)
+    elif hT is not None:
+        _check(hT, "hT", torch.float32, (B, H, Dk, Dv), dev)
+    ws, ws_bytes = None, 0
+    if workspace is not None:
+        if workspace.device != dev or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous tensor on the inputs' device")
+        ws, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+    io = IO_BF16 if q.dtype == torch.bfloat16 else IO_F32
+    with torch.cuda.device(dev):
+        rc = lib.gdn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), ctypes.c_float(scale),
+                         _ptr(h0), _ptr(o), _ptr(hT), B, T, H, Dk, Dv, io, ws, ws_bytes,
+                         _stream_handle(stream))
+    if rc != GLA_OK:
+        detail = lib.gla_last_error_detail().decode() if rc in (6, 9) else ""
+        raise GLAError(rc, "gdn_fwd", detail)
+    return o, hT
 
 
 def launch_counter() -> int:

@@ -218,6 +218,37 @@ gla_status gla_fwd_noalloc(const void *q, const void *k, const void *v, const fl
                            int64_t B, int64_t T, int64_t H, int64_t Dk, int64_t Dv,
                            int seq_splits, gla_stream_t stream);
 
+/*
+ * gdn_fwd — forward (prefill) pass of the gated delta rule, the gated-delta-network kind of
+ * linear attention the operator libraries on the pages target ("面向长序列大模型的线性注意力
+ * 算子性能评测方法与优化实践", section 三.3: a gate and an incremental update of the recurrent
+ * state; "线性注意力GPU算子库的定义与技术解析", section 三). The pages print no formula; this is
+ * the published gated delta rule, per batch b and head h:
+ *     S_0 = h0 (or 0)
+ *     S_t = exp(g_t) (I - beta_t k_t^T k_t) S_{t-1} + beta_t k_t^T v_t      (Dk x Dv, fp32)
+ *     o_t = scale . q_t . S_t,     hT = S_T
+ * with one log-gate g_t and one write strength beta_t per token and head (k_t a row vector).
+ * Layouts (contiguous, row-major): q, k [B, T, H, Dk]; v, o [B, T, H, Dv] in bf16
+ * (io = GLA_IO_BF16) or fp32 (io = GLA_IO_F32); g_log, beta [B, T, H] fp32; h0, hT
+ * [B, H, Dk, Dv] fp32, either may be NULL (zero initial state / final state not written).
+ * The keys are used as given; the recurrence is stable for beta_t |k_t|^2 <= 2, e.g. unit
+ * keys and beta in [0, 1].
+ * Dims: Dk a multiple of 4 in [4, 128], Dv a multiple of 16 in [16, 128]
+ * (GLA_ERR_UNSUPPORTED_DIM otherwise). Pointers are device pointers, 16-byte aligned
+ * (GLA_ERR_MISALIGNED); o and hT must not overlap an input or each other (GLA_ERR_ALIAS).
+ * Workspace: gdn_fwd_workspace_size() bytes of device memory, 16-byte aligned; pass NULL
+ * to use the library's per-device workspace (allocated on first need, grown when a larger
+ * problem arrives, shared with gla_fwd_ex: calls on different streams must not overlap).
+ * A caller workspace smaller than needed, misaligned, or overlapping an argument returns
+ * GLA_ERR_WORKSPACE. fp32 arithmetic on CUDA cores; deterministic (no atomics). Two
+ * kernels, stream-ordered on `stream`; no host synchronisation.
+ */
+size_t gdn_fwd_workspace_size(int64_t B, int64_t T, int64_t H, int64_t Dk, int64_t Dv);
+gla_status gdn_fwd(const void *q, const void *k, const void *v, const float *g_log,
+                   const float *beta, float scale, const float *h0, void *o, float *hT,
+                   int64_t B, int64_t T, int64_t H, int64_t Dk, int64_t Dv, int io,
+                   void *workspace, size_t workspace_bytes, gla_stream_t stream);
+
 /* Library ABI version: major * 10000 + minor * 100 + patch. */
 int gla_version(void);
 

@@ -23,13 +23,14 @@ def _declared_functions():
         if fn.endswith(".h"):
             src = open(os.path.join(ROOT, "include", fn)).read()
             src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-            names |= set(re.findall(r"\b(gla_[a-z0-9_]+)\s*\(", src))
+            names |= set(re.findall(r"\b((?:gla|gdn)_[a-z0-9_]+)\s*\(", src))
     return names
 
 
 def test_exports_every_declared_symbol(lib):
     declared = _declared_functions()
-    assert {"gla_fwd", "gla_fwd_f32", "gla_fwd_ex", "gla_last_device_status"} <= declared
+    assert {"gla_fwd", "gla_fwd_f32", "gla_fwd_ex", "gla_last_device_status", "gdn_fwd",
+            "gdn_fwd_workspace_size"} <= declared
     for name in declared:
         assert hasattr(lib, name), f"libgla.so does not export {name}"
 
@@ -141,3 +142,34 @@ def test_varlen_validation(lib):
     assert _varlen(lib, Dk=64, Dv=64, io=0) in (0, 3, 6, 8)   # valid shape: exact path or no GPU
     assert _varlen(lib, hT=0x1000000000) == 5            # hT over q
     assert _varlen(lib, o=0x7000000000 - 64) == 5        # o over the offsets
+
+
+def _gdn(lib, q=0x1000000000, k=0x2000000000, v=0x3000000000, g=0x4000000000,
+         beta=0x4800000000, h0=None, o=0x5000000000, hT=None, B=1, T=64, H=2, Dk=128, Dv=128,
+         io=0, ws=0x9000000000, ws_bytes=1 << 40):
+    p = lambda x: None if x is None else ctypes.c_void_p(x)  # noqa: E731
+    return lib.gdn_fwd(p(q), p(k), p(v), p(g), p(beta), ctypes.c_float(1.0), p(h0), p(o), p(hT),
+                       B, T, H, Dk, Dv, io, p(ws), ws_bytes, None)
+
+
+def test_gdn_validation(lib):
+    from chunkwise_recurrent_prefill_gb300.gla import load_library
+    load_library()   # sets the argument types
+    assert _gdn(lib, beta=None) == 1                    # GLA_ERR_NULL_ARG
+    assert _gdn(lib, o=None) == 1
+    assert _gdn(lib, T=-1) == 2                         # GLA_ERR_BAD_SHAPE
+    assert _gdn(lib, Dk=130) == 3                       # GLA_ERR_UNSUPPORTED_DIM
+    assert _gdn(lib, Dk=6) == 3                         # not a multiple of 4
+    assert _gdn(lib, Dv=24) == 3                        # not a multiple of 16
+    assert _gdn(lib, beta=0x4800000004) == 4            # GLA_ERR_MISALIGNED
+    assert _gdn(lib, o=0x4800000000) == 5               # o over beta: GLA_ERR_ALIAS
+    assert _gdn(lib, hT=0x3000000000) == 5              # hT over v
+    assert _gdn(lib, ws_bytes=16) == 9                  # workspace too small
+    assert _gdn(lib, ws=0x9000000008) == 9              # workspace misaligned
+    assert _gdn(lib, ws=0x3000000000) == 9              # workspace over v
+    assert _gdn(lib, io=3) == 10                        # GLA_ERR_BAD_OPTION
+    # the workspace size grows with the number of 64-token chunks and is 0 when unsupported
+    one = lib.gdn_fwd_workspace_size(1, 64, 1, 128, 128)
+    assert one > 0 and lib.gdn_fwd_workspace_size(2, 65, 3, 128, 128) == 2 * 2 * 3 * one
+    assert lib.gdn_fwd_workspace_size(1, 64, 1, 130, 128) == 0
+    assert lib.gdn_fwd_workspace_size(1, 0, 1, 128, 128) == 0
