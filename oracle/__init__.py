@@ -1,4 +1,4 @@
-"""Oracle for the GLA prefill forward pass — TEST INFRASTRUCTURE ONLY.
+"""Oracle for the GLA prefill forward pass and the gated delta rule — TEST INFRASTRUCTURE ONLY.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import, call, link or run anything in this package. The product
@@ -9,6 +9,9 @@ Contents:
   gla_oracle.c   fp64 token-by-token recurrence (plain C, OpenMP over heads).
   gla_ref.py     ctypes binding to it, an independent pure-numpy token loop, and an
                  fp64 numpy restatement of the chunkwise algorithm.
+  gdn_ref.py     the gated delta rule: fp64 numpy token loop and chunk algebra, pinned by
+                 ``tests/test_gdn_oracle_pins.py`` (its formula is a reading from outside the
+                 pages, which name the method but print no recurrence).
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 (brute-force decay-matrix attention, the ungated textbook case, closed forms,
