@@ -35,6 +35,7 @@ FLUSH_BYTES = 256 << 20
 KERNEL_SOURCES = {
     "tc": ["chunkwise_recurrent_prefill_gb300/csrc/gla_tc.cu"],
     "exact": ["chunkwise_recurrent_prefill_gb300/csrc/gla_exact.cu"],
+    "gdn": ["chunkwise_recurrent_prefill_gb300/csrc/gdn.cu"],
 }
 
 
@@ -612,7 +613,7 @@ def run_gdn(args, rank, world, dist):
                        "l2": "flushed by a 256 MiB device write before every timed step"},
             "clocks": clocks, "gpu_launches": launches,
             "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak, "traffic": None,
+                         "frac": achieved / peak, "traffic": committed_traffic("gdn", w.name),
                          "peak_source": f"derived: {peak_src}",
                          "algorithmic_flops_per_launch": flops,
                          "algorithmic_bytes_per_launch": nbytes,
