@@ -601,7 +601,7 @@ def run_gdn(args, rank, world, dist):
         cpu = gdn_cpu_oracle_sample(w, x_cpu, args.cpu_seconds)
     if rank == 0:
         print(json.dumps({
-            "metric": "gated delta rule prefill fwd tokens/s (B·T, H=16 D=128 bf16)",
+            "metric": GDN_METRIC,
             "value": weak_scaling_value(w.B * w.T, args.steps, world, total_s),
             "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * per, "ms_p50": ms[len(ms) // 2],
@@ -621,6 +621,53 @@ def run_gdn(args, rank, world, dist):
                          "kernel": "gdn_prep + gdn_scan (one call)"},
             "e2e": None, "cpu_baseline": cpu,
         }), flush=True)
+
+
+GDN_METRIC = "gated delta rule prefill fwd tokens/s (B·T, H=16 D=128 bf16)"
+
+
+def run_reference_gdn(args, rank, world):
+    """--impl reference --op gdn: the fp64 numpy token loop of the gated delta rule, each
+    step a bounded sample (the first T_s tokens of every (batch, head) pair), rank 0 only."""
+    if rank != 0:
+        return
+    from oracle import gdn_ref
+    from chunkwise_recurrent_prefill_gb300.workloads import (GDN_BENCH_WORKLOAD, GDN_WORKLOADS,
+                                                             make_gdn_inputs)
+    w = GDN_WORKLOADS[args.workload or GDN_BENCH_WORKLOAD]
+    x = make_gdn_inputs(w)
+    cut = lambda t, n: None if t is None else t[:, :n]   # noqa: E731
+    args_ = lambda n: [cut(x[k_], n) for k_ in ("q", "k", "v", "g", "beta")]   # noqa: E731
+    cal = min(w.T, 64)
+    t0 = time.perf_counter()
+    gdn_ref.recurrent(*args_(cal), x["scale"], x["h0"])
+    rate = w.B * cal / max(time.perf_counter() - t0, 1e-6)
+    per_step_s = 150.0 / max(1, args.steps + args.warmup)
+    T_s = int(min(w.T, max(1, per_step_s * rate / w.B)))
+    sl = args_(T_s)
+    for _ in range(args.warmup):
+        gdn_ref.recurrent(*sl, x["scale"], x["h0"])
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        gdn_ref.recurrent(*sl, x["scale"], x["h0"])
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = args.steps * w.B * T_s / total
+    sample = (f"each step: first {T_s} of {w.T} tokens of all {w.B}x{w.H} (batch, head) pairs, "
+              f"fp64 numpy token loop on one host core")
+    print(json.dumps({
+        "impl": "reference", "metric": GDN_METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "Dk": w.Dk, "Dv": w.Dv,
+                   "io": w.io, "path": "oracle", "l2": "n/a (host CPU)"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
 
 
 def gdn_cpu_oracle_sample(w, x_cpu, target_s: float):
@@ -649,7 +696,10 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
-        run_reference(args, w or WORKLOADS[BENCH_WORKLOAD], rank, world)
+        if args.op == "gdn":
+            run_reference_gdn(args, rank, world)
+        else:
+            run_reference(args, w or WORKLOADS[BENCH_WORKLOAD], rank, world)
         return
     import torch
     dist = None
