@@ -410,7 +410,20 @@ gla_status gdn_fwd(const void *q, const void *k, const void *v, const float *g_l
     DeviceState *st = nullptr;
     rc = current_device(&st);
     if (rc != GLA_OK) return rc;
-    if (empty) return GLA_OK;
+    if (empty) {
+        // no tokens: the final state is the initial one (zero without h0)
+        if (T == 0 && B * H > 0 && hT) {
+            cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+            const cudaError_t e = h0 ? cudaMemcpyAsync(hT, h0, bs, cudaMemcpyDeviceToDevice, s)
+                                     : cudaMemsetAsync(hT, 0, bs, s);
+            if (e != cudaSuccess) {
+                cudaGetLastError();
+                set_detail("gated delta rule: final state of an empty sequence", e);
+                return GLA_ERR_LAUNCH;
+            }
+        }
+        return GLA_OK;
+    }
     void *ws = workspace;
     if (!ws) {
         rc = library_workspace(st, need, &ws);

@@ -241,7 +241,8 @@ gla_status gla_fwd_noalloc(const void *q, const void *k, const void *v, const fl
  * problem arrives, shared with gla_fwd_ex: calls on different streams must not overlap).
  * A caller workspace smaller than needed, misaligned, or overlapping an argument returns
  * GLA_ERR_WORKSPACE. fp32 arithmetic on CUDA cores; deterministic (no atomics). Two
- * kernels, stream-ordered on `stream`; no host synchronisation.
+ * kernels, stream-ordered on `stream`; no host synchronisation. T = 0 writes hT = h0 (or
+ * zero) and launches nothing.
  */
 size_t gdn_fwd_workspace_size(int64_t B, int64_t T, int64_t H, int64_t Dk, int64_t Dv);
 gla_status gdn_fwd(const void *q, const void *k, const void *v, const float *g_log,

@@ -136,6 +136,16 @@ def test_empty_and_no_state():
     x = _inputs(1, 0, 2, "bf16", seed=1)
     o, hT = gdn_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"])
     assert o.shape == (1, 0, 2, 128) and hT is None
+    # no tokens: hT is the initial state (zero without one)
+    x = _inputs(2, 0, 3, "f32", seed=4, h0=True)
+    o, hT = gdn_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], x["h0"],
+                    return_state=True)
+    torch.cuda.synchronize()
+    assert o.shape == (2, 0, 3, 128) and torch.equal(hT, x["h0"])
+    hT = torch.full((2, 3, 128, 128), 7.0, device=DEV)
+    gdn_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], None, hT=hT)
+    torch.cuda.synchronize()
+    assert not hT.any()
     x = _inputs(1, 96, 2, "bf16", seed=2)
     o, hT = _run(x, want_state=False)
     assert hT is None
