@@ -11,11 +11,13 @@
 // (I + A) W = diag(beta exp(b)) K and A_jm = beta_j exp(b_j - b_m) k_j.k_m for m < j. Then
 //     O   = scale (diag(exp(b)) Q S0 + P U),   P_ij = exp(b_i - b_j) q_i.k_j for j <= i
 //     S1  = exp(b_63) S0 + Kh^T U,             Kh_j = exp(b_63 - b_j) k_j.
-// Everything that does not depend on S0 (A, the triangular solves, P, the decay factors) is
-// computed for all chunks at once by gdn_prep_kernel and written to a workspace; the state
-// then runs through the chunks in gdn_scan_kernel, one CTA per (batch, head, block of state
-// columns): the columns of S are independent under this recurrence (the transition acts on
-// the key axis only), which is what lets B = 1 spread over many SMs.
+// Substituting U, O = Oi + G S0 with Oi = scale P Ut and G = scale (diag(exp(b)) Q - P W).
+// Everything that does not depend on S0 (A, the triangular solves, P, G, Oi, the decay
+// factors) is computed for all chunks at once by gdn_prep_kernel and written to a workspace;
+// the state then runs through the chunks in gdn_scan_kernel, one CTA per (batch, head, block
+// of state columns), which forms U and O from S0 in one pass and then S1: the columns of S
+// are independent under this recurrence (the transition acts on the key axis only), which is
+// what lets B = 1 spread over many SMs.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
