@@ -168,3 +168,22 @@ def test_readback_property_on_gpu():
     torch.cuda.synchronize()
     err = (o - v).abs().max().item() / v.abs().max().item()
     assert err < 1e-4, err
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_degenerate_gates(io):
+    """Full forgetting (g = -1e4: every in-chunk decay underflows to 0, and the masked
+    exponentials above the diagonal overflow, which must never reach a product) and no
+    writes (beta = 0: the state only decays), against the oracle."""
+    x = _inputs(1, 200, 2, io, seed=31, h0=True)
+    xf = {**x, "g": torch.full_like(x["g"], -1e4)}
+    o, hT = _run(xf)
+    assert torch.isfinite(o.float()).all() and torch.isfinite(hT).all()
+    o_ref, h_ref = _oracle(xf)
+    assert_close(o.float().cpu().numpy(), o_ref, io, "o (g = -1e4)")
+    assert_close(hT.cpu().numpy(), h_ref, io, "hT (g = -1e4)")
+    xb = {**x, "beta": torch.zeros_like(x["beta"])}
+    o, hT = _run(xb)
+    o_ref, h_ref = _oracle(xb)
+    assert_close(o.float().cpu().numpy(), o_ref, io, "o (beta = 0)")
+    assert_close(hT.cpu().numpy(), h_ref, io, "hT (beta = 0)")
