@@ -1,5 +1,6 @@
 /*
- * gla.h — C ABI of libgla.so, the GB300 (sm_103a) gated-linear-attention prefill forward.
+ * gla.h — C ABI of libgla.so, the GB300 (sm_103a) gated-linear-attention prefill forward
+ * (and the gated delta rule forward, gdn_fwd, declared at the end).
  *
  * What every entry point computes, per batch b and head h independently
  * ("Linear Attention 在 GPU 上到底慢在哪", section 学长的反馈: the state update
