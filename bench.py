@@ -631,31 +631,33 @@ def run_reference_gdn(args, rank, world):
     step a bounded sample (the first T_s tokens of every (batch, head) pair), rank 0 only."""
     if rank != 0:
         return
+    import oracle
     from oracle import gdn_ref
     from chunkwise_recurrent_prefill_gb300.workloads import (GDN_BENCH_WORKLOAD, GDN_WORKLOADS,
                                                              make_gdn_inputs)
+    oracle.build()
     w = GDN_WORKLOADS[args.workload or GDN_BENCH_WORKLOAD]
     x = make_gdn_inputs(w)
-    cut = lambda t, n: None if t is None else t[:, :n]   # noqa: E731
+    cut = lambda t, n: None if t is None else t[:, :n].contiguous()   # noqa: E731
     args_ = lambda n: [cut(x[k_], n) for k_ in ("q", "k", "v", "g", "beta")]   # noqa: E731
-    cal = min(w.T, 64)
+    cal = min(w.T, 256)
     t0 = time.perf_counter()
-    gdn_ref.recurrent(*args_(cal), x["scale"], x["h0"])
+    gdn_ref.recurrent_c(*args_(cal), x["scale"], x["h0"])
     rate = w.B * cal / max(time.perf_counter() - t0, 1e-6)
     per_step_s = 150.0 / max(1, args.steps + args.warmup)
     T_s = int(min(w.T, max(1, per_step_s * rate / w.B)))
     sl = args_(T_s)
     for _ in range(args.warmup):
-        gdn_ref.recurrent(*sl, x["scale"], x["h0"])
+        gdn_ref.recurrent_c(*sl, x["scale"], x["h0"])
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        gdn_ref.recurrent(*sl, x["scale"], x["h0"])
+        gdn_ref.recurrent_c(*sl, x["scale"], x["h0"])
         times.append(time.perf_counter() - t0)
     total = sum(times)
     value = args.steps * w.B * T_s / total
     sample = (f"each step: first {T_s} of {w.T} tokens of all {w.B}x{w.H} (batch, head) pairs, "
-              f"fp64 numpy token loop on one host core")
+              f"fp64 C token loop on the host cores")
     print(json.dumps({
         "impl": "reference", "metric": GDN_METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -663,30 +665,34 @@ def run_reference_gdn(args, rank, world):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "Dk": w.Dk, "Dv": w.Dv,
                    "io": w.io, "path": "oracle", "l2": "n/a (host CPU)"},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }), flush=True)
 
 
 def gdn_cpu_oracle_sample(w, x_cpu, target_s: float):
-    """The fp64 numpy token loop of the gated delta rule on the first T_s tokens of every
-    (batch, head) pair, T_s sized for about target_s of host time."""
+    """The fp64 C token loop of the gated delta rule (OpenMP over the (batch, head) pairs) on
+    the first T_s tokens of every pair, T_s sized for about target_s of host time."""
+    import oracle
     from oracle import gdn_ref
-    cut = lambda t, n: None if t is None else t[:, :n]   # noqa: E731
+    oracle.build()
+    cut = lambda t, n: None if t is None else t[:, :n].contiguous()   # noqa: E731
     args_ = lambda n: [cut(x_cpu[k_], n) for k_ in ("q", "k", "v", "g", "beta")]   # noqa: E731
-    cal = min(w.T, 64)
+    cal = min(w.T, 256)
     t0 = time.perf_counter()
-    gdn_ref.recurrent(*args_(cal), x_cpu["scale"], x_cpu["h0"])
+    gdn_ref.recurrent_c(*args_(cal), x_cpu["scale"], x_cpu["h0"])
     rate = w.B * cal / max(time.perf_counter() - t0, 1e-6)
     T_s = int(min(w.T, max(64, target_s * rate / w.B)))
+    sl = args_(T_s)
     t0 = time.perf_counter()
-    gdn_ref.recurrent(*args_(T_s), x_cpu["scale"], x_cpu["h0"])
+    gdn_ref.recurrent_c(*sl, x_cpu["scale"], x_cpu["h0"])
     dt = time.perf_counter() - t0
-    return {"value": w.B * T_s / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+    return {"value": w.B * T_s / dt, "unit": "tokens/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
             "sample": f"first {T_s} of {w.T} tokens of all {w.B}x{w.H} (batch, head) pairs, "
-                      f"fp64 numpy token loop (single-threaded einsum), {dt:.2f} s"}
+                      f"fp64 C token loop, {dt:.2f} s"}
 
 
 def main():

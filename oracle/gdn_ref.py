@@ -24,7 +24,9 @@ Functions:
 
 * ``recurrent`` — the token loop above, literally (fp64, numpy, vectorised over batch
   and heads).
-* ``recurrent_head`` — the same loop for one (batch, head), for sampled checks at full
+* ``recurrent_c`` — the same token loop written independently in C (``gdn_oracle.c``,
+  OpenMP over the (batch, head) pairs), for the CPU baselines and large checks.
+* ``recurrent_head`` — the numpy loop for one (batch, head), for sampled checks at full
   size.
 * ``chunkwise`` — the chunk algebra the GPU path uses, in fp64: per chunk a unit lower
   triangular solve turns the delta writes into "new values" U, and the chunk's outputs
@@ -39,7 +41,44 @@ above; within that reading no function here is unpinned.
 """
 from __future__ import annotations
 
+import ctypes
+import os
+import subprocess
+import threading
+
 import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gdn_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_build", "libgdn_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``gdn_oracle.c`` into ``oracle/_build/libgdn_oracle.so`` with gcc (OpenMP)."""
+    os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
+    stale = (not os.path.exists(_LIB_PATH)
+             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+    if force or stale:
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-o", tmp, _SRC, "-lm"],
+                       check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            i64, p = ctypes.c_int64, ctypes.c_void_p
+            lib.gdn_oracle_batch.argtypes = [p, p, p, p, p, ctypes.c_double, p, p, p,
+                                             i64, i64, i64, i64, i64]
+            lib.gdn_oracle_batch.restype = ctypes.c_int
+            _lib = lib
+    return _lib
 
 
 def _f64(x):
@@ -69,6 +108,34 @@ def recurrent(q, k, v, g, beta, scale: float, h0=None):
         S = a * (S - bt * kt[..., :, None] * kS[..., None, :]) + bt * kt[..., :, None] * vt[..., None, :]
         o[:, t] = scale * np.einsum("bhd,bhde->bhe", q[:, t], S)
     return o, S
+
+
+def _c32(x):
+    """Contiguous float32 copy (exact for bf16 inputs), or None."""
+    if x is None:
+        return None
+    if hasattr(x, "detach"):
+        x = x.detach().to("cpu").float().contiguous().numpy()
+    return np.ascontiguousarray(x, dtype=np.float32)
+
+
+def recurrent_c(q, k, v, g, beta, scale: float, h0=None):
+    """The token loop in C (fp64, OpenMP over (batch, head)). Returns (o, hT) as float64."""
+    q, k, v, g, beta, h0 = (_c32(x) for x in (q, k, v, g, beta, h0))
+    B, T, H, Dk = q.shape
+    Dv = v.shape[-1]
+    assert k.shape == q.shape and v.shape == (B, T, H, Dv)
+    assert g.shape == (B, T, H) and beta.shape == (B, T, H)
+    if h0 is not None:
+        assert h0.shape == (B, H, Dk, Dv)
+    o = np.empty((B, T, H, Dv), dtype=np.float64)
+    hT = np.empty((B, H, Dk, Dv), dtype=np.float64)
+    ptr = lambda a: None if a is None else a.ctypes.data_as(ctypes.c_void_p)   # noqa: E731
+    rc = _load().gdn_oracle_batch(ptr(q), ptr(k), ptr(v), ptr(g), ptr(beta), float(scale),
+                                  ptr(h0), ptr(o), ptr(hT), B, T, H, Dk, Dv)
+    if rc != 0:
+        raise MemoryError("oracle scratch allocation failed")
+    return o, hT
 
 
 def recurrent_head(q, k, v, g, beta, scale: float, h0, b: int, h: int, t_end: int | None = None):

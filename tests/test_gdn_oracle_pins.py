@@ -1,8 +1,9 @@
 """Pins for the gated-delta-rule oracle (CPU only).
 
-Both oracle functions (the token loop and the fp64 chunk algebra at several chunk
-sizes, ragged tails included) must pass every check in ``tests/gdn_pins.py``; copies of
-the token loop with a planted mistake must each fail at least one.
+Every oracle function (the numpy token loop, the C token loop, and the fp64 chunk algebra
+at several chunk sizes, ragged tails included) must pass every check in
+``tests/gdn_pins.py``; copies of the token loop with a planted mistake must each fail at
+least one.
 """
 import numpy as np
 import pytest
@@ -15,6 +16,7 @@ def _impls():
     from oracle import gdn_ref
     return {
         "recurrent": gdn_ref.recurrent,
+        "c_recurrent": gdn_ref.recurrent_c,
         "chunk_C1": lambda *a: gdn_ref.chunkwise(*a, C=1),
         "chunk_C4": lambda *a: gdn_ref.chunkwise(*a, C=4),
         "chunk_C5": lambda *a: gdn_ref.chunkwise(*a, C=5),
@@ -23,7 +25,8 @@ def _impls():
 
 
 @pytest.mark.parametrize("check", sorted(gdn_pins.ALL_CHECKS))
-@pytest.mark.parametrize("impl", ["recurrent", "chunk_C1", "chunk_C4", "chunk_C5", "chunk_C64"])
+@pytest.mark.parametrize("impl", ["recurrent", "c_recurrent", "chunk_C1", "chunk_C4", "chunk_C5",
+                                  "chunk_C64"])
 def test_pin(impl, check):
     fn = _impls()[impl]
     rng = np.random.default_rng(4321)
@@ -106,3 +109,19 @@ def test_head_entry_matches_batch():
             assert np.array_equal(oh, o[b, :, h]) and np.array_equal(hh, hT[b, h])
             oh, _ = gdn_ref.recurrent_head(q, k, v, g, beta, 0.4, h0, b, h, t_end=9)
             assert np.allclose(oh, o[b, :9, h], rtol=0, atol=0)
+
+
+def test_c_and_numpy_loops_agree():
+    """The C token loop and the numpy one, written independently, agree to fp64 rounding on
+    the workload distributions (D = 128, ragged T, h0) and on the pins' small cases."""
+    from oracle import gdn_ref
+    from chunkwise_recurrent_prefill_gb300.workloads import make_gdn_inputs, small
+    x = make_gdn_inputs(small("t", B=2, T=77, H=3, io="bf16", seed=12, with_h0=True))
+    o1, h1 = gdn_ref.recurrent(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], x["h0"])
+    o2, h2 = gdn_ref.recurrent_c(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], x["h0"])
+    assert rel(o2, o1) < 1e-13 and rel(h2, h1) < 1e-13
+    q, k, v, g, beta, _ = gdn_pins.rand_case(np.random.default_rng(8), B=1, T=30, H=2, Dk=7, Dv=5,
+                                             with_h0=False)
+    o1, h1 = gdn_ref.recurrent(q, k, v, g, beta, 0.9)
+    o2, h2 = gdn_ref.recurrent_c(q, k, v, g, beta, 0.9)
+    assert rel(o2, o1) < 1e-13 and rel(h2, h1) < 1e-13
