@@ -16,13 +16,25 @@ constexpr int kMaxDevices = 64;
 // Error word raised by kernels (bounded waits that ran out); one per device.
 __device__ unsigned int g_dev_err;
 
+// A workspace the library keeps for one stream of one device.
+struct StreamWorkspace {
+    cudaStream_t stream = nullptr;
+    void *ptr = nullptr;
+    size_t bytes = 0;
+    uint64_t last_use = 0;
+};
+
+// At most this many streams per device keep a library workspace; the least recently used
+// one is freed (cudaFree synchronises the device, so nothing still uses it) to make room.
+constexpr int kMaxStreamWorkspaces = 16;
+
 struct DeviceState {
-    bool probed = false;
+    std::atomic<bool> probed{false};
     bool sm103 = false;
     int num_sms = 0;
     unsigned int *err_word = nullptr;
-    void *ws = nullptr;
-    size_t ws_bytes = 0;
+    StreamWorkspace ws[kMaxStreamWorkspaces];
+    uint64_t ws_clock = 0;
 };
 
 std::mutex g_mu;
@@ -32,9 +44,11 @@ void set_detail(const char *where, cudaError_t e) {
     snprintf(g_detail, sizeof(g_detail), "%s: %s (%d)", where, cudaGetErrorString(e), (int)e);
 }
 std::atomic<uint64_t> g_launches{0};
+std::atomic<uint64_t> g_ws_allocs{0};
 DeviceState g_dev[kMaxDevices];
 
-// Probe the current device once: architecture, SM count, error word address.
+// Probe the current device once (under the library lock): architecture, SM count, error
+// word address.
 gla_status current_device(DeviceState **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -42,25 +56,28 @@ gla_status current_device(DeviceState **out) {
         return GLA_ERR_LAUNCH;
     }
     DeviceState &st = g_dev[dev];
-    if (!st.probed) {
-        int major = 0, minor = 0, sms = 0;
-        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-            cudaGetLastError();
-            return GLA_ERR_LAUNCH;
-        }
-        st.sm103 = (major == 10 && minor == 3);
-        st.num_sms = sms;
-        if (st.sm103) {
-            void *p = nullptr;
-            if (cudaGetSymbolAddress(&p, g_dev_err) != cudaSuccess) {
+    if (!st.probed.load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (!st.probed.load(std::memory_order_relaxed)) {
+            int major = 0, minor = 0, sms = 0;
+            if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
                 cudaGetLastError();
                 return GLA_ERR_LAUNCH;
             }
-            st.err_word = static_cast<unsigned int *>(p);
+            st.sm103 = (major == 10 && minor == 3);
+            st.num_sms = sms;
+            if (st.sm103) {
+                void *p = nullptr;
+                if (cudaGetSymbolAddress(&p, g_dev_err) != cudaSuccess) {
+                    cudaGetLastError();
+                    return GLA_ERR_LAUNCH;
+                }
+                st.err_word = static_cast<unsigned int *>(p);
+            }
+            st.probed.store(true, std::memory_order_release);
         }
-        st.probed = true;
     }
     *out = &st;
     return st.sm103 ? GLA_OK : GLA_ERR_UNSUPPORTED_DEVICE;
@@ -124,26 +141,51 @@ gla_status validate(const void *q, const void *k, const void *v, const float *g,
     return GLA_OK;
 }
 
-// The library-owned workspace of the current device, grown on demand.
-gla_status library_workspace(DeviceState *st, size_t need, void **out) {
+// The library-owned workspace of `stream` on the current device. Each stream has its own, so
+// calls on different streams never share scratch; a stream's buffer is allocated on its first
+// call that needs one and replaced only when a call needs more (sizes are rounded up to a power
+// of two), so repeated calls allocate nothing.
+gla_status library_workspace(DeviceState *st, cudaStream_t stream, size_t need, void **out) {
     std::lock_guard<std::mutex> lock(g_mu);
-    if (st->ws_bytes < need) {
-        if (st->ws) {
-            cudaFree(st->ws);  // synchronises the device: no call still uses the old one
-            st->ws = nullptr;
-            st->ws_bytes = 0;
+    StreamWorkspace *slot = nullptr;
+    for (auto &w : st->ws)
+        if (w.ptr && w.stream == stream) slot = &w;
+    if (!slot) {
+        for (auto &w : st->ws)
+            if (!w.ptr) { slot = &w; break; }
+        if (!slot) {   // every slot taken: reuse the least recently used one
+            slot = &st->ws[0];
+            for (auto &w : st->ws)
+                if (w.last_use < slot->last_use) slot = &w;
         }
+        if (slot->stream != stream && slot->ptr) {
+            cudaFree(slot->ptr);   // synchronises the device: no call still uses it
+            slot->ptr = nullptr;
+            slot->bytes = 0;
+        }
+        slot->stream = stream;
+    }
+    if (slot->bytes < need) {
+        if (slot->ptr) {
+            cudaFree(slot->ptr);   // synchronises the device: no call still uses it
+            slot->ptr = nullptr;
+            slot->bytes = 0;
+        }
+        size_t bytes = 1 << 20;
+        while (bytes < need) bytes <<= 1;
         void *p = nullptr;
-        const cudaError_t e = cudaMalloc(&p, need);
+        const cudaError_t e = cudaMalloc(&p, bytes);
         if (e != cudaSuccess) {
             cudaGetLastError();
             set_detail("workspace cudaMalloc", e);
             return GLA_ERR_WORKSPACE;
         }
-        st->ws = p;
-        st->ws_bytes = need;
+        g_ws_allocs.fetch_add(1, std::memory_order_relaxed);
+        slot->ptr = p;
+        slot->bytes = bytes;
     }
-    *out = st->ws;
+    slot->last_use = ++st->ws_clock;
+    *out = slot->ptr;
     return GLA_OK;
 }
 
@@ -161,6 +203,17 @@ int resolve_path(const gla_options *opt, const gla::Problem &p) {
 
 namespace gla {
 void count_launches(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+int current_device_status() {
+    DeviceState *st = nullptr;
+    return (int)current_device(&st);
+}
+int tc_auto_splits_for(int64_t B, int64_t T, int64_t H) {
+    DeviceState *st = nullptr;
+    const int sms = current_device(&st) == GLA_OK ? st->num_sms : 152;
+    Problem p{};
+    p.B = B; p.T = T; p.H = H; p.Dk = 128; p.Dv = 128;
+    return tc_auto_splits(p, sms);
+}
 void set_error_detail(const char *text) { snprintf(g_detail, sizeof(g_detail), "%s", text); }
 }  // namespace gla
 
@@ -169,6 +222,8 @@ extern "C" {
 const char *gla_last_error_detail(void) { return g_detail; }
 
 uint64_t gla_launch_counter(void) { return g_launches.load(std::memory_order_relaxed); }
+
+uint64_t gla_workspace_allocations(void) { return g_ws_allocs.load(std::memory_order_relaxed); }
 
 int gla_version(void) { return 100; }
 
@@ -253,7 +308,7 @@ gla_status gla_fwd_ex(const void *q, const void *k, const void *v, const float *
                 if (opt->workspace_bytes < need) return GLA_ERR_WORKSPACE;
                 ws = opt->workspace;
             } else {
-                rc = library_workspace(st, need, &ws);
+                rc = library_workspace(st, reinterpret_cast<cudaStream_t>(stream), need, &ws);
                 if (rc != GLA_OK) return rc;
             }
         }
@@ -426,7 +481,7 @@ gla_status gdn_fwd(const void *q, const void *k, const void *v, const float *g_l
     }
     void *ws = workspace;
     if (!ws) {
-        rc = library_workspace(st, need, &ws);
+        rc = library_workspace(st, reinterpret_cast<cudaStream_t>(stream), need, &ws);
         if (rc != GLA_OK) return rc;
     }
     gla::GdnProblem p{q, k, v, g_log, beta, scale, h0, o, hT, B, T, H, Dk, Dv, io};

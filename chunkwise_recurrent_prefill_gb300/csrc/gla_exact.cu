@@ -45,7 +45,8 @@ __global__ void __launch_bounds__(kThreads)
 gla_exact_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO *__restrict__ v,
                  const float *__restrict__ g, float scale, const float *__restrict__ h0,
                  IO *__restrict__ o, float *__restrict__ hT, int64_t T, int64_t H,
-                 int gate_scalar, const int *__restrict__ cu, unsigned *__restrict__ err) {
+                 int gate_scalar, const int *__restrict__ cu, int seq_filter,
+                 unsigned *__restrict__ err) {
     constexpr int KS = DK + 1;
     extern __shared__ float sm[];
     float *qs = sm;                 // [C][KS]  q, later q * exp(b)
@@ -68,6 +69,10 @@ gla_exact_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO *_
         r0 = bad ? 0 : s0;
         Tb = bad ? 0 : s1 - s0;
         if (bad) return;   // uniform across the block: nothing is written
+        // sequences another launch of the call handles (uniform across the block)
+        if ((seq_filter == kShortOnly && Tb >= kShortSeq) ||
+            (seq_filter == kLongOnly && Tb < kShortSeq))
+            return;
     }
 
     for (int i = tid; i < DK * kVB; i += kThreads) {
@@ -161,7 +166,7 @@ cudaError_t launch_typed(const Problem &p, unsigned *err, cudaStream_t s) {
     kern<<<grid, kThreads, smem, s>>>(static_cast<const IO *>(p.q), static_cast<const IO *>(p.k),
                                       static_cast<const IO *>(p.v), p.g, p.scale, p.h0,
                                       static_cast<IO *>(p.o), p.hT, p.T, p.H, p.gate, p.cu,
-                                      err);
+                                      p.seq_filter, err);
     e = cudaGetLastError();
     if (e == cudaSuccess) count_launches(1);
     return e;

@@ -20,7 +20,16 @@ struct Problem {
     int gate;                // GLA_GATE_KEY: g [B,T,H,Dk]; GLA_GATE_SCALAR: g [B,T,H]
     const int *cu;           // packed sequences: B sequences at offsets cu[0..B] along a
                              // single batch of T tokens (device), or null
+    int seq_filter;          // packed sequences only: 0 = every sequence; kShortOnly = only
+                             // those shorter than one 64-token chunk; kLongOnly = only the others
 };
+
+// Packed-sequence filters (Problem::seq_filter): the tensor-core path runs the sequences of at
+// least one chunk, and the exact kernel the shorter ones, whose few bf16-rounded products
+// nothing averages.
+constexpr int kShortOnly = 1;
+constexpr int kLongOnly = 2;
+constexpr int kShortSeq = 64;
 
 // Bits of the device error word kernels may raise (never trap).
 enum : unsigned int {
@@ -28,6 +37,10 @@ enum : unsigned int {
     kDevErrInternal = 2u,    // an input the host could not check was inconsistent (packed-
                              // sequence offsets not non-decreasing from 0 to T)
 };
+
+// Status (a gla_status value) of the current device: GLA_OK for an sm_103 device, else the
+// error gla_fwd_ex would return; probes the device once.
+int current_device_status();
 
 // Host-side count of kernel launches issued by the library (gla_launch_counter).
 void count_launches(unsigned n);
@@ -48,6 +61,9 @@ cudaError_t launch_step(const void *q, const void *k, const void *v, const float
 // tcgen05 path (bf16 io, Dk and Dv in {64, 128}).
 bool tc_supported(const Problem &p);
 int tc_auto_splits(const Problem &p, int num_sms);
+// tc_auto_splits of a bf16 problem of this shape on the current device (152 SMs if it cannot
+// be queried).
+int tc_auto_splits_for(int64_t B, int64_t T, int64_t H);
 int tc_state_pieces(const Problem &p, int splits, int num_sms);
 size_t tc_workspace_bytes(const Problem &p, int splits, int num_sms);
 cudaError_t launch_tc(const Problem &p, int splits, int num_sms, void *ws, size_t ws_bytes,

@@ -70,17 +70,20 @@ extern "C" gla_status gla_fwd_noalloc(const void *q, const void *k, const void *
             gla::set_error_detail(msg);
             return GLA_ERR_WORKSPACE;
         }
-        // automatic split: the largest split count whose scratch fits (scratch grows with it)
-        int s = 1;
-        for (int c = 2; c <= 64; ++c) {
-            opt.seq_splits = c;
-            if (gla_fwd_workspace_size(B, T, H, Dk, Dv, GLA_IO_BF16, &opt) > cap) break;
-            s = c;
+        // automatic split: from the count gla_fwd would pick, down to the largest whose scratch
+        // fits (one segment needs none)
+        int s = gla::tc_auto_splits_for(B, T, H);
+        for (; s > 1; --s) {
+            opt.seq_splits = s;
+            if (gla_fwd_workspace_size(B, T, H, Dk, Dv, GLA_IO_BF16, &opt) <= cap) break;
         }
-        opt.seq_splits = s;
+        opt.seq_splits = s < 1 ? 1 : s;
         need = gla_fwd_workspace_size(B, T, H, Dk, Dv, GLA_IO_BF16, &opt);
     }
     if (need > 0) {
+        // an unsupported device is reported as gla_fwd_ex would, before the symbol lookup
+        const int dev_rc = gla::current_device_status();
+        if (dev_rc != GLA_OK) return (gla_status)dev_rc;
         const gla_status rc = scratch_address(&opt.workspace);
         if (rc != GLA_OK) return rc;
         opt.workspace_bytes = cap;

@@ -39,7 +39,9 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdlib>
+#include <mutex>
 
 #include "gla_internal.h"
 #include "tc_ptx.cuh"
@@ -108,16 +110,13 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
 // TMEM column map of the output kernel (512 columns).
 constexpr uint32_t kColS = 0;      // S~^T fp32, 128 columns
 constexpr uint32_t kColSB = 128;   // S~^T bf16 snapshot (A operand), 2 x 64 columns
-constexpr uint32_t kColP1 = 256;   // P over key dims 0..63 (M=64 layout), 64 columns
-constexpr uint32_t kColP2 = 320;   // P over key dims 64..127, 64 columns
-constexpr uint32_t kColOi = 384;   // O^T intra term, 64 columns
-constexpr uint32_t kColOs = 448;   // O^T inter term, 64 columns
+constexpr uint32_t kColP = 256;    // P (M=64 layout), 64 columns
+constexpr uint32_t kColO = 320;    // O^T = S~^T Q'^T + V^T P^T, 64 columns
 
 // Shared-memory map of the output kernel (bytes from a 1024-aligned base).
 //   q/k/v ring (3 stages): raw tiles as 128B-swizzled [64 x 64] bf16 boxes, two per tile;
-//     the gate warps rewrite q -> Q' and k -> K' (or K^ in an extreme chunk) in place, and
-//     once O(c) has been read the epilogue stages the chunk's bf16 output in its dead Q'
-//     tile, so the stage is released only after that store has read it.
+//     the gate warps rewrite q -> Q' and k -> K' (or K^ in an extreme chunk) in place; the
+//     stage is released once the chunk's O MMAs (its last readers) have completed.
 //   g ring (2 slots): the chunk's log-gates, [64 tokens][128] f32, loaded by TMA and
 //     released as soon as the gate warps have scaled the chunk.
 namespace om {
@@ -176,6 +175,7 @@ struct OutArgs {
     __nv_bfloat16 *o;                  // output (rows a TMA store may not cover)
     int Dk, Dv;                        // head dims of the caller's tensors (64 or 128); the
                                        // kernels work at 128, padding with zeros
+    int long_only;                     // packed sequences: skip those shorter than one chunk
 };
 
 struct StateArgs {
@@ -296,7 +296,7 @@ template <bool kScalar, bool kPacked>
 __global__ void __launch_bounds__(kOutThreads, 1)
 gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg,
-                  const __grid_constant__ CUtensorMap to, const OutArgs a) {
+                  const OutArgs a) {
     using namespace om;
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = align1024(smraw);
@@ -322,6 +322,9 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         tbase = bad_seq ? 0 : s0;
         tend = bad_seq ? 0 : s1;
         bmap = 0;
+        // a sequence shorter than one chunk is left to the exact kernel of the same call
+        // (uniform across the CTA, before any barrier or allocation)
+        if (a.long_only && !bad_seq && tend - tbase < kC) return;
     }
     int cb, ce;
     if (kPacked) {
@@ -364,7 +367,6 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         tma_prefetch_desc(&tk);
         tma_prefetch_desc(&tv);
         tma_prefetch_desc(&tg);
-        tma_prefetch_desc(&to);
     }
     if (warp == 1) tmem_alloc(tslot, 512);
     tc_fence_before();
@@ -448,7 +450,9 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         //   O(c): P tile of c written, O(c-1) read  -> Oi = V^T P^T (4), Os = S~^T Q'^T (8)
         // MMAs that accumulate into TMEM run at their latency, one after another, so the
         // order only decides who waits: U first (the state chain), then P, then O.
-        if (lane == 0) {
+        // The whole warp runs the loop converged: every lane polls, lane 0's view of each
+        // barrier decides (broadcast), and one elected lane issues the MMAs and commits.
+        {
             const uint32_t idP = idesc_bf16(64, 64, 0, 0);
             const uint32_t idU = idesc_bf16(128, 128, 1, 1);
             const uint32_t idOi = idesc_bf16(128, 64, 1, 0);
@@ -458,52 +462,66 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             uint64_t t_idle = 0;
             while (no < n) {
                 bool prog = false;
-                if (nu < np && mbar_test(&bars[SREADY], par(nu))) {
+                const bool rU = __shfl_sync(0xffffffffu, nu < np && mbar_test(&bars[SREADY], par(nu)), 0);
+                if (rU) {
                     tc_fence_after();
-                    TRACE_OUT(5, nu);
+                    if (lane == 0) TRACE_OUT(5, nu);
                     const uint32_t base = smem_u32(sm + (nu % NQ) * QSTAGE);
+                    if (elect_one()) {
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_ss(tm + kColS, smem_desc(base + V + kk * 2048, 8192, 1024),
-                               smem_desc(base + K + kk * 2048, 8192, 1024), idU, 1);
-                    mma_commit(&bars[UDONE]);
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_ss(tm + kColS, smem_desc(base + V + kk * 2048, 8192, 1024),
+                                   smem_desc(base + K + kk * 2048, 8192, 1024), idU, 1);
+                        mma_commit(&bars[UDONE]);
+                    }
+                    __syncwarp();
                     ++nu;
                     prog = true;
                 }
-                if (np < n && mbar_test(&bars[GDONE + np % NQ], par(np / NQ)) &&
-                    (np == 0 || mbar_test(&bars[PFREE], par(np - 1)))) {
+                const bool rP = __shfl_sync(
+                    0xffffffffu, np < n && mbar_test(&bars[GDONE + np % NQ], par(np / NQ)) &&
+                                     (np == 0 || mbar_test(&bars[PFREE], par(np - 1))), 0);
+                if (rP) {
                     tc_fence_after();
-                    TRACE_OUT(3, np);
+                    if (lane == 0) TRACE_OUT(3, np);
                     const uint32_t base = smem_u32(sm + (np % NQ) * QSTAGE);
+                    if (elect_one()) {
 #pragma unroll
-                    for (int x = 0; x < 8; ++x) {
-                        const int half = x & 1, kk = x >> 1;   // the two P tiles alternate
-                        const uint32_t off = half * 8192 + kk * 32;
-                        mma_ss(tm + (half ? kColP2 : kColP1), smem_desc(base + Q + off, 16, 1024),
-                               smem_desc(base + K + off, 16, 1024), idP, kk > 0);
+                        for (int x = 0; x < 8; ++x) {   // key dims 16x .. 16x + 15
+                            const uint32_t off = (x >> 2) * 8192 + (x & 3) * 32;
+                            mma_ss(tm + kColP, smem_desc(base + Q + off, 16, 1024),
+                                   smem_desc(base + K + off, 16, 1024), idP, x > 0);
+                        }
+                        mma_commit(&bars[PFULL]);
                     }
-                    mma_commit(&bars[PFULL]);
-                    TRACE_OUT(4, np);
+                    __syncwarp();
+                    if (lane == 0) TRACE_OUT(4, np);
                     ++np;
                     prog = true;
                 }
-                if (no < nu && mbar_test(&bars[PBF], par(no)) &&
-                    (no == 0 || mbar_test(&bars[OFREE], par(no - 1)))) {
+                const bool rO = __shfl_sync(
+                    0xffffffffu, no < nu && mbar_test(&bars[PBF], par(no)) &&
+                                     (no == 0 || mbar_test(&bars[OFREE], par(no - 1))), 0);
+                if (rO) {
                     tc_fence_after();
-                    TRACE_OUT(6, no);
+                    if (lane == 0) TRACE_OUT(6, no);
                     const uint32_t base = smem_u32(sm + (no % NQ) * QSTAGE);
                     const uint32_t pbase = smem_u32(sm + P);
+                    if (elect_one()) {
+                        // one accumulator: the inter term S~^T Q'^T, then the intra term V^T P^T
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        mma_ts(tm + kColOs, tm + kColSB + (no & 1) * 64 + kk * 8,
-                               smem_desc(base + Q + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
-                               idOs, kk > 0);
-                        if (kk < 4)
-                            mma_ss(tm + kColOi, smem_desc(base + V + kk * 2048, 8192, 1024),
-                                   smem_desc(pbase + kk * 32, 16, 1024), idOi, kk > 0);
+                        for (int kk = 0; kk < 8; ++kk)
+                            mma_ts(tm + kColO, tm + kColSB + (no & 1) * 64 + kk * 8,
+                                   smem_desc(base + Q + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
+                                   idOs, kk > 0);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_ss(tm + kColO, smem_desc(base + V + kk * 2048, 8192, 1024),
+                                   smem_desc(pbase + kk * 32, 16, 1024), idOi, 1);
+                        mma_commit(&bars[OFULL]);   // U(no) and P(no) were issued before O(no)
                     }
-                    mma_commit(&bars[OFULL]);   // U(no) and P(no) were issued before O(no)
-                    TRACE_OUT(7, no);
+                    __syncwarp();
+                    if (lane == 0) TRACE_OUT(7, no);
                     ++no;
                     prog = true;
                 }
@@ -514,101 +532,58 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     __nanosleep(kIssuerNapNs);
                     if (++idle == 256) {
                         t_idle = global_ns();   // the timer is read only on long idle streaks
-                    } else if ((idle & 1023) == 0 && global_ns() - t_idle > kWaitLimitNs) {
+                    } else if ((idle & 1023) == 0 &&
+                               __shfl_sync(0xffffffffu, global_ns() - t_idle > kWaitLimitNs, 0)) {
                         ok = false;
                         break;
                     }
                 }
             }
             // all issued MMAs complete before the CTA tears down its TMEM
-            mma_commit(&bars[FIN]);
+            if (elect_one()) mma_commit(&bars[FIN]);
+            __syncwarp();
             if (!mbar_wait(&bars[FIN], 0)) ok = false;
         }
         __syncwarp();
     } else if (warp >= 2 && warp < 6) {
         // ------------------------------------------------------------ epilogue
+        // O^T(c) from TMEM (lane = value column v, column = token), rounded to bf16 and
+        // stored straight to global memory: a warp writes 64 contiguous bytes of a token row
+        // per store. Once O(c) has completed, every MMA of chunk c has (they complete in issue
+        // order), so its q/k/v stage is released right away.
         const int j = warp & 3;
         const int et = (warp - 2) * 32 + lane;      // 0..127
         const int v = j * 32 + lane;                // O^T lane = value column
-        const uint32_t vbox = (uint32_t)(v >> 6) * 8192;
-        const uint32_t vcol = (uint32_t)(v & 63);
+        const uint64_t pol = l2_policy_evict_first();
+        const int64_t rs = (int64_t)a.H * a.Dv;     // row stride of o (elements)
         for (int c = 0; c < n; ++c) {
             const bool w = mbar_wait(&bars[OFULL], par(c));
             if (named_bar_or(2, 128, !w)) { ok = false; break; }
             if (et == 0) TRACE_OUT(12, c);
             tc_fence_after();
-            float o0[32], o1[32];
-            {
-                uint32_t r0[16], r1[16], r2[16], r3[16];
-                tmem_ld16(tmem_addr(tm, j, kColOi), r0);
-                tmem_ld16(tmem_addr(tm, j, kColOi + 16), r1);
-                tmem_ld16(tmem_addr(tm, j, kColOs), r2);
-                tmem_ld16(tmem_addr(tm, j, kColOs + 16), r3);
-                tmem_wait_ld();
-                reg_fence(r0); reg_fence(r1); reg_fence(r2); reg_fence(r3);
-#pragma unroll
-                for (int x = 0; x < 16; ++x) {
-                    o0[x] = __uint_as_float(r0[x]) + __uint_as_float(r2[x]);
-                    o0[16 + x] = __uint_as_float(r1[x]) + __uint_as_float(r3[x]);
-                }
-                tmem_ld16(tmem_addr(tm, j, kColOi + 32), r0);
-                tmem_ld16(tmem_addr(tm, j, kColOi + 48), r1);
-                tmem_ld16(tmem_addr(tm, j, kColOs + 32), r2);
-                tmem_ld16(tmem_addr(tm, j, kColOs + 48), r3);
-                tmem_wait_ld();
-                reg_fence(r0); reg_fence(r1); reg_fence(r2); reg_fence(r3);
-#pragma unroll
-                for (int x = 0; x < 16; ++x) {
-                    o1[x] = __uint_as_float(r0[x]) + __uint_as_float(r2[x]);
-                    o1[16 + x] = __uint_as_float(r1[x]) + __uint_as_float(r3[x]);
-                }
-            }
+            if (et == 0) mbar_arrive(&bars[QEMPTY + c % NQ]);   // the stage may be refilled
+            float ov[64];
+            tmem_ld64(tmem_addr(tm, j, kColO), ov);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[OFREE]);
-            // stage O (bf16, 128B-swizzled boxes) in the chunk's Q' tile: every MMA of the
-            // chunk has completed, so nothing reads that tile any more
-            uint8_t *ost = sm + (c % NQ) * QSTAGE + Q + vbox;
+            const int64_t t0 = tbase + (int64_t)(cb + c) * kC;
+            const int64_t left = tend - t0;
+            const int vr = left < kC ? (int)left : kC;   // rows of the sequence
+            if (v < a.Dv) {
+                __nv_bfloat16 *op = a.o + ((((int64_t)bmap * a.T + t0) * a.H + h) * a.Dv) + v;
+                if (vr == kC) {
 #pragma unroll
-            for (int x = 0; x < 32; ++x) {
-                *reinterpret_cast<__nv_bfloat16 *>(ost + sw128_offset(x, vcol)) =
-                    __float2bfloat16_rn(o0[x]);   // the output scale is folded into the Q tile
-                *reinterpret_cast<__nv_bfloat16 *>(ost + sw128_offset(32 + x, vcol)) =
-                    __float2bfloat16_rn(o1[x]);
-            }
-            fence_proxy_async_smem();
-            named_bar_sync(2, 128);
-            const int vr = kPacked ? valid_rows(c) : kC;
-            if (kPacked && vr < kC) {
-                // the last chunk of a packed sequence: the rows past its end belong to the next
-                // one, so only the valid rows are written, from registers
-                const int64_t t0 = tbase + (int64_t)(cb + c) * kC;
-                __nv_bfloat16 *op = a.o + (t0 * a.H + h) * a.Dv + v;
-                const int64_t rs = (int64_t)a.H * a.Dv;   // row stride of o
-                if (v < a.Dv) {
+                    for (int x = 0; x < kC; ++x)
+                        st_global_bf16_hint(op + x * rs, __float2bfloat16_rn(ov[x]), pol);
+                } else {
 #pragma unroll
-                    for (int x = 0; x < 32; ++x)
-                        if (x < vr) op[x * rs] = __float2bfloat16_rn(o0[x]);
-#pragma unroll
-                    for (int x = 0; x < 32; ++x)
-                        if (32 + x < vr) op[(32 + x) * rs] = __float2bfloat16_rn(o1[x]);
+                    for (int x = 0; x < kC; ++x)
+                        if (x < vr) st_global_bf16_hint(op + x * rs, __float2bfloat16_rn(ov[x]), pol);
                 }
-                named_bar_sync(2, 128);
-                if (et == 0) mbar_arrive(&bars[QEMPTY + c % NQ]);
-            } else if (et == 0) {
-                const int t0 = (int)(tbase + (cb + c) * kC);
-                uint8_t *qt = sm + (c % NQ) * QSTAGE + Q;
-                const uint64_t pol = l2_policy_evict_first();
-                tma_store_4d_hint(&to, qt, 0, h, t0, bmap, pol);
-                if (a.Dv > 64)   // no store is issued past the caller's last value column
-                    tma_store_4d_hint(&to, qt + 8192, 64, h, t0, bmap, pol);
-                bulk_commit();
-                bulk_wait_read_all();
-                mbar_arrive(&bars[QEMPTY + c % NQ]);   // the stage may be refilled
-                TRACE_OUT(13, c);
             }
+            if (et == 0) TRACE_OUT(13, c);
         }
-        if (et == 0) bulk_wait_all();
         __syncwarp();
     } else if (warp >= 6 && warp < 10) {
         // ------------------------------------------------------------ state + P conversion
@@ -695,18 +670,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             float prow[64];
             const int i = 16 * j + lane;        // P row held by this lane (lane < 16)
             if (!ext) {
-                uint32_t r0[16], r1[16];
-#pragma unroll
-                for (int c0 = 0; c0 < 64; c0 += 16) {
-                    tmem_ld16(tmem_addr(tm, j, kColP1 + c0), r0);
-                    tmem_ld16(tmem_addr(tm, j, kColP2 + c0), r1);
-                    tmem_wait_ld();
-                    reg_fence(r0);
-                    reg_fence(r1);
-#pragma unroll
-                    for (int x = 0; x < 16; ++x)
-                        prow[c0 + x] = __uint_as_float(r0[x]) + __uint_as_float(r1[x]);
-                }
+                tmem_ld64(tmem_addr(tm, j, kColP), prow);
             } else {
                 // exact route: P_ij = scale sum_d q_id k_jd exp(b_id - b_jd), j <= i
 #pragma unroll
@@ -844,21 +808,29 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 }
                 return *reinterpret_cast<const float2 *>(grow + t * kD);
             };
+            // Pass 1: the running log2-gate sums of the thread's tokens, kept in registers for
+            // pass 2 (the g slot is read once and released right after).
             float r0 = 0.f, r1 = 0.f;
             float lo0 = 0.f, hi0 = 0.f, lo1 = 0.f, hi1 = 0.f;   // range of the running sums
-#pragma unroll 1
-            for (int t0 = 0; t0 < tl; t0 += kGateBlock) {
-                float2 gv[kGateBlock];
+            float2 rsum[kGatePart];
 #pragma unroll
-                for (int x = 0; x < kGateBlock; ++x) gv[x] = gpair(t0 + x);
+            for (int t0 = 0; t0 < kGatePart; t0 += kGateBlock) {
+                if (t0 < tl) {
+                    float2 gv[kGateBlock];
 #pragma unroll
-                for (int x = 0; x < kGateBlock; ++x) {
-                    r0 = fmaf(gv[x].x, kLog2e, r0);
-                    r1 = fmaf(gv[x].y, kLog2e, r1);
-                    lo0 = fminf(lo0, r0); hi0 = fmaxf(hi0, r0);
-                    lo1 = fminf(lo1, r1); hi1 = fmaxf(hi1, r1);
+                    for (int x = 0; x < kGateBlock; ++x) gv[x] = gpair(t0 + x);
+#pragma unroll
+                    for (int x = 0; x < kGateBlock; ++x) {
+                        r0 = fmaf(gv[x].x, kLog2e, r0);
+                        r1 = kScalar ? r0 : fmaf(gv[x].y, kLog2e, r1);
+                        rsum[t0 + x] = make_float2(r0, r1);
+                        lo0 = fminf(lo0, r0); hi0 = fmaxf(hi0, r0);
+                        lo1 = fminf(lo1, r1); hi1 = fmaxf(hi1, r1);
+                    }
                 }
             }
+            __syncwarp();
+            if (!kScalar && lane == 0) mbar_arrive(&bars[GEMPTY + gs]);   // the g slot may be refilled
             *reinterpret_cast<float2 *>(xch + part * kD + d) = make_float2(r0, r1);
             named_bar_sync(1, kGateThreads);
             // b = off + (running sum within the range), with off the left-to-right sum of the
@@ -902,81 +874,75 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 for (int t = max(vr - tb, 0); t < tl; ++t)
                     *reinterpret_cast<uint32_t *>(kt + sw128_offset((uint32_t)(tb + t), col)) = 0u;
             }
-            r0 = 0.f;
-            r1 = 0.f;
-            // blocks of kGateBlock tokens: all loads of a block are issued before its stores, so a
-            // block costs one shared-memory round trip
+            // Pass 2, in blocks of kGateBlock tokens: all loads of a block are issued before
+            // its stores, so a block costs one shared-memory round trip.
             if (!ext) {
                 // Q' = scale q 2^(b + L), K' = k 2^-(b + L) with b = off + r: the per-chunk
                 // constants (offset, L, log2 scale) are folded into two exponent biases
                 const float eq0 = off0 + Lq0 + lsc, eq1 = off1 + Lq1 + lsc;
                 const float ek0 = -(off0 + Lq0), ek1 = -(off1 + Lq1);
-#pragma unroll 1
-                for (int t0 = 0; t0 < tl; t0 += kGateBlock) {
-                    float2 gv[kGateBlock];
-                    uint32_t qv[kGateBlock], kv[kGateBlock];
 #pragma unroll
-                    for (int x = 0; x < kGateBlock; ++x) {
-                        const uint32_t off = (uint32_t)(tb + t0) * 128u + swz[x];
-                        gv[x] = gpair(t0 + x);
-                        qv[x] = *reinterpret_cast<const uint32_t *>(qt + off);
-                        kv[x] = *reinterpret_cast<const uint32_t *>(kt + off);
-                    }
+                for (int t0 = 0; t0 < kGatePart; t0 += kGateBlock) {
+                    if (t0 < tl) {
+                        uint32_t qv[kGateBlock], kv[kGateBlock];
 #pragma unroll
-                    for (int x = 0; x < kGateBlock; ++x) {
-                        const float2 qf = unpack_bf16(qv[x]), kf = unpack_bf16(kv[x]);
-                        r0 = fmaf(gv[x].x, kLog2e, r0);
-                        if (kScalar) {
-                            // one gate for every key dimension: both columns share the factors
-                            const float fq = ex2(r0 + eq0), fk = ex2(ek0 - r0);
-                            qv[x] = pack_bf16(qf.x * fq, qf.y * fq);
-                            kv[x] = pack_bf16(kf.x * fk, kf.y * fk);
-                        } else {
-                            r1 = fmaf(gv[x].y, kLog2e, r1);
-                            qv[x] = pack_bf16(qf.x * ex2(r0 + eq0), qf.y * ex2(r1 + eq1));
-                            kv[x] = pack_bf16(kf.x * ex2(ek0 - r0), kf.y * ex2(ek1 - r1));
+                        for (int x = 0; x < kGateBlock; ++x) {
+                            const uint32_t off = (uint32_t)(tb + t0) * 128u + swz[x];
+                            qv[x] = *reinterpret_cast<const uint32_t *>(qt + off);
+                            kv[x] = *reinterpret_cast<const uint32_t *>(kt + off);
                         }
-                    }
 #pragma unroll
-                    for (int x = 0; x < kGateBlock; ++x) {
-                        const uint32_t off = (uint32_t)(tb + t0) * 128u + swz[x];
-                        *reinterpret_cast<uint32_t *>(qt + off) = qv[x];
-                        *reinterpret_cast<uint32_t *>(kt + off) = kv[x];
+                        for (int x = 0; x < kGateBlock; ++x) {
+                            const float2 qf = unpack_bf16(qv[x]), kf = unpack_bf16(kv[x]);
+                            const float2 r = rsum[t0 + x];
+                            if (kScalar) {
+                                // one gate for every key dimension: both columns share the factors
+                                const float fq = ex2(r.x + eq0), fk = ex2(ek0 - r.x);
+                                qv[x] = pack_bf16(qf.x * fq, qf.y * fq);
+                                kv[x] = pack_bf16(kf.x * fk, kf.y * fk);
+                            } else {
+                                qv[x] = pack_bf16(qf.x * ex2(r.x + eq0), qf.y * ex2(r.y + eq1));
+                                kv[x] = pack_bf16(kf.x * ex2(ek0 - r.x), kf.y * ex2(ek1 - r.y));
+                            }
+                        }
+#pragma unroll
+                        for (int x = 0; x < kGateBlock; ++x) {
+                            const uint32_t off = (uint32_t)(tb + t0) * 128u + swz[x];
+                            *reinterpret_cast<uint32_t *>(qt + off) = qv[x];
+                            *reinterpret_cast<uint32_t *>(kt + off) = kv[x];
+                        }
                     }
                 }
             } else {
                 // extreme chunk: K^ = k 2^(Bc - b) with b = off + r formed exactly as the chunk
                 // total was, so that the last token's factor is exactly 1
-#pragma unroll 1
-                for (int t0 = 0; t0 < tl; t0 += kGateBlock) {
-                    float2 gv[kGateBlock];
-                    uint32_t qv[kGateBlock], kv[kGateBlock];
 #pragma unroll
-                    for (int x = 0; x < kGateBlock; ++x) {
-                        const uint32_t off = (uint32_t)(tb + t0) * 128u + swz[x];
-                        gv[x] = gpair(t0 + x);
-                        qv[x] = *reinterpret_cast<const uint32_t *>(qt + off);
-                        kv[x] = *reinterpret_cast<const uint32_t *>(kt + off);
-                    }
+                for (int t0 = 0; t0 < kGatePart; t0 += kGateBlock) {
+                    if (t0 < tl) {
+                        uint32_t qv[kGateBlock], kv[kGateBlock];
 #pragma unroll
-                    for (int x = 0; x < kGateBlock; ++x) {
-                        r0 = fmaf(gv[x].x, kLog2e, r0);
-                        r1 = fmaf(gv[x].y, kLog2e, r1);
-                        const float b0 = off0 + r0, b1 = off1 + r1;
-                        const float2 qf = unpack_bf16(qv[x]), kf = unpack_bf16(kv[x]);
-                        qv[x] = pack_bf16(sc * qf.x * ex2(b0), sc * qf.y * ex2(b1));
-                        kv[x] = pack_bf16(kf.x * ex2(B0 - b0), kf.y * ex2(B1 - b1));
-                    }
+                        for (int x = 0; x < kGateBlock; ++x) {
+                            const uint32_t off = (uint32_t)(tb + t0) * 128u + swz[x];
+                            qv[x] = *reinterpret_cast<const uint32_t *>(qt + off);
+                            kv[x] = *reinterpret_cast<const uint32_t *>(kt + off);
+                        }
 #pragma unroll
-                    for (int x = 0; x < kGateBlock; ++x) {
-                        const uint32_t off = (uint32_t)(tb + t0) * 128u + swz[x];
-                        *reinterpret_cast<uint32_t *>(qt + off) = qv[x];
-                        *reinterpret_cast<uint32_t *>(kt + off) = kv[x];
+                        for (int x = 0; x < kGateBlock; ++x) {
+                            const float2 r = rsum[t0 + x];
+                            const float b0 = off0 + r.x, b1 = off1 + r.y;
+                            const float2 qf = unpack_bf16(qv[x]), kf = unpack_bf16(kv[x]);
+                            qv[x] = pack_bf16(sc * qf.x * ex2(b0), sc * qf.y * ex2(b1));
+                            kv[x] = pack_bf16(kf.x * ex2(B0 - b0), kf.y * ex2(B1 - b1));
+                        }
+#pragma unroll
+                        for (int x = 0; x < kGateBlock; ++x) {
+                            const uint32_t off = (uint32_t)(tb + t0) * 128u + swz[x];
+                            *reinterpret_cast<uint32_t *>(qt + off) = qv[x];
+                            *reinterpret_cast<uint32_t *>(kt + off) = kv[x];
+                        }
                     }
                 }
             }
-            __syncwarp();
-            if (!kScalar && lane == 0) mbar_arrive(&bars[GEMPTY + gs]);   // the g slot may be refilled
             if (gt == 0) xf[slot] = (ext ? 1u : 0u) | (ren ? 2u : 0u);
             fence_proxy_async_smem();
             __syncwarp();
@@ -1307,10 +1273,19 @@ gla_tc_scan_kernel(const float *__restrict__ E, const float *__restrict__ gam,
     }
 }
 
-bool g_attr_done = false;
+// Opt-in shared-memory sizes are a per-device setting of each kernel: set once per device,
+// under a lock (several host threads may make their first call at the same time).
+constexpr int kMaxDevices = 64;
+std::mutex g_attr_mu;
+bool g_attr_done[kMaxDevices];
 
 cudaError_t set_attrs() {
-    if (g_attr_done) return cudaSuccess;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_attr_mu);
+    if (g_attr_done[dev]) return cudaSuccess;
     const void *outs[4] = {(const void *)gla_tc_out_kernel<false, false>,
                            (const void *)gla_tc_out_kernel<true, false>,
                            (const void *)gla_tc_out_kernel<false, true>,
@@ -1318,8 +1293,7 @@ cudaError_t set_attrs() {
     const void *states[2] = {(const void *)gla_tc_state_kernel<false>,
                              (const void *)gla_tc_state_kernel<true>};
     for (int i = 0; i < 4; ++i) {
-        cudaError_t e = cudaFuncSetAttribute(outs[i], cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             om::ALLOC);
+        e = cudaFuncSetAttribute(outs[i], cudaFuncAttributeMaxDynamicSharedMemorySize, om::ALLOC);
         if (e != cudaSuccess) return e;
         if (i < 2) {
             e = cudaFuncSetAttribute(states[i], cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1327,8 +1301,27 @@ cudaError_t set_attrs() {
             if (e != cudaSuccess) return e;
         }
     }
-    g_attr_done = true;
+    g_attr_done[dev] = true;
     return cudaSuccess;
+}
+
+// Test hook of the bounded waits. The environment is read once per process: with
+// GLA_TEST_STALL_ONE_LOAD set, the first tensor-core launch of the process skips the q/k/v
+// load of one chunk in every output CTA (later launches run normally), so its waits run out
+// and the call reports GLA_ERR_DEVICE_TIMEOUT with the context intact.
+std::atomic<int> g_stall_left{-1};   // -1: environment not read yet
+
+bool take_stall_hook() {
+    int left = g_stall_left.load(std::memory_order_relaxed);
+    if (left < 0) {
+        int init = std::getenv("GLA_TEST_STALL_ONE_LOAD") ? 1 : 0, expect = -1;
+        g_stall_left.compare_exchange_strong(expect, init);
+        left = g_stall_left.load(std::memory_order_relaxed);
+    }
+    while (left > 0) {
+        if (g_stall_left.compare_exchange_weak(left, left - 1)) return true;
+    }
+    return false;
 }
 
 int clamp_splits(const Problem &p, int splits) {
@@ -1382,13 +1375,16 @@ size_t tc_workspace_bytes(const Problem &p, int splits, int num_sms) {
 
 cudaError_t launch_tc(const Problem &p, int splits, int num_sms, void *ws, size_t ws_bytes,
                       unsigned int *dev_err, cudaStream_t stream) {
-    if (p.T == 0) return launch_exact(p, dev_err, stream);   // only hT = h0 to write
+    // Fewer tokens than one chunk (for packed sequences: in all of them together): the exact
+    // kernel (each output is a handful of products of bf16-rounded decayed operands here,
+    // with nothing to average their rounding). T = 0 only writes hT = h0.
+    if (p.T < kC) return launch_exact(p, dev_err, stream);
     const int s = p.cu ? 1 : clamp_splits(p, splits);   // packed sequences are not split
     const int64_t mB = p.cu ? 1 : p.B;                   // batch extent of the tensor maps
     const bool scalar = p.gate == 1;
     cudaError_t e = set_attrs();
     if (e != cudaSuccess) return e;
-    CUtensorMap mq, mk, mv, mg, mo;
+    CUtensorMap mq, mk, mv, mg;
     if (!make_bthd_map(&mq, p.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, mB, p.T, p.H, p.Dk, 64, kC,
                        CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_bthd_map(&mk, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, mB, p.T, p.H, p.Dk, 64, kC,
@@ -1399,9 +1395,7 @@ cudaError_t launch_tc(const Problem &p, int splits, int num_sms, void *ws, size_
         !(scalar ? make_bthd_map(&mg, p.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, mB, p.T, p.H,
                                  p.Dk, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B)
                  : make_bthd_map(&mg, p.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, mB, p.T, p.H,
-                                 p.Dk, kD, kC, CU_TENSOR_MAP_SWIZZLE_NONE)) ||
-        !make_bthd_map(&mo, p.o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, mB, p.T, p.H, p.Dv, 64, kC,
-                       CU_TENSOR_MAP_SWIZZLE_128B))
+                                 p.Dk, kD, kC, CU_TENSOR_MAP_SWIZZLE_NONE)))
         return cudaErrorInvalidResourceHandle;   // a tensor map could not be encoded
     const int nchunks = (int)((p.T + kC - 1) / kC);
     const int bh = (int)(p.B * p.H);
@@ -1449,14 +1443,12 @@ cudaError_t launch_tc(const Problem &p, int splits, int num_sms, void *ws, size_
         if (e != cudaSuccess) return e;
         count_launches(2);
     }
-    // Test hook for the bounded waits: with GLA_TEST_STALL_ONE_LOAD set, every output CTA
-    // skips the q/k/v load of one chunk, so the waits for it run out and the call reports
-    // GLA_ERR_DEVICE_TIMEOUT (after ~2 s per wait) with the context intact.
-    const int stall = (std::getenv("GLA_TEST_STALL_ONE_LOAD") && !p.cu)
-                          ? std::min(1, nchunks / s - 1) : -1;
+    // test hook of the bounded waits (see take_stall_hook): one chunk's load is never issued
+    const int stall = (!p.cu && take_stall_hook()) ? std::min(1, nchunks / s - 1) : -1;
     OutArgs oa{static_cast<const __nv_bfloat16 *>(p.q), static_cast<const __nv_bfloat16 *>(p.k),
                p.g, p.h0, p.hT, sstart, p.T, (int)p.H, nchunks, s, p.scale, dev_err, stall,
-               last16, p.cu, static_cast<__nv_bfloat16 *>(p.o), (int)p.Dk, (int)p.Dv};
+               last16, p.cu, static_cast<__nv_bfloat16 *>(p.o), (int)p.Dk, (int)p.Dv,
+               p.cu ? 1 : 0};
     if (s > 1) {
         cudaLaunchAttribute pdl[1];
         pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1469,16 +1461,22 @@ cudaError_t launch_tc(const Problem &p, int splits, int num_sms, void *ws, size_
         cfg.attrs = pdl;
         cfg.numAttrs = 1;
         e = scalar
-                ? cudaLaunchKernelEx(&cfg, gla_tc_out_kernel<true, false>, mq, mk, mv, mg, mo, oa)
-                : cudaLaunchKernelEx(&cfg, gla_tc_out_kernel<false, false>, mq, mk, mv, mg, mo, oa);
+                ? cudaLaunchKernelEx(&cfg, gla_tc_out_kernel<true, false>, mq, mk, mv, mg, oa)
+                : cudaLaunchKernelEx(&cfg, gla_tc_out_kernel<false, false>, mq, mk, mv, mg, oa);
     } else {
         auto kern = p.cu ? (scalar ? gla_tc_out_kernel<true, true> : gla_tc_out_kernel<false, true>)
                          : (scalar ? gla_tc_out_kernel<true, false> : gla_tc_out_kernel<false, false>);
-        kern<<<bh * s, kOutThreads, om::ALLOC, stream>>>(mq, mk, mv, mg, mo, oa);
+        kern<<<bh * s, kOutThreads, om::ALLOC, stream>>>(mq, mk, mv, mg, oa);
         e = cudaGetLastError();
     }
     if (e != cudaSuccess) return e;
     count_launches(1);
+    if (p.cu) {
+        // packed sequences shorter than one chunk: the exact kernel, on the same stream
+        Problem ps = p;
+        ps.seq_filter = kShortOnly;
+        return launch_exact(ps, dev_err, stream);
+    }
     return cudaSuccess;
 }
 

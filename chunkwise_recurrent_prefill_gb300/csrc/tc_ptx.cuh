@@ -89,6 +89,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     }
 }
 
+// One lane of a converged warp (the same lane every time the full warp calls it): the
+// issuer of tcgen05 MMAs and commits. A tcgen05.mma issued from a converged warp through
+// elect.sync is accepted at about twice the rate of one issued by a lone lane on a diverged
+// path (about 34 vs 64 SM cycles for an M=64, N=64, K=16 bf16 MMA on GB300).
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 // ---------------------------------------------------------------- fences / barriers
 // Make this thread's generic-proxy shared-memory writes visible to the async proxy
 // (tensor core operand reads, TMA).
@@ -196,6 +208,14 @@ __device__ __forceinline__ void tma_store_4d_hint(const void *tmap, const void *
         " [%0, {%2, %3, %4, %5}], [%1], %6;" ::"l"(reinterpret_cast<uint64_t>(tmap)),
         "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(pol)
         : "memory");
+}
+
+// 2-byte global store with an L2 cache policy.
+__device__ __forceinline__ void st_global_bf16_hint(__nv_bfloat16 *p, __nv_bfloat16 x,
+                                                    uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.b16 [%0], %1, %2;" ::"l"(p),
+                 "h"(*reinterpret_cast<const unsigned short *>(&x)), "l"(pol)
+                 : "memory");
 }
 
 __device__ __forceinline__ void bulk_commit() {

@@ -83,6 +83,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.gla_last_error_detail.restype = ctypes.c_char_p
             lib.gla_launch_counter.argtypes = []
             lib.gla_launch_counter.restype = ctypes.c_uint64
+            lib.gla_workspace_allocations.argtypes = []
+            lib.gla_workspace_allocations.restype = ctypes.c_uint64
             lib.gla_version.argtypes = []
             lib.gla_version.restype = ctypes.c_int
             lib.gdn_fwd.argtypes = [vp, vp, vp, vp, vp, f32, vp, vp, vp, i64, i64, i64, i64, i64,
@@ -348,6 +350,11 @@ def gdn_fwd(q, k, v, g, beta, scale: float, h0=None, *, o=None, hT=None,
 def launch_counter() -> int:
     """Kernel launches the library has issued in this process."""
     return int(load_library().gla_launch_counter())
+
+
+def workspace_allocations() -> int:
+    """Device allocations the library has made for its per-stream workspaces so far."""
+    return int(load_library().gla_workspace_allocations())
 
 
 def last_device_status(stream=None) -> int:

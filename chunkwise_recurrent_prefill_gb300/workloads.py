@@ -139,7 +139,9 @@ def make_gdn_inputs(w: Workload, device: str | torch.device = "cpu") -> dict:
 
 # Decode-step workload: one token for each of B sequences and H heads on a resident state
 # (the step after prefill). Same recipe: q, k, v, u, then the state S = 0.02 * N(0, 1).
-STEP_WORKLOAD = dict(name="decode_B64_H16_D128", B=64, H=16, D=128, io="bf16", seed=5)
+# B = 256 makes the state (268 MB) larger than the 129 MB L2, so a step's state write-back
+# cannot stay in L2 past the step.
+STEP_WORKLOAD = dict(name="decode_B256_H16_D128", B=256, H=16, D=128, io="bf16", seed=5)
 
 
 def make_step_inputs(B: int, H: int, D: int, io: str = "bf16", seed: int = 0,

@@ -84,9 +84,15 @@ typedef enum { GLA_GATE_KEY = 0, GLA_GATE_SCALAR = 1 } gla_gate;
 typedef struct {
     int path;               /* gla_path                                                */
     int seq_splits;         /* tensor-core path: sequence segments per head; 0 = auto  */
-    void *workspace;        /* device scratch owned by the caller; NULL = the library
-                               keeps one per device (allocated on first need, grown
-                               when a larger problem arrives)                          */
+    void *workspace;        /* device scratch owned by the caller, or NULL. With NULL the
+                               library keeps one buffer per stream and device: allocated
+                               by the first call on that stream that needs scratch,
+                               replaced (cudaFree, which synchronises the device, then
+                               cudaMalloc) only when a call needs more than that stream's
+                               buffer holds; repeated calls of the same shape allocate
+                               nothing. Calls on different streams never share it. A
+                               caller buffer is the caller's to order: two calls whose
+                               kernels overlap on the GPU must not be given the same one. */
     size_t workspace_bytes; /* size of `workspace` in bytes                            */
     int gate;               /* gla_gate (0 = GLA_GATE_KEY)                             */
 } gla_options;
@@ -95,7 +101,11 @@ typedef struct {
  * gla_fwd — bf16 q, k, v, o; fp32 g_log, h0, hT; fp32 state and accumulation.
  * Arguments: q, k, v, g_log (inputs), scale (output multiplier, typically Dk^-0.5),
  * h0 (initial state or NULL), o (output), hT (final state or NULL), shape B, T, H, Dk,
- * Dv, and the stream. Runs the tensor-core path.
+ * Dv, and the stream. Runs the tensor-core path (T < 64 runs the exact kernel instead).
+ * Scratch: when the sequence is split across CTAs the call uses the library's workspace
+ * of `stream` (see gla_options.workspace): concurrent calls on different streams are safe;
+ * the first call on a stream (or the first needing a larger workspace) allocates, so make it
+ * before any stream capture begins.
  */
 gla_status gla_fwd(const void *q, const void *k, const void *v, const float *g_log,
                    float scale, const float *h0, void *o, float *hT,
@@ -111,7 +121,10 @@ gla_status gla_fwd_f32(const float *q, const float *k, const float *v, const flo
 /*
  * gla_fwd_ex — the general entry: io selects bf16 or fp32 q/k/v/o, opt (may be NULL)
  * selects the path, the sequence split, the workspace and the gate shape. The tensor-core
- * path needs bf16 I/O and Dk, Dv in {64, 128}.
+ * path needs bf16 I/O and Dk, Dv in {64, 128}; with fewer than 64 tokens it runs the exact
+ * kernel (whose results it then returns), since a handful of bf16-rounded products is all
+ * each output would be. Scratch as gla_fwd: opt->workspace, else the stream's own library
+ * workspace.
  */
 gla_status gla_fwd_ex(const void *q, const void *k, const void *v, const float *g_log,
                       float scale, const float *h0, void *o, float *hT,
@@ -142,7 +155,9 @@ gla_status gla_step(const void *q, const void *k, const void *v, const float *g_
  * h0, hT [N, H, Dk, Dv] fp32; cu_seqlens: DEVICE int32 [N + 1], non-decreasing, cu_seqlens[0]
  * = 0 and cu_seqlens[N] = T. The offsets are read on the device only: violations are
  * reported by gla_last_device_status as GLA_ERR_BAD_SEQLENS. Sequences are not split
- * (opt->seq_splits is ignored): the tensor-core path runs one CTA per sequence and head.
+ * (opt->seq_splits is ignored): the tensor-core path runs one CTA per sequence and head for
+ * every sequence of at least 64 tokens, and a second launch of the exact kernel on the same
+ * stream computes the shorter ones.
  * Other arguments, options and errors as gla_fwd_ex. This serves the batch-efficiency concern
  * of "面向长序列大模型的线性注意力算子性能评测方法与优化实践", section 四、评测维度设计 (no
  * padding to the longest sequence of a batch); the pages define no varlen interface.
@@ -185,6 +200,11 @@ const char *gla_status_string(gla_status s);
  * the library's kernels ran inside a timed region. */
 uint64_t gla_launch_counter(void);
 
+/* Number of device allocations (cudaMalloc) the library has made for its own per-stream
+ * workspaces in this process (all devices). A caller can check that its steady-state calls
+ * allocate nothing. */
+uint64_t gla_workspace_allocations(void);
+
 /* Size in bytes of the fixed scratch array behind gla_fwd_noalloc (16 MiB). */
 #define GLA_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 
@@ -196,13 +216,14 @@ uint64_t gla_launch_counter(void);
  * on a latency-critical path where the library's own workspace growth (cudaFree followed
  * by cudaMalloc, which synchronises the whole device) would stall other streams.
  *
- * Scratch: the tensor-core path's sequence split needs B*H*(splits-1)*131584 bytes of
- * scratch. This entry point takes it from one array of GLA_NOALLOC_SCRATCH_BYTES compiled
- * into the library, which every GPU that runs this entry point holds until the process
- * exits. seq_splits = 0 picks the split automatically, capped at the largest count whose
- * scratch fits; seq_splits > 0 whose scratch does not fit returns GLA_ERR_WORKSPACE
- * (gla_last_error_detail() gives the bytes needed) before anything is launched.
- * seq_splits < 0 returns GLA_ERR_BAD_OPTION.
+ * Scratch: the tensor-core path's sequence split needs the bytes gla_fwd_workspace_size()
+ * reports for the same shape and seq_splits (about B*H*(splits-1)*128 KiB, more where the
+ * state pass is cut into pieces). This entry point takes it from one array of
+ * GLA_NOALLOC_SCRATCH_BYTES compiled into the library, which every GPU that runs this entry
+ * point holds until the process exits. seq_splits = 0 picks the split gla_fwd would pick,
+ * lowered to the largest count whose scratch fits; seq_splits > 0 whose scratch does not fit
+ * returns GLA_ERR_WORKSPACE (gla_last_error_detail() gives the bytes needed) before anything
+ * is launched. seq_splits < 0 returns GLA_ERR_BAD_OPTION.
  *
  * Set-up: the first call on a device (with that device current) looks up the array's
  * device address with cudaGetSymbolAddress and caches it; make that first call before
@@ -238,8 +259,8 @@ gla_status gla_fwd_noalloc(const void *q, const void *k, const void *v, const fl
  * (GLA_ERR_UNSUPPORTED_DIM otherwise). Pointers are device pointers, 16-byte aligned
  * (GLA_ERR_MISALIGNED); o and hT must not overlap an input or each other (GLA_ERR_ALIAS).
  * Workspace: gdn_fwd_workspace_size() bytes of device memory, 16-byte aligned; pass NULL
- * to use the library's per-device workspace (allocated on first need, grown when a larger
- * problem arrives, shared with gla_fwd_ex: calls on different streams must not overlap).
+ * to use the library's workspace of `stream` (one per stream and device, shared with
+ * gla_fwd_ex calls on that stream; see gla_options.workspace).
  * A caller workspace smaller than needed, misaligned, or overlapping an argument returns
  * GLA_ERR_WORKSPACE. fp32 arithmetic on CUDA cores; deterministic (no atomics). Two
  * kernels, stream-ordered on `stream`; no host synchronisation. T = 0 writes hT = h0 (or

@@ -1,19 +1,24 @@
 """Failure detection without a GPU fault: a bounded pipeline wait that runs out.
 
-With GLA_TEST_STALL_ONE_LOAD set, the output kernel's TMA producer never issues the q/k/v
-load of one chunk. Every wait that depends on it gives up after its bounded limit, the
-kernel raises the library's device error word, drains what it issued, frees its TMEM and
-returns. The host then reads GLA_ERR_DEVICE_TIMEOUT, and the next call on the same context
-is correct.
+With GLA_TEST_STALL_ONE_LOAD set when a process starts, the library's first tensor-core
+launch in that process has its TMA producer skip the q/k/v load of one chunk. Every wait that
+depends on it gives up after its bounded limit, the kernel raises the library's device error
+word, drains what it issued, frees its TMEM and returns. The host then reads
+GLA_ERR_DEVICE_TIMEOUT, and the next call on the same context is correct. The library reads
+the variable once per process, so the scenario runs in a child process (tests/stall_child.py).
 """
-import time
+import json
+import os
+import subprocess
+import sys
 
 import pytest
-import torch
 
-from parity import assert_close
+from parity import TOL
 
 pytestmark = pytest.mark.gpu
+
+HERE = os.path.dirname(os.path.abspath(__file__))
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -22,29 +27,17 @@ def _built():
     __graft_entry__.build()
 
 
-def test_bounded_wait_times_out_and_context_survives(monkeypatch):
-    import oracle
-    from chunkwise_recurrent_prefill_gb300 import gla_fwd, last_device_status
-    from chunkwise_recurrent_prefill_gb300.workloads import make_inputs, small
-    x = make_inputs(small("stall", B=1, T=512, H=2, io="bf16", seed=6, with_h0=True),
-                    torch.device("cuda:0"))
-    assert last_device_status() == 0
-    monkeypatch.setenv("GLA_TEST_STALL_ONE_LOAD", "1")
-    t0 = time.time()
-    gla_fwd(x["q"], x["k"], x["v"], x["g"], x["scale"], x["h0"], return_state=True, path="tc",
-            seq_splits=1)
-    status = last_device_status()
-    waited = time.time() - t0
-    monkeypatch.delenv("GLA_TEST_STALL_ONE_LOAD")
-    assert status == 7, status                      # GLA_ERR_DEVICE_TIMEOUT
-    assert 1.0 < waited < 30.0, waited              # the waits are bounded (~2 s each)
-    assert last_device_status() == 0                # reading the status cleared it
-    o, hT = gla_fwd(x["q"], x["k"], x["v"], x["g"], x["scale"], x["h0"], return_state=True,
-                    path="tc", seq_splits=1)
-    torch.cuda.synchronize()
-    assert last_device_status() == 0
-    cpu = lambda t: None if t is None else t.cpu()  # noqa: E731
-    o_ref, h_ref = oracle.recurrent(cpu(x["q"]), cpu(x["k"]), cpu(x["v"]), cpu(x["g"]),
-                                    x["scale"], cpu(x["h0"]))
-    assert_close(o.float().cpu().numpy(), o_ref, "bf16", "o after timeout")
-    assert_close(hT.cpu().numpy(), h_ref, "bf16", "hT after timeout")
+def test_bounded_wait_times_out_and_context_survives():
+    env = dict(os.environ, GLA_TEST_STALL_ONE_LOAD="1")
+    r = subprocess.run([sys.executable, os.path.join(HERE, "stall_child.py")], env=env,
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-2000:]
+    out = json.loads(r.stdout.strip().splitlines()[-1])
+    assert out["status_before"] == 0
+    assert out["status_stalled"] == 7, out            # GLA_ERR_DEVICE_TIMEOUT
+    assert 1.0 < out["waited_s"] < 30.0, out          # the waits are bounded (~2 s each)
+    assert out["status_cleared"] == 0                 # reading the status cleared it
+    assert out["status_after"] == 0
+    for name in ("o_err", "hT_err"):
+        mx, mean = out[name]
+        assert mx <= TOL["bf16"]["max"] and mean <= TOL["bf16"]["mean"], (name, mx, mean)

@@ -2,15 +2,15 @@
 each sequence alone. Sequence lengths cover empty, single-token, partial-chunk and
 multi-chunk cases in one batch.
 
-bf16 tolerances as elsewhere; a sequence shorter than one 64-token chunk on the tensor-core
-path is held to max and mean <= 1.5e-2 (the few-token bf16 rounding floor: each output is a
-handful of bf16 dot products with nothing to average the rounding).
+Every sequence is held to the stated tolerances (bf16: max 1.5e-2, mean 5e-3). On the
+tensor-core path the sequences shorter than one 64-token chunk are computed by the exact
+kernel in a second launch of the same call, so they meet the bound too.
 """
 import numpy as np
 import pytest
 import torch
 
-from parity import assert_close, errors
+from parity import assert_close
 
 pytestmark = pytest.mark.gpu
 
@@ -60,14 +60,37 @@ def test_varlen_matches_oracle_per_sequence(path, io, gate):
             assert np.array_equal(h_out, h_ref), f"seq {i}: empty sequence must return h0"
             continue
         o_out = o[a:b].float().cpu().numpy()[None]
-        if path == "tc" and b - a < 64:
-            for out, ref in ((o_out, o_ref), (h_out, h_ref)):
-                mx, mean = errors(out, ref)
-                assert mx <= 1.5e-2 and mean <= 1.5e-2, (i, b - a, mx, mean)
-        else:
-            tol = "f32" if io == "f32" else "bf16"
-            assert_close(o_out, o_ref, tol, f"seq {i} (T={b - a}) o")
-            assert_close(h_out, h_ref, tol, f"seq {i} (T={b - a}) hT")
+        tol = "f32" if io == "f32" else "bf16"
+        assert_close(o_out, o_ref, tol, f"seq {i} (T={b - a}) o")
+        assert_close(h_out, h_ref, tol, f"seq {i} (T={b - a}) hT")
+
+
+@pytest.mark.parametrize("gate", ["key", "scalar"])
+def test_varlen_only_short_sequences(gate):
+    """A packed batch in which every sequence is shorter than one chunk (the tensor-core launch
+    then has nothing to do and the exact launch computes everything), and one whose total is
+    under a chunk (the call runs the exact kernel alone)."""
+    import oracle  # noqa: F401
+    from chunkwise_recurrent_prefill_gb300 import gla_fwd_varlen, last_device_status
+    from chunkwise_recurrent_prefill_gb300.workloads import make_inputs, small
+    for lens in ([1, 7, 63, 40, 2, 63], [3, 0, 20]):
+        H = 2
+        x = make_inputs(small("short", B=1, T=sum(lens), H=H, io="bf16", seed=sum(lens),
+                              gate=gate), DEV)
+        x = {n: (x[n][0] if n in ("q", "k", "v", "g") else x[n]) for n in x}
+        h0 = (0.02 * torch.randn(len(lens), H, 128, 128,
+                                 generator=torch.Generator("cpu").manual_seed(9))).to(DEV)
+        cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device=DEV)
+        o, hT = gla_fwd_varlen(x["q"], x["k"], x["v"], x["g"], x["scale"], cu, h0,
+                               return_state=True, path="tc", gate=gate)
+        torch.cuda.synchronize()
+        assert last_device_status() == 0
+        offs = np.concatenate([[0], np.cumsum(lens)])
+        for i, (a, b) in enumerate(zip(offs[:-1], offs[1:])):
+            o_ref, h_ref = _oracle_seq(x, x["scale"], h0, a, b, i, gate)
+            if b > a:
+                assert_close(o[a:b].float().cpu().numpy()[None], o_ref, "bf16", f"seq {i} o")
+            assert_close(hT[i].cpu().numpy()[None], h_ref, "bf16", f"seq {i} hT")
 
 
 def test_varlen_does_not_touch_neighbours():

@@ -4,9 +4,10 @@ Some hosts hand all device memory to their own pool and must account for every b
 some call from latency-critical code where a cudaMalloc / cudaFree (which synchronises the
 whole device) is not allowed. For them the library offers gla_fwd_noalloc, which takes the
 tensor-core path's scratch from a fixed array compiled into the library. These tests check,
-through the C ABI, that it gives what gla_fwd gives (bf16 parity tolerance) on two calls in
-a row that reuse the array, and that a request whose scratch does not fit is refused before
-anything runs. This file is collected last on purpose.
+through the C ABI, that its results match the fp64 oracle and gla_fwd (bf16 parity
+tolerance) on two calls in a row that reuse the array, that its automatic split steps down
+to the largest one whose scratch fits, and that a request whose scratch does not fit is
+refused before anything runs. This file is collected last on purpose.
 """
 import ctypes
 
@@ -27,9 +28,11 @@ def _lib():
 
 
 def _raw_call(lib, B, T, H, seq_splits, addr=0x1000000000):
-    """Call with fake, far-apart device addresses: only host-side checks may run."""
+    """Host-side checks only: q is NULL, so even a call that got past the scratch checks would
+    be refused (GLA_ERR_NULL_ARG) before anything launched; the other pointers are fake,
+    far-apart addresses that nothing dereferences."""
     p = lambda i: ctypes.c_void_p(addr * (i + 1))  # noqa: E731
-    return lib.gla_fwd_noalloc(p(0), p(1), p(2), p(3), ctypes.c_float(1.0), None, p(4), None,
+    return lib.gla_fwd_noalloc(None, p(1), p(2), p(3), ctypes.c_float(1.0), None, p(4), None,
                                B, T, H, 128, 128, seq_splits, None)
 
 
@@ -49,7 +52,16 @@ def _inputs(B, T, H, seed, with_h0=True):
                        torch.device("cuda:0"))
 
 
+def _oracle(x):
+    import oracle
+    cpu = lambda t: None if t is None else t.cpu()  # noqa: E731
+    return oracle.recurrent(cpu(x["q"]), cpu(x["k"]), cpu(x["v"]), cpu(x["g"]), x["scale"],
+                            cpu(x["h0"]))
+
+
 def _compare(x, seq_splits):
+    """gla_fwd_noalloc against the fp64 oracle and against gla_fwd (same split request), both
+    at the bf16 parity tolerance. Returns the noalloc outputs."""
     from chunkwise_recurrent_prefill_gb300 import gla_fwd, gla_fwd_noalloc, last_device_status
     B, T, H, D = x["q"].shape
     o = torch.empty((B, T, H, D), dtype=torch.bfloat16, device="cuda:0")
@@ -58,11 +70,16 @@ def _compare(x, seq_splits):
                     seq_splits=seq_splits)
     torch.cuda.synchronize()
     assert last_device_status() == 0
-    o_ref, h_ref = gla_fwd(x["q"], x["k"], x["v"], x["g"], x["scale"], x["h0"],
+    o_fwd, h_fwd = gla_fwd(x["q"], x["k"], x["v"], x["g"], x["scale"], x["h0"],
                            return_state=True, seq_splits=seq_splits)
     torch.cuda.synchronize()
-    assert_close(o.float().cpu().numpy(), o_ref.float().cpu().numpy(), "bf16", "o(noalloc)")
-    assert_close(hT.cpu().numpy(), h_ref.cpu().numpy(), "bf16", "hT(noalloc)")
+    o_ref, h_ref = _oracle(x)
+    o_np, h_np = o.float().cpu().numpy(), hT.cpu().numpy()
+    assert_close(o_np, o_ref, "bf16", "o(noalloc) vs oracle")
+    assert_close(h_np, h_ref, "bf16", "hT(noalloc) vs oracle")
+    assert_close(o_np, o_fwd.float().cpu().numpy(), "bf16", "o(noalloc) vs gla_fwd")
+    assert_close(h_np, h_fwd.cpu().numpy(), "bf16", "hT(noalloc) vs gla_fwd")
+    return o, hT
 
 
 @pytest.mark.gpu
@@ -96,3 +113,23 @@ def test_noalloc_oversize_refused_and_auto_split_capped():
     # automatic split of gla_fwd_noalloc is capped to fit and still matches gla_fwd
     assert workspace_size(1, 16384, 16) > MAX_SCRATCH
     _compare(x, seq_splits=0)
+
+
+@pytest.mark.gpu
+def test_noalloc_auto_split_one_head_long_sequence():
+    """One head of 16384 tokens: gla_fwd would cut it into 152 segments (19.9 MB of scratch).
+    The automatic split of gla_fwd_noalloc steps down from there to the largest count that fits
+    the 16 MiB array: 128 segments (127 x 131584 B). Its outputs are then bit for bit those of
+    gla_fwd with seq_splits=128 (same kernels, same split, deterministic)."""
+    from chunkwise_recurrent_prefill_gb300 import gla_fwd
+    from chunkwise_recurrent_prefill_gb300.gla import workspace_size
+    _lib()
+    assert workspace_size(1, 16384, 1) > MAX_SCRATCH
+    assert workspace_size(1, 16384, 1, seq_splits=128) <= MAX_SCRATCH
+    assert workspace_size(1, 16384, 1, seq_splits=129) > MAX_SCRATCH
+    x = _inputs(1, 16384, 1, seed=44)
+    o, hT = _compare(x, seq_splits=0)
+    o128, h128 = gla_fwd(x["q"], x["k"], x["v"], x["g"], x["scale"], x["h0"], return_state=True,
+                         seq_splits=128)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o128) and torch.equal(hT, h128)
