@@ -59,7 +59,7 @@ constexpr int kD = 128;                // Dk = Dv
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kExtreme2 = 50.f;      // |b| (log2 units) beyond which P takes the exact route
 constexpr float kRenorm2 = 50.f;       // |L| (log2 units) beyond which the state is renormalised
-constexpr int64_t kL2KeepBytes = 96ll << 20;  // state-pass reads kept in L2 for the output pass
+constexpr int64_t kL2KeepBytes = 64ll << 20;  // state-pass reads kept in L2 for the output pass
 constexpr int kGateBlock = 8;          // tokens per load/compute/store block of the gate warps
 constexpr unsigned kProducerNapNs = 128;  // idle back-off of the TMA producer's polling loop
 constexpr unsigned kIssuerNapNs = 32;     // idle back-off of the MMA issuers' polling loops
@@ -808,29 +808,21 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 }
                 return *reinterpret_cast<const float2 *>(grow + t * kD);
             };
-            // Pass 1: the running log2-gate sums of the thread's tokens, kept in registers for
-            // pass 2 (the g slot is read once and released right after).
             float r0 = 0.f, r1 = 0.f;
             float lo0 = 0.f, hi0 = 0.f, lo1 = 0.f, hi1 = 0.f;   // range of the running sums
-            float2 rsum[kGatePart];
+#pragma unroll 1
+            for (int t0 = 0; t0 < tl; t0 += kGateBlock) {
+                float2 gv[kGateBlock];
 #pragma unroll
-            for (int t0 = 0; t0 < kGatePart; t0 += kGateBlock) {
-                if (t0 < tl) {
-                    float2 gv[kGateBlock];
+                for (int x = 0; x < kGateBlock; ++x) gv[x] = gpair(t0 + x);
 #pragma unroll
-                    for (int x = 0; x < kGateBlock; ++x) gv[x] = gpair(t0 + x);
-#pragma unroll
-                    for (int x = 0; x < kGateBlock; ++x) {
-                        r0 = fmaf(gv[x].x, kLog2e, r0);
-                        r1 = kScalar ? r0 : fmaf(gv[x].y, kLog2e, r1);
-                        rsum[t0 + x] = make_float2(r0, r1);
-                        lo0 = fminf(lo0, r0); hi0 = fmaxf(hi0, r0);
-                        lo1 = fminf(lo1, r1); hi1 = fmaxf(hi1, r1);
-                    }
+                for (int x = 0; x < kGateBlock; ++x) {
+                    r0 = fmaf(gv[x].x, kLog2e, r0);
+                    r1 = fmaf(gv[x].y, kLog2e, r1);
+                    lo0 = fminf(lo0, r0); hi0 = fmaxf(hi0, r0);
+                    lo1 = fminf(lo1, r1); hi1 = fmaxf(hi1, r1);
                 }
             }
-            __syncwarp();
-            if (!kScalar && lane == 0) mbar_arrive(&bars[GEMPTY + gs]);   // the g slot may be refilled
             *reinterpret_cast<float2 *>(xch + part * kD + d) = make_float2(r0, r1);
             named_bar_sync(1, kGateThreads);
             // b = off + (running sum within the range), with off the left-to-right sum of the
@@ -874,75 +866,81 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 for (int t = max(vr - tb, 0); t < tl; ++t)
                     *reinterpret_cast<uint32_t *>(kt + sw128_offset((uint32_t)(tb + t), col)) = 0u;
             }
-            // Pass 2, in blocks of kGateBlock tokens: all loads of a block are issued before
-            // its stores, so a block costs one shared-memory round trip.
+            r0 = 0.f;
+            r1 = 0.f;
+            // blocks of kGateBlock tokens: all loads of a block are issued before its stores, so a
+            // block costs one shared-memory round trip
             if (!ext) {
                 // Q' = scale q 2^(b + L), K' = k 2^-(b + L) with b = off + r: the per-chunk
                 // constants (offset, L, log2 scale) are folded into two exponent biases
                 const float eq0 = off0 + Lq0 + lsc, eq1 = off1 + Lq1 + lsc;
                 const float ek0 = -(off0 + Lq0), ek1 = -(off1 + Lq1);
+#pragma unroll 1
+                for (int t0 = 0; t0 < tl; t0 += kGateBlock) {
+                    float2 gv[kGateBlock];
+                    uint32_t qv[kGateBlock], kv[kGateBlock];
 #pragma unroll
-                for (int t0 = 0; t0 < kGatePart; t0 += kGateBlock) {
-                    if (t0 < tl) {
-                        uint32_t qv[kGateBlock], kv[kGateBlock];
+                    for (int x = 0; x < kGateBlock; ++x) {
+                        const uint32_t off = (uint32_t)(tb + t0) * 128u + swz[x];
+                        gv[x] = gpair(t0 + x);
+                        qv[x] = *reinterpret_cast<const uint32_t *>(qt + off);
+                        kv[x] = *reinterpret_cast<const uint32_t *>(kt + off);
+                    }
 #pragma unroll
-                        for (int x = 0; x < kGateBlock; ++x) {
-                            const uint32_t off = (uint32_t)(tb + t0) * 128u + swz[x];
-                            qv[x] = *reinterpret_cast<const uint32_t *>(qt + off);
-                            kv[x] = *reinterpret_cast<const uint32_t *>(kt + off);
+                    for (int x = 0; x < kGateBlock; ++x) {
+                        const float2 qf = unpack_bf16(qv[x]), kf = unpack_bf16(kv[x]);
+                        r0 = fmaf(gv[x].x, kLog2e, r0);
+                        if (kScalar) {
+                            // one gate for every key dimension: both columns share the factors
+                            const float fq = ex2(r0 + eq0), fk = ex2(ek0 - r0);
+                            qv[x] = pack_bf16(qf.x * fq, qf.y * fq);
+                            kv[x] = pack_bf16(kf.x * fk, kf.y * fk);
+                        } else {
+                            r1 = fmaf(gv[x].y, kLog2e, r1);
+                            qv[x] = pack_bf16(qf.x * ex2(r0 + eq0), qf.y * ex2(r1 + eq1));
+                            kv[x] = pack_bf16(kf.x * ex2(ek0 - r0), kf.y * ex2(ek1 - r1));
                         }
+                    }
 #pragma unroll
-                        for (int x = 0; x < kGateBlock; ++x) {
-                            const float2 qf = unpack_bf16(qv[x]), kf = unpack_bf16(kv[x]);
-                            const float2 r = rsum[t0 + x];
-                            if (kScalar) {
-                                // one gate for every key dimension: both columns share the factors
-                                const float fq = ex2(r.x + eq0), fk = ex2(ek0 - r.x);
-                                qv[x] = pack_bf16(qf.x * fq, qf.y * fq);
-                                kv[x] = pack_bf16(kf.x * fk, kf.y * fk);
-                            } else {
-                                qv[x] = pack_bf16(qf.x * ex2(r.x + eq0), qf.y * ex2(r.y + eq1));
-                                kv[x] = pack_bf16(kf.x * ex2(ek0 - r.x), kf.y * ex2(ek1 - r.y));
-                            }
-                        }
-#pragma unroll
-                        for (int x = 0; x < kGateBlock; ++x) {
-                            const uint32_t off = (uint32_t)(tb + t0) * 128u + swz[x];
-                            *reinterpret_cast<uint32_t *>(qt + off) = qv[x];
-                            *reinterpret_cast<uint32_t *>(kt + off) = kv[x];
-                        }
+                    for (int x = 0; x < kGateBlock; ++x) {
+                        const uint32_t off = (uint32_t)(tb + t0) * 128u + swz[x];
+                        *reinterpret_cast<uint32_t *>(qt + off) = qv[x];
+                        *reinterpret_cast<uint32_t *>(kt + off) = kv[x];
                     }
                 }
             } else {
                 // extreme chunk: K^ = k 2^(Bc - b) with b = off + r formed exactly as the chunk
                 // total was, so that the last token's factor is exactly 1
+#pragma unroll 1
+                for (int t0 = 0; t0 < tl; t0 += kGateBlock) {
+                    float2 gv[kGateBlock];
+                    uint32_t qv[kGateBlock], kv[kGateBlock];
 #pragma unroll
-                for (int t0 = 0; t0 < kGatePart; t0 += kGateBlock) {
-                    if (t0 < tl) {
-                        uint32_t qv[kGateBlock], kv[kGateBlock];
+                    for (int x = 0; x < kGateBlock; ++x) {
+                        const uint32_t off = (uint32_t)(tb + t0) * 128u + swz[x];
+                        gv[x] = gpair(t0 + x);
+                        qv[x] = *reinterpret_cast<const uint32_t *>(qt + off);
+                        kv[x] = *reinterpret_cast<const uint32_t *>(kt + off);
+                    }
 #pragma unroll
-                        for (int x = 0; x < kGateBlock; ++x) {
-                            const uint32_t off = (uint32_t)(tb + t0) * 128u + swz[x];
-                            qv[x] = *reinterpret_cast<const uint32_t *>(qt + off);
-                            kv[x] = *reinterpret_cast<const uint32_t *>(kt + off);
-                        }
+                    for (int x = 0; x < kGateBlock; ++x) {
+                        r0 = fmaf(gv[x].x, kLog2e, r0);
+                        r1 = fmaf(gv[x].y, kLog2e, r1);
+                        const float b0 = off0 + r0, b1 = off1 + r1;
+                        const float2 qf = unpack_bf16(qv[x]), kf = unpack_bf16(kv[x]);
+                        qv[x] = pack_bf16(sc * qf.x * ex2(b0), sc * qf.y * ex2(b1));
+                        kv[x] = pack_bf16(kf.x * ex2(B0 - b0), kf.y * ex2(B1 - b1));
+                    }
 #pragma unroll
-                        for (int x = 0; x < kGateBlock; ++x) {
-                            const float2 r = rsum[t0 + x];
-                            const float b0 = off0 + r.x, b1 = off1 + r.y;
-                            const float2 qf = unpack_bf16(qv[x]), kf = unpack_bf16(kv[x]);
-                            qv[x] = pack_bf16(sc * qf.x * ex2(b0), sc * qf.y * ex2(b1));
-                            kv[x] = pack_bf16(kf.x * ex2(B0 - b0), kf.y * ex2(B1 - b1));
-                        }
-#pragma unroll
-                        for (int x = 0; x < kGateBlock; ++x) {
-                            const uint32_t off = (uint32_t)(tb + t0) * 128u + swz[x];
-                            *reinterpret_cast<uint32_t *>(qt + off) = qv[x];
-                            *reinterpret_cast<uint32_t *>(kt + off) = kv[x];
-                        }
+                    for (int x = 0; x < kGateBlock; ++x) {
+                        const uint32_t off = (uint32_t)(tb + t0) * 128u + swz[x];
+                        *reinterpret_cast<uint32_t *>(qt + off) = qv[x];
+                        *reinterpret_cast<uint32_t *>(kt + off) = kv[x];
                     }
                 }
             }
+            __syncwarp();
+            if (!kScalar && lane == 0) mbar_arrive(&bars[GEMPTY + gs]);   // the g slot may be refilled
             if (gt == 0) xf[slot] = (ext ? 1u : 0u) | (ren ? 2u : 0u);
             fence_proxy_async_smem();
             __syncwarp();
