@@ -18,10 +18,16 @@
 // of state columns), which forms U and O from S0 in one pass and then S1: the columns of S
 // are independent under this recurrence (the transition acts on the key axis only), which is
 // what lets B = 1 spread over many SMs.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <mutex>
+#include <type_traits>
+
 #include "gla_internal.h"
+#include "tc_ptx.cuh"
+#include "tma_host.h"
 
 namespace gla {
 namespace {
@@ -72,6 +78,22 @@ struct WsLayout {
     }
 };
 
+// Workspace of the tensor-core scan (bf16 I/O, Dk = Dv = 128): one array per quantity, so
+// that each is a plain 2-D tensor the scan can tile with TMA. For chunk blk = bh * nchunks + c:
+//   W [blk][64][Dk]    G [blk][64][Dk]    Kt [blk][Dk][64] (Kh transposed)
+//   U [blk][64][Dv]    O [blk][64][Dv]    C [blk] (b_63, the chunk's summed log-gate)
+struct SoA {
+    float *W, *G, *Kt, *U, *O, *C;
+    __host__ __device__ SoA(float *ws, int64_t nblk, int Dk, int Dv) {
+        W = ws;
+        G = W + nblk * kC * Dk;
+        Kt = G + nblk * kC * Dk;
+        U = Kt + nblk * Dk * kC;
+        O = U + nblk * kC * Dv;
+        C = O + nblk * kC * Dv;
+    }
+};
+
 struct GdnArgs {
     const void *q, *k, *v;
     const float *g, *beta;
@@ -82,13 +104,14 @@ struct GdnArgs {
     int64_t T;
     int H, Dk, Dv, nchunks;
     float *ws;
+    int64_t nblk;            // B * H * nchunks (structure-of-arrays workspace)
 };
 
 constexpr int kPieces = kC * kMaxD / 4 / kThreads;   // 4-element pieces of a tile per thread
 
 // ---------------------------------------------------------------------------------------
 // Chunk-parallel part: one CTA per (batch, head, chunk).
-template <typename T>
+template <typename T, bool kSoA>
 __global__ void __launch_bounds__(kThreads, 2) gdn_prep_kernel(GdnArgs a) {
     extern __shared__ __align__(16) float smp[];
     float *Qt = smp;                                  // [Dk][kPrepStride]; later v [64][Dv]
@@ -113,6 +136,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prep_kernel(GdnArgs a) {
     auto row = [&](int j) -> int64_t { return (bb * a.T + t0 + j) * a.H + h; };   // token row
     const WsLayout L(Dk, Dv);
     float *ws = a.ws + blk * L.total;
+    const SoA so(a.ws, a.nblk, Dk, Dv);
 
     // q and k in 4-element pieces (piece p: row j = p % 64, key dims 4 (p / 64) ..), all
     // loads of a thread in flight at once; then transposed into [d][j]. The 32 lanes of a
@@ -158,17 +182,26 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prep_kernel(GdnArgs a) {
         ek[tid] = expf(bs[kC - 1] - bs[tid]);
     }
     __syncthreads();
-    // Kh = exp(b_63 - b_j) k_j straight from the pieces in registers; exp(b_63)
-#pragma unroll
-    for (int it = 0; it < kPieces; ++it) {
-        const int p = tid + kThreads * it, j = p & (kC - 1), c4 = p >> 6;
-        if (p < npk) {
-            const float e = ek[j];
-            *reinterpret_cast<float4 *>(ws + L.oK + (int64_t)j * Dk + 4 * c4) =
-                make_float4(e * kr[it].x, e * kr[it].y, e * kr[it].z, e * kr[it].w);
+    if (kSoA) {
+        // Kh transposed, [d][j], from the transposed k tile; the chunk's summed log-gate
+        for (int idx = tid; idx < Dk * kC; idx += kThreads) {
+            const int d = idx / kC, j = idx % kC;
+            so.Kt[(blk * Dk + d) * kC + j] = ek[j] * Kt[d * kPrepStride + j];
         }
+        if (tid == 0) so.C[blk] = bs[kC - 1];
+    } else {
+        // Kh = exp(b_63 - b_j) k_j straight from the pieces in registers; exp(b_63)
+#pragma unroll
+        for (int it = 0; it < kPieces; ++it) {
+            const int p = tid + kThreads * it, j = p & (kC - 1), c4 = p >> 6;
+            if (p < npk) {
+                const float e = ek[j];
+                *reinterpret_cast<float4 *>(ws + L.oK + (int64_t)j * Dk + 4 * c4) =
+                    make_float4(e * kr[it].x, e * kr[it].y, e * kr[it].z, e * kr[it].w);
+            }
+        }
+        if (tid < 4) ws[L.oC + tid] = tid == 0 ? eb[kC - 1] : 0.f;
     }
-    if (tid < 4) ws[L.oC + tid] = tid == 0 ? eb[kC - 1] : 0.f;
 
     // K K^T and Q K^T, one 4 x 4 tile of each per thread: rows 4 mg .., columns 4 ng ..
     {
@@ -212,8 +245,13 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prep_kernel(GdnArgs a) {
     // Qh = scale exp(b_i) q_i (transposed) goes to the workspace, where it becomes G below;
     // then the q tile's space takes v, rows j, for the right-hand sides of the solve
     for (int idx = tid; idx < Dk * kC; idx += kThreads) {
-        const int d = idx / kC, i = idx % kC;
-        ws[L.oG + idx] = a.scale * eb[i] * Qt[d * kPrepStride + i];
+        if (kSoA) {
+            const int i = idx / Dk, d = idx % Dk;
+            so.G[(blk * kC + i) * Dk + d] = a.scale * eb[i] * Qt[d * kPrepStride + i];
+        } else {
+            const int d = idx / kC, i = idx % kC;
+            ws[L.oG + idx] = a.scale * eb[i] * Qt[d * kPrepStride + i];
+        }
     }
     __syncthreads();
     float *Vs = Qt;   // [64][Dv]
@@ -260,12 +298,18 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prep_kernel(GdnArgs a) {
             x[j] = r - (s0 + s1);
         }
         if (isk) {
-            float *wt = ws + L.oW + (int64_t)col * kC;
+            if (kSoA) {
+                float *w = so.W + blk * kC * Dk + col;
 #pragma unroll
-            for (int j = 0; j < kC; j += 4)
-                *reinterpret_cast<float4 *>(wt + j) = make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
+                for (int j = 0; j < kC; ++j) w[(int64_t)j * Dk] = x[j];
+            } else {
+                float *wt = ws + L.oW + (int64_t)col * kC;
+#pragma unroll
+                for (int j = 0; j < kC; j += 4)
+                    *reinterpret_cast<float4 *>(wt + j) = make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
+            }
         } else {
-            float *ut = ws + L.oU + cv;
+            float *ut = kSoA ? so.U + blk * kC * Dv + cv : ws + L.oU + cv;
 #pragma unroll
             for (int j = 0; j < kC; ++j) ut[(int64_t)j * Dv] = x[j];
         }
@@ -287,12 +331,18 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prep_kernel(GdnArgs a) {
                 }
                 y[r] = s0 + s1;
             }
-            if (isk) {   // G = Qh - P W, in place of Qh (this thread's own row of it)
-                float4 *gp = reinterpret_cast<float4 *>(ws + L.oG + (int64_t)col * kC + i0);
-                const float4 qh = *gp;
-                *gp = make_float4(qh.x - y[0], qh.y - y[1], qh.z - y[2], qh.w - y[3]);
+            if (isk) {   // G = Qh - P W, in place of Qh (this thread's own column of it)
+                if (kSoA) {
+                    float *gp = so.G + (blk * kC + i0) * Dk + col;
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) gp[(int64_t)r * Dk] -= y[r];
+                } else {
+                    float4 *gp = reinterpret_cast<float4 *>(ws + L.oG + (int64_t)col * kC + i0);
+                    const float4 qh = *gp;
+                    *gp = make_float4(qh.x - y[0], qh.y - y[1], qh.z - y[2], qh.w - y[3]);
+                }
             } else {
-                float *op = ws + L.oO + cv;
+                float *op = kSoA ? so.O + blk * kC * Dv + cv : ws + L.oO + cv;
 #pragma unroll
                 for (int r = 0; r < 4; ++r) op[(int64_t)(i0 + r) * Dv] = y[r];
             }
@@ -545,17 +595,386 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_scan_kernel(GdnArgs a) {
     }
 }
 
+// ---------------------------------------------------------------------------------------
+// Serial part on the tensor cores (bf16 I/O, Dk = Dv = 128): one CTA per (batch, head), the
+// fp32 state kept in TMEM across all chunks, transposed (lane = value column v, column = key
+// row d) and decay-normalised: S = 2^L S~ with one scalar L per head (the gate is one per
+// token). Per chunk c, with the prep's W, G, Kh, Ut, Oi and b_63:
+//   [W S | G S]^T = S~^T [W | G]^T 2^L    one MMA chain, A = S~^T straight from TMEM (tf32)
+//   U = Ut - 2^L (W S~),  O = Oi + 2^L (G S~)                      (CUDA cores, fp32)
+//   S~ += (2^-L' U)^T Kh,  L' = L + b_63 log2(e)      A = the scaled U^T, from TMEM (tf32)
+// The state is rescaled (S~ <- 2^L' S~, L' <- 0) when |L'| passes kRenormL2, before the
+// update that would use it; a full-forgetting chunk (b_63 very negative) so zeroes S~.
+// tf32 operands (10-bit mantissa) keep the fp32 state's accuracy far inside the bf16 output
+// tolerance (an fp64 simulation of these products even with bf16 operands stays at a mean
+// relative error of 2e-3 in o and hT).
+namespace gt {
+constexpr int kStages = 2;
+// stage: four [W | G] slabs (dk 32 s .. 32 s + 31: W rows then G rows, 128 rows x 128 B,
+// 128B-swizzled, one swizzle atom per 8 rows) and two Kh^T boxes (tokens 32 s .., 128 rows)
+constexpr uint32_t WG = 0, WGSLAB = 16384, KT = 65536, KTBOX = 16384, STAGE = 98304;
+constexpr uint32_t BAR = kStages * STAGE;
+constexpr uint32_t NBAR = 12;
+constexpr uint32_t TSLOT = BAR + NBAR * 8;
+constexpr uint32_t ALLOC = TSLOT + 16 + 1024;
+// TMEM columns
+constexpr uint32_t kS = 0;       // S~^T, 128 columns
+constexpr uint32_t kWG = 128;    // [W S~ | G S~]^T, 2 x 128 columns (double buffered)
+constexpr uint32_t kU = 384;     // scaled U^T (A operand of the update), 64 columns
+constexpr int kThreadsTC = 14 * 32;   // producer, MMA issuer, 8 U warps, 4 O warps
+constexpr float kRenormL2 = 60.f;
+enum { FULL = 0, EMPTY = 2, WGD = 4, WGF = 6, URDY = 8, FIN = 9 };
+}  // namespace gt
+
+// tcgen05.mma kind::tf32 with A from TMEM: D (+)= A[tmem] * B[smem]
+__device__ __forceinline__ void mma_tf32_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Instruction descriptor for kind::tf32, fp32 accumulation, both operands K-major.
+__host__ __device__ constexpr uint32_t idesc_tf32(uint32_t M, uint32_t N) {
+    return (1u << 4)            // D format: f32
+           | (2u << 7)          // A format: tf32
+           | (2u << 10)         // B format: tf32
+           | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+__device__ __forceinline__ float ex2f(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// 2-D tiled load (x = inner coordinate, y = row) into shared memory.
+__device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, uint64_t *bar, int x,
+                                            int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(tc::smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(tc::smem_u32(bar)), "r"(x), "r"(y)
+        : "memory");
+}
+
+__global__ void __launch_bounds__(gt::kThreadsTC, 1)
+gdn_tc_scan_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap tg,
+                   const __grid_constant__ CUtensorMap tkt, GdnArgs a, unsigned *err) {
+    using namespace gt;
+    extern __shared__ uint8_t smraw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) &
+                                              ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + BAR);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + TSLOT);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t bh = blockIdx.x;
+    const int64_t bb = bh / a.H, h = bh % a.H;
+    const int n = a.nchunks;
+    const int64_t blk0 = bh * n;
+    const SoA so(a.ws, a.nblk, kMaxD, kMaxD);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            tc::mbar_init(&bars[FULL + i], 1);
+            tc::mbar_init(&bars[EMPTY + i], 1);
+            tc::mbar_init(&bars[WGD + i], 1);
+            tc::mbar_init(&bars[WGF + i], 4);
+        }
+        tc::mbar_init(&bars[URDY], 8);
+        tc::mbar_init(&bars[FIN], 1);
+        tc::fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tc::tma_prefetch_desc(&tw);
+        tc::tma_prefetch_desc(&tg);
+        tc::tma_prefetch_desc(&tkt);
+    }
+    if (warp == 1) tc::tmem_alloc(tslot, 512);
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tm = *tslot;
+    // the initial state, transposed into TMEM (U warps: lane quarter j, key rows of their half)
+    if (warp >= 2 && warp < 10) {
+        const int j = warp & 3, half = (warp - 2) >> 2, v = j * 32 + lane;
+#pragma unroll 1
+        for (int d0 = 64 * half; d0 < 64 * half + 64; d0 += 16) {
+            uint32_t r[16];
+#pragma unroll
+            for (int x = 0; x < 16; ++x)
+                r[x] = a.h0 ? __float_as_uint(a.h0[(bh * kMaxD + d0 + x) * kMaxD + v]) : 0u;
+            tc::tmem_st16(tc::tmem_addr(tm, j, kS + d0), r);
+        }
+        tc::tmem_wait_st();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    bool ok = true;
+
+    if (warp == 0) {
+        // ---- TMA producer: [W | G] slabs and Kh^T boxes of each chunk
+        if (lane == 0) {
+            int issued = 0;
+            for (int c = 0; c < n && ok; ++c) {
+                const int st = c % kStages;
+                if (c >= kStages && !tc::mbar_wait(&bars[EMPTY + st], ((c / kStages) - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                uint64_t *fb = &bars[FULL + st];
+                tc::mbar_arrive_expect_tx(fb, STAGE);
+                uint8_t *base = sm + st * STAGE;
+                const int row = (int)((blk0 + c) * kC);
+#pragma unroll
+                for (int sl = 0; sl < 4; ++sl) {
+                    tma_load_2d(base + WG + sl * WGSLAB, &tw, fb, 32 * sl, row);
+                    tma_load_2d(base + WG + sl * WGSLAB + 8192, &tg, fb, 32 * sl, row);
+                }
+                const int krow = (int)((blk0 + c) * kMaxD);
+#pragma unroll
+                for (int bx = 0; bx < 2; ++bx)
+                    tma_load_2d(base + KT + bx * KTBOX, &tkt, fb, 32 * bx, krow);
+                ++issued;
+            }
+            // no bulk copy may still be landing when the CTA exits
+            for (int i = 0; i < kStages && i < issued; ++i) {
+                const int uses = (issued - 1 - i) / kStages + 1;
+                if (!tc::mbar_wait(&bars[FULL + i], (uses - 1) & 1)) ok = false;
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---- MMA issuer (converged warp, one elected lane issues)
+        const uint32_t idWG = idesc_tf32(128, 128), idUP = idesc_tf32(128, 128);
+        for (int c = 0; c < n; ++c) {
+            const int st = c % kStages, wb = c & 1;
+            bool w = tc::mbar_wait(&bars[FULL + st], (c / kStages) & 1);
+            if (w && c >= 2) w = tc::mbar_wait(&bars[WGF + wb], ((c >> 1) - 1) & 1);
+            if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+            tc::tc_fence_after();
+            const uint32_t base = tc::smem_u32(sm + st * STAGE);
+            if (tc::elect_one()) {
+                // [W S~ | G S~]^T: K = 128 key rows in 16 steps of 8 (32 bytes of a slab row)
+#pragma unroll
+                for (int kk = 0; kk < 16; ++kk)
+                    mma_tf32_ts(tm + kWG + wb * 128, tm + kS + kk * 8,
+                                tc::smem_desc(base + WG + (kk >> 2) * WGSLAB + (kk & 3) * 32, 16, 1024),
+                                idWG, kk > 0);
+                tc::mma_commit(&bars[WGD + wb]);
+            }
+            __syncwarp();
+            w = tc::mbar_wait(&bars[URDY], c & 1);
+            if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+            tc::tc_fence_after();
+            if (tc::elect_one()) {
+                // S~^T += (scaled U)^T Kh: K = 64 tokens in 8 steps of 8
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_tf32_ts(tm + kS, tm + kU + kk * 8,
+                                tc::smem_desc(base + KT + (kk >> 2) * KTBOX + (kk & 3) * 32, 16, 1024),
+                                idUP, 1);
+                tc::mma_commit(&bars[EMPTY + st]);   // the stage's last reader
+            }
+            __syncwarp();
+        }
+        if (tc::elect_one()) tc::mma_commit(&bars[FIN]);
+        __syncwarp();
+        if (!tc::mbar_wait(&bars[FIN], 0)) ok = false;
+    } else if (warp < 10) {
+        // ---- U warps: U = Ut - 2^L (W S~), scaled by 2^-L' into TMEM; rescale S~ when due
+        const int j = warp & 3, half = (warp - 2) >> 2, v = j * 32 + lane;
+        const int t0 = 32 * half;
+        float L = 0.f;
+        float ut[32];
+        auto load_ut = [&](int c) {
+            const float *src = so.U + ((blk0 + c) * kC + t0) * kMaxD + v;
+#pragma unroll
+            for (int x = 0; x < 32; ++x) ut[x] = src[x * kMaxD];
+        };
+        if (n > 0) load_ut(0);
+        for (int c = 0; c < n; ++c) {
+            const float bsum = so.C[blk0 + c];
+            const bool w = tc::mbar_wait(&bars[WGD + (c & 1)], (c >> 1) & 1);
+            if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+            tc::tc_fence_after();
+            float acc[32];
+            {
+                uint32_t r0[16], r1[16];
+                tc::tmem_ld16(tc::tmem_addr(tm, j, kWG + (c & 1) * 128 + t0), r0);
+                tc::tmem_ld16(tc::tmem_addr(tm, j, kWG + (c & 1) * 128 + t0 + 16), r1);
+                tc::tmem_wait_ld();
+                tc::reg_fence(r0);
+                tc::reg_fence(r1);
+#pragma unroll
+                for (int x = 0; x < 16; ++x) {
+                    acc[x] = __uint_as_float(r0[x]);
+                    acc[16 + x] = __uint_as_float(r1[x]);
+                }
+            }
+            const float eL = ex2f(L);
+            float Ln = L + bsum * 1.4426950408889634f;
+            const bool ren = !(fabsf(Ln) <= kRenormL2);   // also on NaN
+            if (ren) {
+                // every MMA reading S~ for this chunk (the [W | G] chain) has completed: scale
+                // this warp's lane quarter, key rows of its half, by 2^L'
+                const float f = ex2f(Ln);
+#pragma unroll 1
+                for (int d0 = 64 * half; d0 < 64 * half + 64; d0 += 16) {
+                    uint32_t r[16];
+                    tc::tmem_ld16(tc::tmem_addr(tm, j, kS + d0), r);
+                    tc::tmem_wait_ld();
+                    tc::reg_fence(r);
+#pragma unroll
+                    for (int x = 0; x < 16; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * f);
+                    tc::tmem_st16(tc::tmem_addr(tm, j, kS + d0), r);
+                }
+                Ln = 0.f;
+            }
+            const float su = ex2f(-Ln);
+            uint32_t u0[16], u1[16];
+#pragma unroll
+            for (int x = 0; x < 16; ++x) {
+                u0[x] = __float_as_uint((ut[x] - eL * acc[x]) * su);
+                u1[x] = __float_as_uint((ut[16 + x] - eL * acc[16 + x]) * su);
+            }
+            tc::tmem_st16(tc::tmem_addr(tm, j, kU + t0), u0);
+            tc::tmem_st16(tc::tmem_addr(tm, j, kU + t0 + 16), u1);
+            tc::tmem_wait_st();
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&bars[URDY]);
+            L = Ln;
+            if (c + 1 < n) load_ut(c + 1);
+        }
+        // final state hT = 2^L S~ (transposed back), once every update has completed
+        if (ok && a.hT) {
+            if (!tc::mbar_wait(&bars[FIN], 0)) {
+                ok = false;
+            } else {
+                tc::tc_fence_after();
+                const float eL = ex2f(L);
+#pragma unroll 1
+                for (int d0 = 64 * half; d0 < 64 * half + 64; d0 += 16) {
+                    uint32_t r[16];
+                    tc::tmem_ld16(tc::tmem_addr(tm, j, kS + d0), r);
+                    tc::tmem_wait_ld();
+                    tc::reg_fence(r);
+#pragma unroll
+                    for (int x = 0; x < 16; ++x)
+                        a.hT[(bh * kMaxD + d0 + x) * kMaxD + v] = __uint_as_float(r[x]) * eL;
+                }
+            }
+        }
+    } else {
+        // ---- O warps: o = Oi + 2^L (G S~), rounded to bf16 and stored
+        const int j = warp & 3, v = j * 32 + lane;
+        __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.o);
+        float L = 0.f;
+        float oi[64];
+        auto load_oi = [&](int c) {
+            const float *src = so.O + (blk0 + c) * kC * kMaxD + v;
+#pragma unroll
+            for (int x = 0; x < 64; ++x) oi[x] = src[x * kMaxD];
+        };
+        if (n > 0) load_oi(0);
+        for (int c = 0; c < n; ++c) {
+            const float bsum = so.C[blk0 + c];
+            const bool w = tc::mbar_wait(&bars[WGD + (c & 1)], (c >> 1) & 1);
+            if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+            tc::tc_fence_after();
+            const float eL = ex2f(L);
+            const int64_t tb = (int64_t)c * kC;
+            const int vr = (int)(a.T - tb < kC ? a.T - tb : kC);
+            __nv_bfloat16 *op = o + ((bb * a.T + tb) * a.H + h) * kMaxD + v;
+            const int64_t rs = (int64_t)a.H * kMaxD;
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {   // 16 tokens at a time
+                uint32_t r[16];
+                tc::tmem_ld16(tc::tmem_addr(tm, j, kWG + (c & 1) * 128 + 64 + 16 * q4), r);
+                tc::tmem_wait_ld();
+                tc::reg_fence(r);
+#pragma unroll
+                for (int x = 0; x < 16; ++x) {
+                    const int t = 16 * q4 + x;
+                    if (t < vr) op[t * rs] = __float2bfloat16_rn(oi[t] + eL * __uint_as_float(r[x]));
+                }
+            }
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&bars[WGF + (c & 1)]);   // the accumulator is free
+            float Ln = L + bsum * 1.4426950408889634f;
+            if (!(fabsf(Ln) <= kRenormL2)) Ln = 0.f;   // the U warps rescaled S~ here
+            L = Ln;
+            if (c + 1 < n) load_oi(c + 1);
+        }
+    }
+
+    if (!ok) atomicOr(err, kDevErrTimeout);
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tm, 512);
+    }
+}
+
 constexpr size_t kPrepSmem = (size_t)(2 * kMaxD * kPrepStride + 2 * kC * kC + 5 * kC) * sizeof(float);
 
-template <typename T>
-cudaError_t launch_typed(const GdnArgs &a, int64_t BH, int num_sms, cudaStream_t s) {
-    const int64_t nprep = BH * a.nchunks;
-    cudaError_t e = cudaFuncSetAttribute(gdn_prep_kernel<T>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem);
+// Shared-memory opt-in of the tensor-core scan, once per device.
+std::mutex g_gdn_attr_mu;
+bool g_gdn_attr_done[64];
+
+cudaError_t launch_tc_scan(const GdnArgs &a, int64_t BH, unsigned *err, cudaStream_t s) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    gdn_prep_kernel<T><<<(unsigned)nprep, kThreads, kPrepSmem, s>>>(a);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lock(g_gdn_attr_mu);
+        if (!g_gdn_attr_done[dev]) {
+            e = cudaFuncSetAttribute(gdn_tc_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)gt::ALLOC);
+            if (e != cudaSuccess) return e;
+            g_gdn_attr_done[dev] = true;
+        }
+    }
+    const SoA so(a.ws, a.nblk, kMaxD, kMaxD);
+    CUtensorMap mw, mg, mk;
+    if (!make_2d_map(&mw, so.W, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.nblk * kC, kMaxD, 32, 64,
+                     CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_2d_map(&mg, so.G, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.nblk * kC, kMaxD, 32, 64,
+                     CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_2d_map(&mk, so.Kt, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.nblk * kMaxD, kC, 32, 128,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidResourceHandle;   // a tensor map could not be encoded
+    gdn_tc_scan_kernel<<<(unsigned)BH, gt::kThreadsTC, gt::ALLOC, s>>>(mw, mg, mk, a, err);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_typed(const GdnArgs &a, int64_t BH, int num_sms, unsigned *err,
+                         cudaStream_t s) {
+    const int64_t nprep = BH * a.nchunks;
+    // bf16 I/O at head dims 128: the tensor-core scan (tf32), with the structure-of-arrays
+    // workspace; otherwise the fp32 CUDA-core scan
+    const bool tc = std::is_same<T, __nv_bfloat16>::value && a.Dk == kMaxD && a.Dv == kMaxD;
+    auto prep = tc ? gdn_prep_kernel<T, true> : gdn_prep_kernel<T, false>;
+    cudaError_t e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kPrepSmem);
+    if (e != cudaSuccess) return e;
+    prep<<<(unsigned)nprep, kThreads, kPrepSmem, s>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    if (tc) {
+        e = launch_tc_scan(a, BH, err, s);
+        if (e == cudaSuccess) count_launches(2);
+        return e;
+    }
     // 16 state columns per CTA where 32 would leave SMs idle
     const bool narrow = BH * (a.Dv / 32) < num_sms || a.Dv % 32 != 0;
     if (narrow) {
@@ -587,7 +1006,8 @@ size_t gdn_workspace_bytes(int64_t B, int64_t T, int64_t H, int64_t Dk, int64_t 
     return (size_t)(B * H * nchunks) * (size_t)WsLayout((int)Dk, (int)Dv).total * sizeof(float);
 }
 
-cudaError_t launch_gdn(const GdnProblem &p, void *ws, int num_sms, cudaStream_t s) {
+cudaError_t launch_gdn(const GdnProblem &p, void *ws, int num_sms, unsigned *err,
+                       cudaStream_t s) {
     GdnArgs a;
     a.q = p.q;
     a.k = p.k;
@@ -605,8 +1025,9 @@ cudaError_t launch_gdn(const GdnProblem &p, void *ws, int num_sms, cudaStream_t 
     a.nchunks = (int)((p.T + kC - 1) / kC);
     a.ws = static_cast<float *>(ws);
     const int64_t BH = p.B * p.H;
-    return p.io == 0 /* bf16 */ ? launch_typed<__nv_bfloat16>(a, BH, num_sms, s)
-                     : launch_typed<float>(a, BH, num_sms, s);
+    a.nblk = BH * a.nchunks;
+    return p.io == 0 /* bf16 */ ? launch_typed<__nv_bfloat16>(a, BH, num_sms, err, s)
+                     : launch_typed<float>(a, BH, num_sms, err, s);
 }
 
 }  // namespace gla

@@ -485,7 +485,8 @@ gla_status gdn_fwd(const void *q, const void *k, const void *v, const float *g_l
         if (rc != GLA_OK) return rc;
     }
     gla::GdnProblem p{q, k, v, g_log, beta, scale, h0, o, hT, B, T, H, Dk, Dv, io};
-    const cudaError_t e = gla::launch_gdn(p, ws, st->num_sms, reinterpret_cast<cudaStream_t>(stream));
+    const cudaError_t e = gla::launch_gdn(p, ws, st->num_sms, st->err_word,
+                                          reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) {
         cudaGetLastError();
         set_detail("gated delta rule launch", e);

@@ -82,6 +82,7 @@ struct GdnProblem {
 };
 bool gdn_supported(int64_t Dk, int64_t Dv);
 size_t gdn_workspace_bytes(int64_t B, int64_t T, int64_t H, int64_t Dk, int64_t Dv);
-cudaError_t launch_gdn(const GdnProblem &p, void *ws, int num_sms, cudaStream_t s);
+cudaError_t launch_gdn(const GdnProblem &p, void *ws, int num_sms, unsigned int *dev_err,
+                       cudaStream_t s);
 
 }  // namespace gla

@@ -120,7 +120,9 @@ constexpr uint32_t kColO = 320;    // O^T = S~^T Q'^T + V^T P^T, 64 columns
 //   g ring (2 slots): the chunk's log-gates, [64 tokens][128] f32, loaded by TMA and
 //     released as soon as the gate warps have scaled the chunk.
 namespace om {
-constexpr int NQ = 3;                   // q/k/v stages
+constexpr int NQ = 3;                   // q/k/v stages (per-key gates)
+constexpr int NQS = 4;                  // q/k/v stages with a scalar gate: the fourth stage
+                                        // takes the log-gate ring's space
 constexpr int NG = 2;                   // log-gate slots
 constexpr int NR = 4;                   // per-chunk ring of scales and flags (written by the
                                         // gates of c, read before O(c) completes)
@@ -139,12 +141,15 @@ constexpr uint32_t NBAR = 24;
 constexpr uint32_t TSLOT = BAR + NBAR * 8;
 constexpr uint32_t ALLOC = TSLOT + 16 + 1024;
 static_assert(ALLOC <= 232448, "output kernel shared memory");
+static_assert(NQS * QSTAGE + 512 <= P, "scalar-gate stages and factors fit below the P tile");
+constexpr uint32_t FAC = NQS * QSTAGE;  // [64] float2 per-token factors (scalar gate)
 }  // namespace om
 
 // mbarrier indices of the output kernel
+// (q/k/v rings of up to 4 stages: 4 with a scalar gate, whose log-gate ring is unused)
 enum {
-    QFULL = 0, QEMPTY = 3, GFULL = 6, GEMPTY = 8, GDONE = 10, PFULL = 13, PFREE = 14, PBF = 15,
-    SREADY = 16, UDONE = 17, OFULL = 18, OFREE = 19, FIN = 20,
+    QFULL = 0, QEMPTY = 4, GFULL = 8, GEMPTY = 10, GDONE = 12, PFULL = 16, PFREE = 17, PBF = 18,
+    SREADY = 19, UDONE = 20, OFULL = 21, OFREE = 22, FIN = 23,
 };
 static_assert(FIN < (int)om::NBAR, "output kernel barrier map");
 
@@ -298,6 +303,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg,
                   const OutArgs a) {
     using namespace om;
+    constexpr int NQ = kScalar ? NQS : om::NQ;   // q/k/v stages of this instance
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = align1024(smraw);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + BAR);
@@ -848,6 +854,32 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             L0 = ext ? 0.f : Lq0 + B0;
             L1 = ext ? 0.f : Lq1 + B1;
             if (gt == 0) TRACE_OUT(18, c);
+            // scalar gate: the factors are the same in every key dimension, so the 64 token
+            // threads compute them once per chunk (two ex2 each) for pass 2 to multiply by; the
+            // running sum and the range offset are formed exactly as the key-pair threads form
+            // them, so the numbers are the same. The barrier after the stage wait below
+            // publishes them.
+            float2 *fac = reinterpret_cast<float2 *>(sm + FAC);
+            if (kScalar && gt < kC) {
+                const int pt = gt / kGatePart, tbt = pt * kGatePart;
+                const float *gc = gsc + (c & 1) * kC;
+                float rt = 0.f;
+                for (int u = tbt; u <= gt; ++u) rt = fmaf(gc[u], kLog2e, rt);
+                float Bt = 0.f, offt = 0.f;
+#pragma unroll
+                for (int q = 0; q < kGateParts; ++q) {
+                    const float tq = xch[q * kD];
+                    if (q == pt) offt = Bt;
+                    Bt = q == 0 ? tq : Bt + tq;
+                }
+                if (!ext) {
+                    const float eq = offt + Lq0 + lsc, ek = -(offt + Lq0);
+                    fac[gt] = make_float2(ex2(rt + eq), ex2(ek - rt));
+                } else {
+                    const float bt = offt + rt;
+                    fac[gt] = make_float2(sc * ex2(bt), ex2(B0 - bt));
+                }
+            }
             w = mbar_wait(&bars[QFULL + qs], par(c / NQ));
             if (named_bar_or(1, kGateThreads, !w)) { ok = false; break; }
             // ring entries of chunk c: written only now, after the stage of chunk c arrived
@@ -889,13 +921,13 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
 #pragma unroll
                     for (int x = 0; x < kGateBlock; ++x) {
                         const float2 qf = unpack_bf16(qv[x]), kf = unpack_bf16(kv[x]);
-                        r0 = fmaf(gv[x].x, kLog2e, r0);
                         if (kScalar) {
-                            // one gate for every key dimension: both columns share the factors
-                            const float fq = ex2(r0 + eq0), fk = ex2(ek0 - r0);
-                            qv[x] = pack_bf16(qf.x * fq, qf.y * fq);
-                            kv[x] = pack_bf16(kf.x * fk, kf.y * fk);
+                            // one gate for every key dimension: the token's precomputed factors
+                            const float2 f = fac[tb + t0 + x];
+                            qv[x] = pack_bf16(qf.x * f.x, qf.y * f.x);
+                            kv[x] = pack_bf16(kf.x * f.y, kf.y * f.y);
                         } else {
+                            r0 = fmaf(gv[x].x, kLog2e, r0);
                             r1 = fmaf(gv[x].y, kLog2e, r1);
                             qv[x] = pack_bf16(qf.x * ex2(r0 + eq0), qf.y * ex2(r1 + eq1));
                             kv[x] = pack_bf16(kf.x * ex2(ek0 - r0), kf.y * ex2(ek1 - r1));
@@ -924,12 +956,18 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     }
 #pragma unroll
                     for (int x = 0; x < kGateBlock; ++x) {
-                        r0 = fmaf(gv[x].x, kLog2e, r0);
-                        r1 = fmaf(gv[x].y, kLog2e, r1);
-                        const float b0 = off0 + r0, b1 = off1 + r1;
                         const float2 qf = unpack_bf16(qv[x]), kf = unpack_bf16(kv[x]);
-                        qv[x] = pack_bf16(sc * qf.x * ex2(b0), sc * qf.y * ex2(b1));
-                        kv[x] = pack_bf16(kf.x * ex2(B0 - b0), kf.y * ex2(B1 - b1));
+                        if (kScalar) {
+                            const float2 f = fac[tb + t0 + x];
+                            qv[x] = pack_bf16(qf.x * f.x, qf.y * f.x);
+                            kv[x] = pack_bf16(kf.x * f.y, kf.y * f.y);
+                        } else {
+                            r0 = fmaf(gv[x].x, kLog2e, r0);
+                            r1 = fmaf(gv[x].y, kLog2e, r1);
+                            const float b0 = off0 + r0, b1 = off1 + r1;
+                            qv[x] = pack_bf16(sc * qf.x * ex2(b0), sc * qf.y * ex2(b1));
+                            kv[x] = pack_bf16(kf.x * ex2(B0 - b0), kf.y * ex2(B1 - b1));
+                        }
                     }
 #pragma unroll
                     for (int x = 0; x < kGateBlock; ++x) {

@@ -45,4 +45,19 @@ inline bool make_bthd_map(CUtensorMap *m, const void *base, CUtensorMapDataType 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Map of a row-major [rows, cols] matrix (cols innermost) with a box of (box_cols, box_rows).
+inline bool make_2d_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt,
+                        uint32_t elem_bytes, int64_t rows, int64_t cols, uint32_t box_cols,
+                        uint32_t box_rows, CUtensorMapSwizzle swz) {
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(cols * elem_bytes)};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace gla
