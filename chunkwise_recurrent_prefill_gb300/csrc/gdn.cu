@@ -651,6 +651,11 @@ __device__ __forceinline__ float ex2f(float x) {
     return y;
 }
 
+// Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2.
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // 2-D tiled load (x = inner coordinate, y = row) into shared memory.
 __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, uint64_t *bar, int x,
                                             int y) {
@@ -720,8 +725,19 @@ gdn_tc_scan_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant
         // ---- TMA producer: [W | G] slabs and Kh^T boxes of each chunk
         if (lane == 0) {
             int issued = 0;
+            // the fp32 Ut and Oi tiles the U and O warps read with plain loads: brought into L2
+            // two chunks ahead, so their loads do not wait on DRAM
+            constexpr uint32_t kTile = kC * kMaxD * sizeof(float);
+            for (int c = 0; c < 2 && c < n; ++c) {
+                prefetch_l2(so.U + (blk0 + c) * kC * kMaxD, kTile);
+                prefetch_l2(so.O + (blk0 + c) * kC * kMaxD, kTile);
+            }
             for (int c = 0; c < n && ok; ++c) {
                 const int st = c % kStages;
+                if (c + 2 < n) {
+                    prefetch_l2(so.U + (blk0 + c + 2) * kC * kMaxD, kTile);
+                    prefetch_l2(so.O + (blk0 + c + 2) * kC * kMaxD, kTile);
+                }
                 if (c >= kStages && !tc::mbar_wait(&bars[EMPTY + st], ((c / kStages) - 1) & 1)) {
                     ok = false;
                     break;
