@@ -111,7 +111,7 @@ constexpr int kPieces = kC * kMaxD / 4 / kThreads;   // 4-element pieces of a ti
 
 // ---------------------------------------------------------------------------------------
 // Chunk-parallel part: one CTA per (batch, head, chunk).
-template <typename T, bool kSoA>
+template <typename T>
 __global__ void __launch_bounds__(kThreads, 2) gdn_prep_kernel(GdnArgs a) {
     extern __shared__ __align__(16) float smp[];
     float *Qt = smp;                                  // [Dk][kPrepStride]; later v [64][Dv]
@@ -136,7 +136,6 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prep_kernel(GdnArgs a) {
     auto row = [&](int j) -> int64_t { return (bb * a.T + t0 + j) * a.H + h; };   // token row
     const WsLayout L(Dk, Dv);
     float *ws = a.ws + blk * L.total;
-    const SoA so(a.ws, a.nblk, Dk, Dv);
 
     // q and k in 4-element pieces (piece p: row j = p % 64, key dims 4 (p / 64) ..), all
     // loads of a thread in flight at once; then transposed into [d][j]. The 32 lanes of a
@@ -182,26 +181,17 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prep_kernel(GdnArgs a) {
         ek[tid] = expf(bs[kC - 1] - bs[tid]);
     }
     __syncthreads();
-    if (kSoA) {
-        // Kh transposed, [d][j], from the transposed k tile; the chunk's summed log-gate
-        for (int idx = tid; idx < Dk * kC; idx += kThreads) {
-            const int d = idx / kC, j = idx % kC;
-            so.Kt[(blk * Dk + d) * kC + j] = ek[j] * Kt[d * kPrepStride + j];
-        }
-        if (tid == 0) so.C[blk] = bs[kC - 1];
-    } else {
-        // Kh = exp(b_63 - b_j) k_j straight from the pieces in registers; exp(b_63)
+    // Kh = exp(b_63 - b_j) k_j straight from the pieces in registers; exp(b_63)
 #pragma unroll
-        for (int it = 0; it < kPieces; ++it) {
-            const int p = tid + kThreads * it, j = p & (kC - 1), c4 = p >> 6;
-            if (p < npk) {
-                const float e = ek[j];
-                *reinterpret_cast<float4 *>(ws + L.oK + (int64_t)j * Dk + 4 * c4) =
-                    make_float4(e * kr[it].x, e * kr[it].y, e * kr[it].z, e * kr[it].w);
-            }
+    for (int it = 0; it < kPieces; ++it) {
+        const int p = tid + kThreads * it, j = p & (kC - 1), c4 = p >> 6;
+        if (p < npk) {
+            const float e = ek[j];
+            *reinterpret_cast<float4 *>(ws + L.oK + (int64_t)j * Dk + 4 * c4) =
+                make_float4(e * kr[it].x, e * kr[it].y, e * kr[it].z, e * kr[it].w);
         }
-        if (tid < 4) ws[L.oC + tid] = tid == 0 ? eb[kC - 1] : 0.f;
     }
+    if (tid < 4) ws[L.oC + tid] = tid == 0 ? eb[kC - 1] : 0.f;
 
     // K K^T and Q K^T, one 4 x 4 tile of each per thread: rows 4 mg .., columns 4 ng ..
     {
@@ -245,13 +235,8 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prep_kernel(GdnArgs a) {
     // Qh = scale exp(b_i) q_i (transposed) goes to the workspace, where it becomes G below;
     // then the q tile's space takes v, rows j, for the right-hand sides of the solve
     for (int idx = tid; idx < Dk * kC; idx += kThreads) {
-        if (kSoA) {
-            const int i = idx / Dk, d = idx % Dk;
-            so.G[(blk * kC + i) * Dk + d] = a.scale * eb[i] * Qt[d * kPrepStride + i];
-        } else {
-            const int d = idx / kC, i = idx % kC;
-            ws[L.oG + idx] = a.scale * eb[i] * Qt[d * kPrepStride + i];
-        }
+        const int d = idx / kC, i = idx % kC;
+        ws[L.oG + idx] = a.scale * eb[i] * Qt[d * kPrepStride + i];
     }
     __syncthreads();
     float *Vs = Qt;   // [64][Dv]
@@ -298,18 +283,12 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prep_kernel(GdnArgs a) {
             x[j] = r - (s0 + s1);
         }
         if (isk) {
-            if (kSoA) {
-                float *w = so.W + blk * kC * Dk + col;
+            float *wt = ws + L.oW + (int64_t)col * kC;
 #pragma unroll
-                for (int j = 0; j < kC; ++j) w[(int64_t)j * Dk] = x[j];
-            } else {
-                float *wt = ws + L.oW + (int64_t)col * kC;
-#pragma unroll
-                for (int j = 0; j < kC; j += 4)
-                    *reinterpret_cast<float4 *>(wt + j) = make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
-            }
+            for (int j = 0; j < kC; j += 4)
+                *reinterpret_cast<float4 *>(wt + j) = make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
         } else {
-            float *ut = kSoA ? so.U + blk * kC * Dv + cv : ws + L.oU + cv;
+            float *ut = ws + L.oU + cv;
 #pragma unroll
             for (int j = 0; j < kC; ++j) ut[(int64_t)j * Dv] = x[j];
         }
@@ -332,17 +311,11 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prep_kernel(GdnArgs a) {
                 y[r] = s0 + s1;
             }
             if (isk) {   // G = Qh - P W, in place of Qh (this thread's own column of it)
-                if (kSoA) {
-                    float *gp = so.G + (blk * kC + i0) * Dk + col;
-#pragma unroll
-                    for (int r = 0; r < 4; ++r) gp[(int64_t)r * Dk] -= y[r];
-                } else {
-                    float4 *gp = reinterpret_cast<float4 *>(ws + L.oG + (int64_t)col * kC + i0);
-                    const float4 qh = *gp;
-                    *gp = make_float4(qh.x - y[0], qh.y - y[1], qh.z - y[2], qh.w - y[3]);
-                }
+                float4 *gp = reinterpret_cast<float4 *>(ws + L.oG + (int64_t)col * kC + i0);
+                const float4 qh = *gp;
+                *gp = make_float4(qh.x - y[0], qh.y - y[1], qh.z - y[2], qh.w - y[3]);
             } else {
-                float *op = kSoA ? so.O + blk * kC * Dv + cv : ws + L.oO + cv;
+                float *op = ws + L.oO + cv;
 #pragma unroll
                 for (int r = 0; r < 4; ++r) op[(int64_t)(i0 + r) * Dv] = y[r];
             }
@@ -621,7 +594,7 @@ constexpr uint32_t ALLOC = TSLOT + 16 + 1024;
 constexpr uint32_t kS = 0;       // S~^T, 128 columns
 constexpr uint32_t kWG = 128;    // [W S~ | G S~]^T, 2 x 128 columns (double buffered)
 constexpr uint32_t kU = 384;     // scaled U^T (A operand of the update), 64 columns
-constexpr int kThreadsTC = 14 * 32;   // producer, MMA issuer, 8 U warps, 4 O warps
+constexpr int kThreadsTC = 18 * 32;   // producer, MMA issuer, 8 U warps, 8 O warps
 constexpr float kRenormL2 = 60.f;
 enum { FULL = 0, EMPTY = 2, WGD = 4, WGF = 6, URDY = 8, FIN = 9 };
 }  // namespace gt
@@ -687,7 +660,7 @@ gdn_tc_scan_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant
             tc::mbar_init(&bars[FULL + i], 1);
             tc::mbar_init(&bars[EMPTY + i], 1);
             tc::mbar_init(&bars[WGD + i], 1);
-            tc::mbar_init(&bars[WGF + i], 4);
+            tc::mbar_init(&bars[WGF + i], 8);
         }
         tc::mbar_init(&bars[URDY], 8);
         tc::mbar_init(&bars[FIN], 1);
@@ -888,14 +861,14 @@ gdn_tc_scan_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant
         }
     } else {
         // ---- O warps: o = Oi + 2^L (G S~), rounded to bf16 and stored
-        const int j = warp & 3, v = j * 32 + lane;
+        const int j = warp & 3, v = j * 32 + lane, th = 32 * ((warp - 10) >> 2);
         __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.o);
         float L = 0.f;
-        float oi[64];
+        float oi[32];
         auto load_oi = [&](int c) {
-            const float *src = so.O + (blk0 + c) * kC * kMaxD + v;
+            const float *src = so.O + ((blk0 + c) * kC + th) * kMaxD + v;
 #pragma unroll
-            for (int x = 0; x < 64; ++x) oi[x] = src[x * kMaxD];
+            for (int x = 0; x < 32; ++x) oi[x] = src[x * kMaxD];
         };
         if (n > 0) load_oi(0);
         for (int c = 0; c < n; ++c) {
@@ -908,16 +881,22 @@ gdn_tc_scan_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant
             const int vr = (int)(a.T - tb < kC ? a.T - tb : kC);
             __nv_bfloat16 *op = o + ((bb * a.T + tb) * a.H + h) * kMaxD + v;
             const int64_t rs = (int64_t)a.H * kMaxD;
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {   // 16 tokens at a time
-                uint32_t r[16];
-                tc::tmem_ld16(tc::tmem_addr(tm, j, kWG + (c & 1) * 128 + 64 + 16 * q4), r);
+            {
+                uint32_t r0[16], r1[16];
+                tc::tmem_ld16(tc::tmem_addr(tm, j, kWG + (c & 1) * 128 + 64 + th), r0);
+                tc::tmem_ld16(tc::tmem_addr(tm, j, kWG + (c & 1) * 128 + 64 + th + 16), r1);
                 tc::tmem_wait_ld();
-                tc::reg_fence(r);
+                tc::reg_fence(r0);
+                tc::reg_fence(r1);
 #pragma unroll
                 for (int x = 0; x < 16; ++x) {
-                    const int t = 16 * q4 + x;
-                    if (t < vr) op[t * rs] = __float2bfloat16_rn(oi[t] + eL * __uint_as_float(r[x]));
+                    const int t = th + x;
+                    if (t < vr) op[t * rs] = __float2bfloat16_rn(oi[x] + eL * __uint_as_float(r0[x]));
+                }
+#pragma unroll
+                for (int x = 0; x < 16; ++x) {
+                    const int t = th + 16 + x;
+                    if (t < vr) op[t * rs] = __float2bfloat16_rn(oi[16 + x] + eL * __uint_as_float(r1[x]));
                 }
             }
             tc::tc_fence_before();
@@ -937,6 +916,492 @@ gdn_tc_scan_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant
         tc::tc_fence_after();
         tc::tmem_dealloc(tm, 512);
     }
+}
+
+// ---------------------------------------------------------------------------------------
+// Tensor-core prep (bf16 I/O, Dk = Dv = 128): one CTA per (batch, head, chunk), two CTAs per
+// SM. The chunk's contractions run on tcgen05 with bf16 operands and fp32 accumulation in
+// TMEM; the triangular inverse stays in fp32 on the CUDA cores:
+//   [K K^T ; Q K^T]                       (K, Q exact in bf16)       -> A, P
+//   T = (I + A)^-1                        forward substitution, one column per thread
+//   [P Tw | P Tu]^T = [Tw | Tu]^T P^T     Tw = T diag(beta e^b),  Tu = T diag(beta)
+//   [W ; -P W] = [Tw ; -P Tw] K           (W = Tw K solves (I + A) W = diag(beta e^b) K)
+//   [Ut ; Oi]  = [Tu ;  P Tu] V           (Ut solves (I + A) Ut = diag(beta) V, Oi = P Ut)
+// and G = scale diag(e^b) Q - P W is finished in the epilogue. Each fp32 coefficient matrix
+// enters the tensor cores as two bf16 operands, hi = bf16(x) and lo = bf16(x - hi), and a
+// product of two such matrices takes hi*hi + lo*hi + hi*lo: about 16 significant bits (the
+// scan then reads these tiles as tf32, 11 bits). The results leave through 128B-swizzled
+// shared-memory staging and TMA tensor stores, in the structure-of-arrays workspace layout.
+namespace gp {
+// shared memory (bytes from the 1024-aligned base); every operand tile is 64 rows x 128 B,
+// 128B-swizzled (8 KB)
+constexpr uint32_t KQ = 0;          // k d0..63 | q d0..63 | k d64..127 | q d64..127
+constexpr uint32_t V = 32768;       // v d0..63 | v d64..127
+constexpr uint32_t TT = 49152;      // T (fp32) and merge scratch; then
+                                    // Tw^T hi | Tu^T hi | Tw^T lo | Tu^T lo   (row m, column j)
+constexpr uint32_t AP = 81920;      // A (fp32, stride kAStride); then P hi | lo; then
+                                    // (-P Tw)^T hi | lo; then (P Tu)^T hi | lo (row m, column i)
+constexpr uint32_t SMALL = AP + 18432;   // b, beta, e^b, beta e^b, e^(b63 - b), b log2(e)
+constexpr uint32_t BAR = SMALL + 6 * 256;
+constexpr uint32_t NBAR = 5;
+constexpr uint32_t TSLOT = BAR + NBAR * 8;
+constexpr uint32_t ALLOC = TSLOT + 16 + 1024;
+constexpr uint32_t ST0 = 32768, ST1 = 65536;   // fp32 output staging once the MMAs are done
+constexpr int kAStride = 68;
+constexpr int kThreadsP = 256;
+// TMEM columns (256 allocated): [KK^T ; QK^T] at 0 (64 columns), [P Tw | P Tu]^T at 64
+// (64), [W ; -P W] at 128 (128), [Ut ; Oi] at 0 (128, after the first two are read)
+constexpr uint32_t kD1 = 0, kD2 = 64, kD3 = 128, kD4 = 0;
+enum { LOAD = 0, M1 = 1, M2 = 2, M3 = 3, M4 = 4 };
+}  // namespace gp
+
+// Load 64 consecutive TMEM columns of this warp's lane quarter as fp32 (one wait).
+__device__ __forceinline__ void tmem_ld64f(uint32_t taddr, float (&out)[64]) {
+    uint32_t r0[16], r1[16], r2[16], r3[16];
+    tc::tmem_ld16(taddr, r0);
+    tc::tmem_ld16(taddr + 16, r1);
+    tc::tmem_ld16(taddr + 32, r2);
+    tc::tmem_ld16(taddr + 48, r3);
+    tc::tmem_wait_ld();
+    tc::reg_fence(r0);
+    tc::reg_fence(r1);
+    tc::reg_fence(r2);
+    tc::reg_fence(r3);
+#pragma unroll
+    for (int x = 0; x < 16; ++x) {
+        out[x] = __uint_as_float(r0[x]);
+        out[16 + x] = __uint_as_float(r1[x]);
+        out[32 + x] = __uint_as_float(r2[x]);
+        out[48 + x] = __uint_as_float(r3[x]);
+    }
+}
+
+// x -> (hi, lo) bf16 pairs with hi = bf16(x), lo = bf16(x - hi), two elements per word
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+    hi = tc::pack_bf16(x0, x1);
+    const float2 f = tc::unpack_bf16(hi);
+    lo = tc::pack_bf16(x0 - f.x, x1 - f.y);
+}
+
+// Row `row` of a 64-column bf16 operand tile pair (hi at `hi`, lo at `lo`, 128B-swizzled):
+// the 64 values x[0..63] scaled by f.
+__device__ __forceinline__ void store_split_row(uint8_t *hi, uint8_t *lo, int row,
+                                                const float (&x)[64], float f) {
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) {
+        uint32_t h[4], l[4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) split2(f * x[8 * ch + 2 * p], f * x[8 * ch + 2 * p + 1], h[p], l[p]);
+        const uint32_t off = tc::sw128_offset(row, 8 * ch);
+        *reinterpret_cast<uint4 *>(hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4 *>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+    }
+}
+
+// 64 fp32 values of row `row` into a staged [rows x 128] fp32 tile held as four
+// 128B-swizzled boxes of 32 columns (8 KB each for 64 rows), columns c0 .. c0 + 63.
+__device__ __forceinline__ void stage_row64(uint8_t *tile, int row, int c0, const float (&v)[64]) {
+#pragma unroll
+    for (int c4 = 0; c4 < 16; ++c4) {
+        const int col = c0 + 4 * c4, box = col >> 5, ch = (col & 31) >> 2;
+        *reinterpret_cast<float4 *>(tile + box * 8192 + row * 128 + ((ch ^ (row & 7)) << 4)) =
+            make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
+    }
+}
+
+// 2-D tiled bulk tensor store from shared memory (bulk-group completion).
+__device__ __forceinline__ void tma_store_2d(const void *tmap, const void *src, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(tmap)),
+        "r"(tc::smem_u32(src)), "r"(x), "r"(y)
+        : "memory");
+}
+
+__global__ void __launch_bounds__(gp::kThreadsP, 2)
+gdn_tc_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tw,
+                   const __grid_constant__ CUtensorMap tg, const __grid_constant__ CUtensorMap tu,
+                   const __grid_constant__ CUtensorMap to, GdnArgs a, unsigned *err) {
+    using namespace gp;
+    extern __shared__ uint8_t smraw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) &
+                                              ~uintptr_t(1023));
+    float *bs = reinterpret_cast<float *>(sm + SMALL);   // cumulative log-gate b_j
+    float *be = bs + kC;                                 // beta_j
+    float *eb = be + kC;                                 // e^(b_j)
+    float *bg = eb + kC;                                 // beta_j e^(b_j)
+    float *ek = bg + kC;                                 // e^(b_63 - b_j)
+    float *bl = ek + kC;                                 // b_j log2(e)
+    float *As = reinterpret_cast<float *>(sm + AP);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + BAR);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + TSLOT);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t blk = blockIdx.x;
+    const int c = (int)(blk % a.nchunks);
+    const int64_t bh = blk / a.nchunks;
+    const int64_t bb = bh / a.H, h = bh % a.H;
+    const int64_t t0 = (int64_t)c * kC;
+    const int nval = (int)(a.T - t0 < kC ? a.T - t0 : kC);
+    const uint32_t base = tc::smem_u32(sm);
+    const SoA so(a.ws, a.nblk, kMaxD, kMaxD);
+    bool ok = true;
+
+    if (warp == 1) {
+        if (lane == 0) {   // barriers, then the q, k, v tiles (rows past the end read as zero)
+            for (int i = 0; i < (int)NBAR; ++i) tc::mbar_init(&bars[i], 1);
+            tc::fence_mbar_init();
+            uint64_t *lb = &bars[LOAD];
+            tc::mbar_arrive_expect_tx(lb, 6 * 8192);
+            const int tt = (int)t0, hh = (int)h, b4 = (int)bb;
+            tc::tma_load_4d(sm + KQ, &tk, lb, 0, hh, tt, b4);
+            tc::tma_load_4d(sm + KQ + 8192, &tq, lb, 0, hh, tt, b4);
+            tc::tma_load_4d(sm + KQ + 16384, &tk, lb, 64, hh, tt, b4);
+            tc::tma_load_4d(sm + KQ + 24576, &tq, lb, 64, hh, tt, b4);
+            tc::tma_load_4d(sm + V, &tv, lb, 0, hh, tt, b4);
+            tc::tma_load_4d(sm + V + 8192, &tv, lb, 64, hh, tt, b4);
+        }
+        // gates, two tokens per lane; rows past the sequence end decay by nothing and write
+        // nothing. Inclusive cumulative sum: pair sums, then a warp scan.
+        const int j0 = 2 * lane;
+        float g0 = 0.f, g1 = 0.f, be0 = 0.f, be1 = 0.f;
+        const int64_t r0 = (bb * a.T + t0 + j0) * a.H + h;
+        if (j0 < nval) { g0 = a.g[r0]; be0 = a.beta[r0]; }
+        if (j0 + 1 < nval) { g1 = a.g[r0 + a.H]; be1 = a.beta[r0 + a.H]; }
+        float inc = g0 + g1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += y;
+        }
+        float ex = __shfl_up_sync(0xffffffffu, inc, 1);
+        if (lane == 0) ex = 0.f;
+        const float c0 = ex + g0, c1 = c0 + g1;
+        const float l63 = __shfl_sync(0xffffffffu, c1, 31) * 1.4426950408889634f;
+        const float l0 = c0 * 1.4426950408889634f, l1 = c1 * 1.4426950408889634f;
+        bs[j0] = c0;
+        bs[j0 + 1] = c1;
+        be[j0] = be0;
+        be[j0 + 1] = be1;
+        bl[j0] = l0;
+        bl[j0 + 1] = l1;
+        const float e0 = ex2f(l0), e1 = ex2f(l1);
+        eb[j0] = e0;
+        eb[j0 + 1] = e1;
+        bg[j0] = be0 * e0;
+        bg[j0 + 1] = be1 * e1;
+        ek[j0] = ex2f(l63 - l0);
+        ek[j0 + 1] = ex2f(l63 - l1);
+    }
+    if (warp == 0) tc::tmem_alloc(tslot, 256);
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tm = *tslot;
+    if (warp == 0) {   // [K ; Q] K^T: M = 128 (k rows, then q rows), N = 64, K = 128 key dims
+        const bool w = tc::mbar_wait(&bars[LOAD], 0);
+        ok = __all_sync(0xffffffffu, w);
+        tc::tc_fence_after();
+        if (tc::elect_one()) {
+            const uint32_t id1 = tc::idesc_bf16(128, 64, 0, 0);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t off = base + KQ + (kk >> 2) * 16384 + (kk & 3) * 32;
+                tc::mma_ss(tm + kD1, tc::smem_desc(off, 16, 1024), tc::smem_desc(off, 16, 1024),
+                           id1, kk > 0);
+            }
+            tc::mma_commit(&bars[M1]);
+        }
+        __syncwarp();
+    }
+
+    // one 64-value row per thread of warps 0..3, reused through the steps below:
+    // the A row or P row, then the column of T (threads 0..63), then a row of [P Tw | P Tu]^T
+    float w[64];
+    if (warp < 4) {
+        ok &= tc::mbar_wait(&bars[M1], 0);
+        tc::tc_fence_after();
+        tmem_ld64f(tc::tmem_addr(tm, warp, kD1), w);
+        const int r = tid & (kC - 1);
+        const float lr = bl[r];
+        if (tid < kC) {
+            // A_rm = beta_r e^(b_r - b_m) k_r.k_m for m < r
+            const float sr = be[r];
+            float *ar = As + r * kAStride;
+#pragma unroll
+            for (int m4 = 0; m4 < 16; ++m4) {
+                float av[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int m = 4 * m4 + e;
+                    av[e] = m < r ? sr * ex2f(lr - bl[m]) * w[m] : 0.f;
+                }
+                *reinterpret_cast<float4 *>(ar + 4 * m4) = make_float4(av[0], av[1], av[2], av[3]);
+            }
+        } else {
+            // P_rm = scale e^(b_r - b_m) q_r.k_m for m <= r (kept in registers)
+#pragma unroll
+            for (int m = 0; m < kC; ++m) w[m] = m <= r ? a.scale * ex2f(lr - bl[m]) * w[m] : 0.f;
+        }
+        tc::tc_fence_before();
+        tc::named_bar_sync(1, 128);
+
+        // T = (I + A)^-1 (unit lower triangular) in shared memory, blocked: the four 16 x 16
+        // diagonal blocks by forward substitution, then pairs merged into 32 x 32 and 64 x 64
+        // inverses through  [L0 0 ; A10 L1]^-1 = [L0^-1 0 ; -L1^-1 A10 L0^-1  L1^-1].
+        float *Ts = reinterpret_cast<float *>(sm + TT);
+        float *Ys = Ts + kC * kAStride;
+        if (tid < kC) {
+            const int b0 = (tid >> 4) * 16, m = tid & 15;
+            float x[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const float *ar = As + (b0 + j) * kAStride + b0;
+                float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                for (int l = 0; l + 3 < j; l += 4) {
+                    const float4 av = *reinterpret_cast<const float4 *>(ar + l);
+                    s0 = fmaf(av.x, x[l], s0);
+                    s1 = fmaf(av.y, x[l + 1], s1);
+                    s0 = fmaf(av.z, x[l + 2], s0);
+                    s1 = fmaf(av.w, x[l + 3], s1);
+                }
+#pragma unroll
+                for (int l = j & ~3; l < j; ++l) s0 = fmaf(ar[l], x[l], s0);
+                x[j] = (j == m ? 1.f : 0.f) - (s0 + s1);
+                Ts[(b0 + j) * kAStride + b0 + m] = x[j];
+                // the zero block right of an even diagonal block, read by the 64 x 64 merge
+                if (!(b0 & 16)) Ts[(b0 + j) * kAStride + b0 + 16 + m] = 0.f;
+            }
+        }
+        tc::named_bar_sync(1, 128);
+        {   // 16 -> 32: rows 16 .. 31 of each 32-block, columns 0 .. 15 (4 rows per thread)
+            const int pr = (tid >> 6) * 32, i0 = ((tid >> 4) & 3) * 4, m = tid & 15;
+            float y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int l = 0; l < 16; ++l) {
+                const float tv = Ts[(pr + l) * kAStride + pr + m];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) y[e] = fmaf(As[(pr + 16 + i0 + e) * kAStride + pr + l], tv, y[e]);
+            }
+            float *yp = Ys + (tid >> 6) * 16 * 20;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) yp[(i0 + e) * 20 + m] = y[e];
+            tc::named_bar_sync(1, 128);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) y[e] = 0.f;
+#pragma unroll
+            for (int l = 0; l < 16; ++l) {
+                const float yv = yp[l * 20 + m];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    y[e] = fmaf(Ts[(pr + 16 + i0 + e) * kAStride + pr + 16 + l], yv, y[e]);
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) Ts[(pr + 16 + i0 + e) * kAStride + pr + m] = -y[e];
+        }
+        tc::named_bar_sync(1, 128);
+        {   // 32 -> 64: rows 32 .. 63, columns 0 .. 31 (8 rows per thread)
+            const int i0 = (tid >> 5) * 8, m = tid & 31;
+            float y[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) y[e] = 0.f;
+#pragma unroll 4
+            for (int l = 0; l < 32; l += 4) {
+                const float t0v = Ts[l * kAStride + m], t1v = Ts[(l + 1) * kAStride + m];
+                const float t2v = Ts[(l + 2) * kAStride + m], t3v = Ts[(l + 3) * kAStride + m];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float4 av = *reinterpret_cast<const float4 *>(As + (32 + i0 + e) * kAStride + l);
+                    y[e] = fmaf(av.x, t0v, fmaf(av.y, t1v, fmaf(av.z, t2v, fmaf(av.w, t3v, y[e]))));
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) Ys[(i0 + e) * 36 + m] = y[e];
+            tc::named_bar_sync(1, 128);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) y[e] = 0.f;
+#pragma unroll 4
+            for (int l = 0; l < 32; l += 4) {
+                const float y0 = Ys[l * 36 + m], y1 = Ys[(l + 1) * 36 + m];
+                const float y2 = Ys[(l + 2) * 36 + m], y3 = Ys[(l + 3) * 36 + m];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float4 tv = *reinterpret_cast<const float4 *>(Ts + (32 + i0 + e) * kAStride + 32 + l);
+                    y[e] = fmaf(tv.x, y0, fmaf(tv.y, y1, fmaf(tv.z, y2, fmaf(tv.w, y3, y[e]))));
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) Ts[(32 + i0 + e) * kAStride + m] = -y[e];
+        }
+        tc::named_bar_sync(1, 128);
+        if (tid < kC) {   // column m of T
+#pragma unroll
+            for (int j = 0; j < kC; ++j) w[j] = j >= tid ? Ts[j * kAStride + tid] : 0.f;
+        }
+    } else {
+        // Kh^T [d][j] = e^(b_63 - b_j) k_j[d], straight to global memory: each warp store is
+        // 32 tokens of one key row (128 bytes)
+        const bool wl = tc::mbar_wait(&bars[LOAD], 0);
+        ok &= wl;
+        float *kt = so.Kt + blk * kMaxD * kC;
+#pragma unroll 8
+        for (int it = 0; it < 64; ++it) {
+            const int rh = (warp - 4) * 64 + it, d = rh >> 1, j = (rh & 1) * 32 + lane;
+            const __nv_bfloat16 kv = *reinterpret_cast<const __nv_bfloat16 *>(
+                sm + KQ + (d >> 6) * 16384 + tc::sw128_offset(j, d & 63));
+            kt[d * kC + j] = ek[j] * __bfloat162float(kv);
+        }
+    }
+    __syncthreads();   // A and T are dead from here
+    if (tid < kC) {
+        // row m of Tw^T and Tu^T: T_jm beta_m e^(b_m) and T_jm beta_m over j
+        store_split_row(sm + TT, sm + TT + 16384, tid, w, bg[tid]);
+        store_split_row(sm + TT + 8192, sm + TT + 24576, tid, w, be[tid]);
+    } else if (tid < 2 * kC) {
+        store_split_row(sm + AP, sm + AP + 8192, tid - kC, w, 1.f);   // row i of P
+    }
+    tc::fence_proxy_async_smem();
+    __syncthreads();
+    if (warp == 0) {
+        // [Tw | Tu]^T P^T: M = 128 (Tw^T rows, then Tu^T rows), N = 64, K = 64 tokens j;
+        // hi*hi, lo*hi, hi*lo
+        __syncwarp();
+        tc::tc_fence_after();
+        if (tc::elect_one()) {
+            const uint32_t id2 = tc::idesc_bf16(128, 64, 0, 0);
+#pragma unroll
+            for (int t = 0; t < 3; ++t) {
+                const uint32_t ao = base + TT + (t == 1 ? 16384 : 0);
+                const uint32_t bo = base + AP + (t == 2 ? 8192 : 0);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    tc::mma_ss(tm + kD2, tc::smem_desc(ao + kk * 32, 16, 1024),
+                               tc::smem_desc(bo + kk * 32, 16, 1024), id2, (t | kk) > 0);
+            }
+            tc::mma_commit(&bars[M2]);
+        }
+        __syncwarp();
+    }
+    if (warp < 4) {
+        // lane m < 64: (P Tw)_{i m} over i; lane 64 + m: (P Tu)_{i m} over i
+        ok &= tc::mbar_wait(&bars[M2], 0);
+        tc::tc_fence_after();
+        tmem_ld64f(tc::tmem_addr(tm, warp, kD2), w);
+        if (tid < kC) store_split_row(sm + AP, sm + AP + 8192, tid, w, -1.f);   // (-P Tw)^T
+    }
+    tc::fence_proxy_async_smem();
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        // [Tw ; -P Tw] K: A MN-major (M atoms Tw^T and (-P Tw)^T), B = k MN-major (N = key
+        // dims), K = 64 tokens m; A hi then A lo
+        __syncwarp();
+        tc::tc_fence_after();
+        if (tc::elect_one()) {
+            const uint32_t id3 = tc::idesc_bf16(128, 128, 1, 1);
+#pragma unroll
+            for (int hl = 0; hl < 2; ++hl) {
+                const uint32_t ao = TT + hl * 16384, lbo = AP + hl * 8192 - ao;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    tc::mma_ss(tm + kD3, tc::smem_desc(base + ao + kk * 2048, lbo, 1024),
+                               tc::smem_desc(base + KQ + kk * 2048, 16384, 1024), id3, (hl | kk) > 0);
+            }
+            tc::mma_commit(&bars[M3]);
+        }
+        __syncwarp();
+    }
+    if (tid >= kC && tid < 2 * kC) {
+        // (P Tu)^T replaces (-P Tw)^T once the MMAs reading it have completed
+        ok &= tc::mbar_wait(&bars[M3], 0);
+        store_split_row(sm + AP, sm + AP + 8192, tid - kC, w, 1.f);
+    }
+    tc::fence_proxy_async_smem();
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        // [Tu ; P Tu] V, into the columns of the two products read above
+        __syncwarp();
+        tc::tc_fence_after();
+        if (tc::elect_one()) {
+            const uint32_t id4 = tc::idesc_bf16(128, 128, 1, 1);
+#pragma unroll
+            for (int hl = 0; hl < 2; ++hl) {
+                const uint32_t ao = TT + 8192 + hl * 16384, lbo = AP + hl * 8192 - ao;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    tc::mma_ss(tm + kD4, tc::smem_desc(base + ao + kk * 2048, lbo, 1024),
+                               tc::smem_desc(base + V + kk * 2048, 8192, 1024), id4, (hl | kk) > 0);
+            }
+            tc::mma_commit(&bars[M4]);
+        }
+        __syncwarp();
+    }
+    ok &= tc::mbar_wait(&bars[M4], 0);
+    tc::tc_fence_after();
+
+    // ---- epilogue: staged through shared memory (v, Tw/Tu and P areas are dead), TMA stores
+    const int q4 = warp & 3, hc = warp >> 2, r = 32 * q4 + lane, rr = r & (kC - 1);
+    const int yrow = (int)(blk * kC);
+    {
+        // W (lanes 0..63) and G = scale e^(b_i) q_i - P W (lanes 64..127), columns 64 hc ..
+        float v[64];
+        tmem_ld64f(tc::tmem_addr(tm, q4, kD3 + 64 * hc), v);
+        if (r >= kC) {
+            const float f = a.scale * eb[rr];
+            const uint8_t *qt = sm + KQ + 8192 + hc * 16384;
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+                const uint4 qq = *reinterpret_cast<const uint4 *>(qt + tc::sw128_offset(rr, 8 * ch));
+                const uint32_t qw[4] = {qq.x, qq.y, qq.z, qq.w};
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    const float2 qf = tc::unpack_bf16(qw[p]);
+                    v[8 * ch + 2 * p] = fmaf(f, qf.x, v[8 * ch + 2 * p]);
+                    v[8 * ch + 2 * p + 1] = fmaf(f, qf.y, v[8 * ch + 2 * p + 1]);
+                }
+            }
+        }
+        stage_row64(sm + (r < kC ? ST0 : ST1), rr, 64 * hc, v);
+    }
+    tc::fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+#pragma unroll
+        for (int bx = 0; bx < 4; ++bx) {
+            tma_store_2d(&tw, sm + ST0 + bx * 8192, 32 * bx, yrow);
+            tma_store_2d(&tg, sm + ST1 + bx * 8192, 32 * bx, yrow);
+        }
+        tc::bulk_commit();
+        tc::bulk_wait_read_all();
+    }
+    __syncthreads();
+    {
+        // Ut (lanes 0..63) and Oi = P Ut (lanes 64..127)
+        float v[64];
+        tmem_ld64f(tc::tmem_addr(tm, q4, kD4 + 64 * hc), v);
+        stage_row64(sm + (r < kC ? ST0 : ST1), rr, 64 * hc, v);
+    }
+    tc::fence_proxy_async_smem();
+    tc::tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+#pragma unroll
+        for (int bx = 0; bx < 4; ++bx) {
+            tma_store_2d(&tu, sm + ST0 + bx * 8192, 32 * bx, yrow);
+            tma_store_2d(&to, sm + ST1 + bx * 8192, 32 * bx, yrow);
+        }
+        tc::bulk_commit();
+        so.C[blk] = bs[kC - 1];
+        tc::bulk_wait_all();
+    }
+    if (warp == 0) {   // TMEM is no longer read
+        __syncwarp();
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tm, 256);
+    }
+    if (!ok) atomicOr(err, kDevErrTimeout);
 }
 
 constexpr size_t kPrepSmem = (size_t)(2 * kMaxD * kPrepStride + 2 * kC * kC + 5 * kC) * sizeof(float);
@@ -972,6 +1437,41 @@ cudaError_t launch_tc_scan(const GdnArgs &a, int64_t BH, unsigned *err, cudaStre
     return cudaGetLastError();
 }
 
+
+std::mutex g_gdn_prep_attr_mu;
+bool g_gdn_prep_attr_done[64];
+
+cudaError_t launch_tc_prep(const GdnArgs &a, int64_t B, unsigned *err, cudaStream_t s) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lock(g_gdn_prep_attr_mu);
+        if (!g_gdn_prep_attr_done[dev]) {
+            e = cudaFuncSetAttribute(gdn_tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)gp::ALLOC);
+            if (e != cudaSuccess) return e;
+            g_gdn_prep_attr_done[dev] = true;
+        }
+    }
+    const SoA so(a.ws, a.nblk, kMaxD, kMaxD);
+    const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
+    CUtensorMap mq, mk, mv, mw, mg, mu, mo;
+    if (!make_bthd_map(&mq, a.q, bf, 2, B, a.T, a.H, kMaxD, 64, kC, sw) ||
+        !make_bthd_map(&mk, a.k, bf, 2, B, a.T, a.H, kMaxD, 64, kC, sw) ||
+        !make_bthd_map(&mv, a.v, bf, 2, B, a.T, a.H, kMaxD, 64, kC, sw) ||
+        !make_2d_map(&mw, so.W, f32, 4, a.nblk * kC, kMaxD, 32, kC, sw) ||
+        !make_2d_map(&mg, so.G, f32, 4, a.nblk * kC, kMaxD, 32, kC, sw) ||
+        !make_2d_map(&mu, so.U, f32, 4, a.nblk * kC, kMaxD, 32, kC, sw) ||
+        !make_2d_map(&mo, so.O, f32, 4, a.nblk * kC, kMaxD, 32, kC, sw))
+        return cudaErrorInvalidResourceHandle;   // a tensor map could not be encoded
+    gdn_tc_prep_kernel<<<(unsigned)a.nblk, gp::kThreadsP, gp::ALLOC, s>>>(mq, mk, mv, mw, mg, mu,
+                                                                         mo, a, err);
+    return cudaGetLastError();
+}
+
 template <typename T>
 cudaError_t launch_typed(const GdnArgs &a, int64_t BH, int num_sms, unsigned *err,
                          cudaStream_t s) {
@@ -979,18 +1479,19 @@ cudaError_t launch_typed(const GdnArgs &a, int64_t BH, int num_sms, unsigned *er
     // bf16 I/O at head dims 128: the tensor-core scan (tf32), with the structure-of-arrays
     // workspace; otherwise the fp32 CUDA-core scan
     const bool tc = std::is_same<T, __nv_bfloat16>::value && a.Dk == kMaxD && a.Dv == kMaxD;
-    auto prep = tc ? gdn_prep_kernel<T, true> : gdn_prep_kernel<T, false>;
-    cudaError_t e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kPrepSmem);
-    if (e != cudaSuccess) return e;
-    prep<<<(unsigned)nprep, kThreads, kPrepSmem, s>>>(a);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
     if (tc) {
+        cudaError_t e = launch_tc_prep(a, BH / a.H, err, s);
+        if (e != cudaSuccess) return e;
         e = launch_tc_scan(a, BH, err, s);
         if (e == cudaSuccess) count_launches(2);
         return e;
     }
+    cudaError_t e = cudaFuncSetAttribute(gdn_prep_kernel<T>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem);
+    if (e != cudaSuccess) return e;
+    gdn_prep_kernel<T><<<(unsigned)nprep, kThreads, kPrepSmem, s>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
     // 16 state columns per CTA where 32 would leave SMs idle
     const bool narrow = BH * (a.Dv / 32) < num_sms || a.Dv % 32 != 0;
     if (narrow) {
