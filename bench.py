@@ -552,10 +552,13 @@ def run_step(args, rank, world, dist):
 
 
 def gdn_flops_per_token_head(Dk: int, Dv: int, C: int = 64) -> int:
-    """fp32 flops of the gated-delta-rule chunk algebra per token and head (causal halves
+    """Flops of the gated-delta-rule chunk algebra per token and head (causal halves
     of the in-chunk products): K K^T and Q K^T 2*C*Dk, the triangular solves C*(Dk+Dv),
     W S, Qh S and Kh^T U 6*Dk*Dv, P U C*Dv."""
     return 2 * C * Dk + C * (Dk + Dv) + 6 * Dk * Dv + C * Dv
+
+
+TF32_PER_BF16 = 1.1 / 2.25   # nominal dense tensor rates of the part (PFLOP/s)
 
 
 def fp32_alu_peak_tflops(sm_mhz: float | None) -> tuple[float, str]:
@@ -638,11 +641,22 @@ def run_gdn(args, rank, world, dist):
     per = total_s / args.steps
     clocks = sampler.summary(clock_source)
     flops = w.B * w.T * w.H * gdn_flops_per_token_head(w.Dk, w.Dv)
-    peak, peak_src = fp32_alu_peak_tflops(clocks.get("sm_mhz"))
     achieved = flops / per / 1e12
     es = 2 if w.io == "bf16" else 4
     nbytes = w.B * w.T * w.H * ((2 * w.Dk + 2 * w.Dv) * es + 8)
-    hbm_gbs, _, _ = load_peaks()
+    hbm_gbs, bf16_tflops, peaks_src = load_peaks()
+    tensor_path = w.io == "bf16" and w.Dk == 128 and w.Dv == 128
+    if tensor_path:
+        # tcgen05 kernels: bf16 products in the prep, tf32 products in the serial scan (the
+        # larger share of the call); the tf32 peak is the measured bf16 peak x the nominal
+        # dense tf32 / bf16 ratio (1.1 / 2.25 PFLOP/s)
+        bound, peak = "tensor", bf16_tflops * TF32_PER_BF16
+        peak_desc = (f"{peaks_src}: MEASURED_PEAKS.json bf16_tflops (burst) x {TF32_PER_BF16:.3f} "
+                     "(nominal dense tf32 / bf16)")
+        path = "gdn (tcgen05: bf16 prep, tf32 state scan)"
+    else:
+        peak, peak_desc = fp32_alu_peak_tflops(clocks.get("sm_mhz"))
+        bound, peak_desc, path = "alu", "derived: " + peak_desc, "gdn (fp32 CUDA cores)"
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = gdn_cpu_oracle_sample(w, x_cpu, args.cpu_seconds)
@@ -652,16 +666,17 @@ def run_gdn(args, rank, world, dist):
             "value": weak_scaling_value(w.B * w.T, args.steps, world, total_s),
             "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * per, "ms_p50": ms[len(ms) // 2],
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "tf32" if tensor_path else "f32",
             "data": "synthetic (seeded unit-norm q/k, N(0,1) v, logsigmoid(N(0,1))/16 gates, "
                     "sigmoid(N(0,1)) write strengths)",
             "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "Dk": w.Dk, "Dv": w.Dv,
-                       "io": w.io, "h0": w.with_h0, "hT": w.want_hT, "path": "gdn (fp32 CUDA cores)",
+                       "io": w.io, "h0": w.with_h0, "hT": w.want_hT, "path": path,
                        "l2": "flushed by a 256 MiB device write before every timed step"},
             "clocks": clocks, "gpu_launches": launches,
-            "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "traffic": committed_traffic("gdn", w.name),
-                         "peak_source": f"derived: {peak_src}",
+                         "peak_source": peak_desc,
                          "algorithmic_flops_per_launch": flops,
                          "algorithmic_bytes_per_launch": nbytes,
                          "hbm_frac": nbytes / per / 1e9 / hbm_gbs,

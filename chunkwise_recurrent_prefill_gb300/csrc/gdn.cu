@@ -1,4 +1,7 @@
-// Gated delta rule forward (prefill), chunkwise, fp32 CUDA cores.
+// Gated delta rule forward (prefill), chunkwise. bf16 I/O at head dims 128 runs on the
+// tensor cores (gdn_tc_prep_kernel: tcgen05 bf16 products; gdn_tc_scan_kernel: tcgen05 tf32
+// products with the fp32 state in TMEM); every other case runs the fp32 CUDA-core pair
+// gdn_prep_kernel / gdn_scan_kernel, which take the same chunk algebra.
 //
 // Per batch and head, with one log-gate g_t and one write strength beta_t per token:
 //     S_t = exp(g_t) (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T,   o_t = scale q_t S_t
@@ -13,11 +16,12 @@
 //     S1  = exp(b_63) S0 + Kh^T U,             Kh_j = exp(b_63 - b_j) k_j.
 // Substituting U, O = Oi + G S0 with Oi = scale P Ut and G = scale (diag(exp(b)) Q - P W).
 // Everything that does not depend on S0 (A, the triangular solves, P, G, Oi, the decay
-// factors) is computed for all chunks at once by gdn_prep_kernel and written to a workspace;
-// the state then runs through the chunks in gdn_scan_kernel, one CTA per (batch, head, block
-// of state columns), which forms U and O from S0 in one pass and then S1: the columns of S
-// are independent under this recurrence (the transition acts on the key axis only), which is
-// what lets B = 1 spread over many SMs.
+// factors) is computed for all chunks at once by the prep kernel and written to a workspace;
+// the state then runs through the chunks in the scan kernel, which forms U and O from S0 in
+// one pass and then S1. The fp32 scan runs one CTA per (batch, head, block of state columns):
+// the columns of S are independent under this recurrence (the transition acts on the key
+// axis only), which is what lets B = 1 spread over many SMs; the tensor-core scan keeps the
+// whole 128 x 128 state of one (batch, head) in TMEM.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <stdint.h>

@@ -26,6 +26,8 @@ def test_gdn_flops_and_peak():
     peak, src = bench.fp32_alu_peak_tflops(None)
     assert abs(peak - 152 * 128 * 2 * 2.07e9 / 1e12) < 1e-9 and "2070 MHz" in src
     assert abs(bench.fp32_alu_peak_tflops(1000.0)[0] - 152 * 128 * 2 * 1e9 / 1e12) < 1e-9
+    # the tensor-core path's tf32 peak: the measured bf16 peak x the nominal dense ratio
+    assert abs(bench.TF32_PER_BF16 - 1.1 / 2.25) < 1e-12
 
 
 def test_weak_scaling_value():
