@@ -892,6 +892,9 @@ gdn_tc_scan_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant
                 tc::tmem_wait_ld();
                 tc::reg_fence(r0);
                 tc::reg_fence(r1);
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&bars[WGF + (c & 1)]);   // the accumulator is free
 #pragma unroll
                 for (int x = 0; x < 16; ++x) {
                     const int t = th + x;
@@ -903,9 +906,6 @@ gdn_tc_scan_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant
                     if (t < vr) op[t * rs] = __float2bfloat16_rn(oi[16 + x] + eL * __uint_as_float(r1[x]));
                 }
             }
-            tc::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&bars[WGF + (c & 1)]);   // the accumulator is free
             float Ln = L + bsum * 1.4426950408889634f;
             if (!(fabsf(Ln) <= kRenormL2)) Ln = 0.f;   // the U warps rescaled S~ here
             L = Ln;
