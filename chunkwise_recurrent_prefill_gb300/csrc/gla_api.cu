@@ -207,11 +207,11 @@ int current_device_status() {
     DeviceState *st = nullptr;
     return (int)current_device(&st);
 }
-int tc_auto_splits_for(int64_t B, int64_t T, int64_t H) {
+int tc_auto_splits_for(int64_t B, int64_t T, int64_t H, int64_t Dk, int64_t Dv) {
     DeviceState *st = nullptr;
     const int sms = current_device(&st) == GLA_OK ? st->num_sms : 152;
     Problem p{};
-    p.B = B; p.T = T; p.H = H; p.Dk = 128; p.Dv = 128;
+    p.B = B; p.T = T; p.H = H; p.Dk = Dk; p.Dv = Dv;
     return tc_auto_splits(p, sms);
 }
 void set_error_detail(const char *text) { snprintf(g_detail, sizeof(g_detail), "%s", text); }

@@ -63,7 +63,7 @@ bool tc_supported(const Problem &p);
 int tc_auto_splits(const Problem &p, int num_sms);
 // tc_auto_splits of a bf16 problem of this shape on the current device (152 SMs if it cannot
 // be queried).
-int tc_auto_splits_for(int64_t B, int64_t T, int64_t H);
+int tc_auto_splits_for(int64_t B, int64_t T, int64_t H, int64_t Dk, int64_t Dv);
 int tc_state_pieces(const Problem &p, int splits, int num_sms);
 size_t tc_workspace_bytes(const Problem &p, int splits, int num_sms);
 cudaError_t launch_tc(const Problem &p, int splits, int num_sms, void *ws, size_t ws_bytes,

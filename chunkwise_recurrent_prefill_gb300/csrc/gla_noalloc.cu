@@ -72,7 +72,7 @@ extern "C" gla_status gla_fwd_noalloc(const void *q, const void *k, const void *
         }
         // automatic split: from the count gla_fwd would pick, down to the largest whose scratch
         // fits (one segment needs none)
-        int s = gla::tc_auto_splits_for(B, T, H);
+        int s = gla::tc_auto_splits_for(B, T, H, Dk, Dv);
         for (; s > 1; --s) {
             opt.seq_splits = s;
             if (gla_fwd_workspace_size(B, T, H, Dk, Dv, GLA_IO_BF16, &opt) <= cap) break;

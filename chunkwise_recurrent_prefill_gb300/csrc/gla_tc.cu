@@ -112,6 +112,9 @@ constexpr uint32_t kColS = 0;      // S~^T fp32, 128 columns
 constexpr uint32_t kColSB = 128;   // S~^T bf16 snapshot (A operand), 2 x 64 columns
 constexpr uint32_t kColP = 256;    // P (M=64 layout), 64 columns
 constexpr uint32_t kColO = 320;    // O^T = S~^T Q'^T + V^T P^T, 64 columns
+// head pairs (two heads of dims 64 as one of 128): the second head's P and O^T
+constexpr uint32_t kColP2 = 384;
+constexpr uint32_t kColO2 = 448;
 
 // Shared-memory map of the output kernel (bytes from a 1024-aligned base).
 //   q/k/v ring (3 stages): raw tiles as 128B-swizzled [64 x 64] bf16 boxes, two per tile;
@@ -137,7 +140,7 @@ constexpr uint32_t XCH = XF + 64;       // [<=4][128] f32 token-range totals of 
 constexpr uint32_t GSC = XCH + 2048;    // [2][64] f32 scalar gates of two chunks (scalar mode)
 constexpr uint32_t SCR = GSC + 512;     // [4][64] f32 exact-path scratch
 constexpr uint32_t BAR = SCR + 1024;    // mbarriers
-constexpr uint32_t NBAR = 24;
+constexpr uint32_t NBAR = 26;
 constexpr uint32_t TSLOT = BAR + NBAR * 8;
 constexpr uint32_t ALLOC = TSLOT + 16 + 1024;
 static_assert(ALLOC <= 232448, "output kernel shared memory");
@@ -150,6 +153,7 @@ constexpr uint32_t FAC = NQS * QSTAGE;  // [64] float2 per-token factors (scalar
 enum {
     QFULL = 0, QEMPTY = 4, GFULL = 8, GEMPTY = 10, GDONE = 12, PFULL = 16, PFREE = 17, PBF = 18,
     SREADY = 19, UDONE = 20, OFULL = 21, OFREE = 22, FIN = 23,
+    OAFULL = 24, PBF2 = 25,   // head pairs: first head's O^T done; second head's P tile written
 };
 static_assert(FIN < (int)om::NBAR, "output kernel barrier map");
 
@@ -297,7 +301,14 @@ __device__ __forceinline__ uint32_t par(int use) { return (uint32_t)use & 1u; }
 // kPacked: the batches are sequences packed along one token axis at offsets a.cu; the rows
 // of a sequence's last chunk past its end are masked (batched tensors need no masking: the
 // rows past T are zero-filled by the tensor copies and clipped by the stores).
-template <bool kScalar, bool kPacked>
+// kPair: the tensors hold head pairs (2p, 2p + 1) of dims 64 as heads p of dims 128
+// (adjacent heads are contiguous in [B,T,H,64], so the tiles are the same). The state of a
+// pair is block diagonal; its off-diagonal blocks collect cross-head products that are never
+// read: the bf16 snapshot (the only operand read from the state) zeroes them, and hT
+// writes the diagonal blocks. P and the intra term are per head: P of the second head
+// accumulates apart, the P tile is filled twice, and the second head's O^T (its lanes are
+// value columns 64..127) accumulates in a second column block.
+template <bool kScalar, bool kPacked, bool kPair = false>
 __global__ void __launch_bounds__(kOutThreads, 1)
 gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg,
@@ -366,6 +377,8 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         mbar_init(&bars[OFULL], 1);
         mbar_init(&bars[OFREE], 4);
         mbar_init(&bars[FIN], 1);
+        mbar_init(&bars[OAFULL], 1);
+        mbar_init(&bars[PBF2], 4);
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -464,9 +477,10 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             const uint32_t idOi = idesc_bf16(128, 64, 1, 0);
             const uint32_t idOs = idesc_bf16(128, 64, 0, 0);
             int np = 0, nu = 0, no = 0;
+            int nb = kPair ? 0 : n;   // head pairs: second-head O groups issued
             uint32_t idle = 0;
             uint64_t t_idle = 0;
-            while (no < n) {
+            while (no < n || nb < n) {
                 bool prog = false;
                 const bool rU = __shfl_sync(0xffffffffu, nu < np && mbar_test(&bars[SREADY], par(nu)), 0);
                 if (rU) {
@@ -495,8 +509,11 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
 #pragma unroll
                         for (int x = 0; x < 8; ++x) {   // key dims 16x .. 16x + 15
                             const uint32_t off = (x >> 2) * 8192 + (x & 3) * 32;
-                            mma_ss(tm + kColP, smem_desc(base + Q + off, 16, 1024),
-                                   smem_desc(base + K + off, 16, 1024), idP, x > 0);
+                            // head pairs: each head's P over its own 64 key dims
+                            const uint32_t dst = (kPair && x >= 4) ? kColP2 : kColP;
+                            mma_ss(tm + dst, smem_desc(base + Q + off, 16, 1024),
+                                   smem_desc(base + K + off, 16, 1024), idP,
+                                   kPair ? (x & 3) > 0 : x > 0);
                         }
                         mma_commit(&bars[PFULL]);
                     }
@@ -524,12 +541,38 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                         for (int kk = 0; kk < 4; ++kk)
                             mma_ss(tm + kColO, smem_desc(base + V + kk * 2048, 8192, 1024),
                                    smem_desc(pbase + kk * 32, 16, 1024), idOi, 1);
-                        mma_commit(&bars[OFULL]);   // U(no) and P(no) were issued before O(no)
+                        // U(no) and P(no) were issued before O(no)
+                        mma_commit(&bars[kPair ? OAFULL : OFULL]);
                     }
                     __syncwarp();
                     if (lane == 0) TRACE_OUT(7, no);
                     ++no;
                     prog = true;
+                }
+                if (kPair) {
+                    // second head of the pair: its P tile replaced the first head's once the
+                    // first head's O^T had completed; lanes 64..127 of this block are its O^T
+                    const bool rB = __shfl_sync(0xffffffffu, nb < no && mbar_test(&bars[PBF2], par(nb)), 0);
+                    if (rB) {
+                        tc_fence_after();
+                        const uint32_t base = smem_u32(sm + (nb % NQ) * QSTAGE);
+                        const uint32_t pbase = smem_u32(sm + P);
+                        if (elect_one()) {
+#pragma unroll
+                            for (int kk = 0; kk < 8; ++kk)
+                                mma_ts(tm + kColO2, tm + kColSB + (nb & 1) * 64 + kk * 8,
+                                       smem_desc(base + Q + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
+                                       idOs, kk > 0);
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk)
+                                mma_ss(tm + kColO2, smem_desc(base + V + kk * 2048, 8192, 1024),
+                                       smem_desc(pbase + kk * 32, 16, 1024), idOi, 1);
+                            mma_commit(&bars[OFULL]);
+                        }
+                        __syncwarp();
+                        ++nb;
+                        prog = true;
+                    }
                 }
                 if (prog) {
                     idle = 0;
@@ -569,7 +612,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             tc_fence_after();
             if (et == 0) mbar_arrive(&bars[QEMPTY + c % NQ]);   // the stage may be refilled
             float ov[64];
-            tmem_ld64(tmem_addr(tm, j, kColO), ov);
+            tmem_ld64(tmem_addr(tm, j, (kPair && j >= 2) ? kColO2 : kColO), ov);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[OFREE]);
@@ -608,17 +651,27 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             pdl_wait_prerequisites();
             if (threadIdx.x == 6 * 32) TRACE_GLOB(0, 1);
             init = a.sstart + ((size_t)bh * (a.splits - 1) + (seg - 1)) * (kD * kD);
-        } else if (a.h0)
-            init = a.h0 + (size_t)bh * a.Dk * a.Dv;
+        } else if (a.h0) {
+            // head pairs: this lane's value column belongs to head 2 bh + v / 64, whose 64 x 64
+            // h0 fills the diagonal block of its key rows
+            init = kPair ? a.h0 + ((size_t)2 * bh + (v >> 6)) * 4096
+                         : a.h0 + (size_t)bh * a.Dk * a.Dv;
+        }
         // start states are 128 x 128 internally; h0 has the caller's Dk x Dv (zero padded)
         const int irows = seg > 0 ? kD : a.Dk, icols = seg > 0 ? kD : a.Dv;
 #pragma unroll 1
         for (int d0 = 0; d0 < kD; d0 += 16) {
             uint32_t r[16];
 #pragma unroll
-            for (int x = 0; x < 16; ++x)
-                r[x] = (init && d0 + x < irows && v < icols)
-                           ? __float_as_uint(init[(d0 + x) * icols + v]) : 0u;
+            for (int x = 0; x < 16; ++x) {
+                const int d = d0 + x;
+                if (kPair && seg == 0)
+                    r[x] = (init && (d >> 6) == (v >> 6))
+                               ? __float_as_uint(init[(d & 63) * 64 + (v & 63)]) : 0u;
+                else
+                    r[x] = (init && d < irows && v < icols)
+                               ? __float_as_uint(init[d * icols + v]) : 0u;
+            }
             tmem_st16(tmem_addr(tm, j, kColS + d0), r);
         }
         tmem_wait_st();
@@ -641,12 +694,14 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
 #pragma unroll
                     for (int x = 0; x < 64; ++x) sv[x] *= gl[half * 64 + x];
                 }
+                // head pairs: the blocks across heads are not state; the snapshot holds zeros
+                const bool cross = kPair && half != (j >> 1);
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
                     uint32_t pk[8];
 #pragma unroll
                     for (int x = 0; x < 8; ++x)
-                        pk[x] = pack_bf16(sv[16 * cc + 2 * x], sv[16 * cc + 2 * x + 1]);
+                        pk[x] = cross ? 0u : pack_bf16(sv[16 * cc + 2 * x], sv[16 * cc + 2 * x + 1]);
                     tmem_st8(tmem_addr(tm, j, kColSB + (c & 1) * 64 + half * 32 + cc * 8), pk);
                 }
                 if (ext) {
@@ -675,59 +730,74 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             tc_fence_after();
             float prow[64];
             const int i = 16 * j + lane;        // P row held by this lane (lane < 16)
-            if (!ext) {
-                tmem_ld64(tmem_addr(tm, j, kColP), prow);
-            } else {
-                // exact route: P_ij = scale sum_d q_id k_jd exp(b_id - b_jd), j <= i
-#pragma unroll
-                for (int x = 0; x < 64; ++x) prow[x] = 0.f;
-                float *gcol = scr, *qcol = scr + 64, *kcol = scr + 128, *bcol = scr + 192;
-                const int64_t t0 = tbase + (int64_t)(cb + c) * kC;
-                for (int d = 0; d < a.Dk; ++d) {   // padded key dims add nothing
-                    if (st_t < 64) {
-                        const int64_t t = t0 + st_t;
-                        const bool in = t < tend;
-                        const int64_t idx = (((int64_t)bmap * a.T + t) * a.H + h) * a.Dk + d;
-                        gcol[st_t] = in ? (kScalar ? a.g[idx / a.Dk] : a.g[idx]) : 0.f;
-                        qcol[st_t] = in ? __bfloat162float(a.q[idx]) : 0.f;
-                        kcol[st_t] = in ? __bfloat162float(a.k[idx]) : 0.f;
-                    }
-                    named_bar_sync(3, 128);
-                    if (st_t == 0) {
-                        float s = 0.f;
-                        for (int t = 0; t < 64; ++t) { s += gcol[t]; bcol[t] = s; }
-                    }
-                    named_bar_sync(3, 128);
-                    if (lane < 16) {
-                        const float qi = a.scale * qcol[i], bi = bcol[i];
-#pragma unroll
-                        for (int x = 0; x < 64; ++x)
-                            if (x <= i) prow[x] += qi * kcol[x] * ex2((bi - bcol[x]) * kLog2e);
-                    }
-                    named_bar_sync(3, 128);
+            // head pairs fill the P tile twice: the second head's P once the first head's
+            // O^T (the tile's reader) has completed
+            bool pok = true;
+#pragma unroll 1
+            for (int ph = 0; ph < (kPair ? 2 : 1); ++ph) {
+                if (ph == 1) {
+                    w = mbar_wait(&bars[OAFULL], par(c));
+                    if (named_bar_or(3, 128, !w)) { pok = false; break; }
+                    tc_fence_after();
                 }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[PFREE]);
-            if (lane < 16) {
-                uint8_t *pt = sm + P;
+                if (!ext) {
+                    tmem_ld64(tmem_addr(tm, j, ph ? kColP2 : kColP), prow);
+                } else {
+                    // exact route: P_ij = scale sum_d q_id k_jd exp(b_id - b_jd), j <= i
 #pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
-                    uint32_t wv[4];
+                    for (int x = 0; x < 64; ++x) prow[x] = 0.f;
+                    float *gcol = scr, *qcol = scr + 64, *kcol = scr + 128, *bcol = scr + 192;
+                    const int64_t t0 = tbase + (int64_t)(cb + c) * kC;
+                    const int dlo = kPair ? 64 * ph : 0, dhi = kPair ? dlo + 64 : a.Dk;
+                    for (int d = dlo; d < dhi; ++d) {   // padded key dims add nothing
+                        if (st_t < 64) {
+                            const int64_t t = t0 + st_t;
+                            const bool in = t < tend;
+                            const int64_t idx = (((int64_t)bmap * a.T + t) * a.H + h) * a.Dk + d;
+                            gcol[st_t] = in ? (kScalar ? a.g[idx / a.Dk] : a.g[idx]) : 0.f;
+                            qcol[st_t] = in ? __bfloat162float(a.q[idx]) : 0.f;
+                            kcol[st_t] = in ? __bfloat162float(a.k[idx]) : 0.f;
+                        }
+                        named_bar_sync(3, 128);
+                        if (st_t == 0) {
+                            float s = 0.f;
+                            for (int t = 0; t < 64; ++t) { s += gcol[t]; bcol[t] = s; }
+                        }
+                        named_bar_sync(3, 128);
+                        if (lane < 16) {
+                            const float qi = a.scale * qcol[i], bi = bcol[i];
 #pragma unroll
-                    for (int x = 0; x < 4; ++x) {
-                        const int col = cc * 8 + 2 * x;
-                        wv[x] = pack_bf16(col <= i ? prow[col] : 0.f,
-                                          col + 1 <= i ? prow[col + 1] : 0.f);
+                            for (int x = 0; x < 64; ++x)
+                                if (x <= i) prow[x] += qi * kcol[x] * ex2((bi - bcol[x]) * kLog2e);
+                        }
+                        named_bar_sync(3, 128);
                     }
-                    *reinterpret_cast<uint4 *>(pt + sw128_offset(i, cc * 8)) =
-                        make_uint4(wv[0], wv[1], wv[2], wv[3]);
                 }
+                if (!kPair || ph == 1) {   // every P accumulator of c has been read
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars[PFREE]);
+                }
+                if (lane < 16) {
+                    uint8_t *pt = sm + P;
+#pragma unroll
+                    for (int cc = 0; cc < 8; ++cc) {
+                        uint32_t wv[4];
+#pragma unroll
+                        for (int x = 0; x < 4; ++x) {
+                            const int col = cc * 8 + 2 * x;
+                            wv[x] = pack_bf16(col <= i ? prow[col] : 0.f,
+                                              col + 1 <= i ? prow[col + 1] : 0.f);
+                        }
+                        *reinterpret_cast<uint4 *>(pt + sw128_offset(i, cc * 8)) =
+                            make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[ph ? PBF2 : PBF]);
             }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[PBF]);
+            if (!pok) { ok = false; break; }
             if (v == 0) TRACE_OUT(11, c);
         }
         if (ok && !bad_seq && a.hT && seg == a.splits - 1) {
@@ -735,15 +805,25 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 ok = false;
             } else {
                 tc_fence_after();
-                float *hp = a.hT + (size_t)bh * a.Dk * a.Dv + v;
-#pragma unroll 1
-                for (int half = 0; half < a.Dk / 64; ++half) {
+                if (kPair) {
+                    // the diagonal block of this lane's head: key rows of the same half
+                    const int hb = j >> 1;
+                    float *hq = a.hT + ((size_t)2 * bh + hb) * 4096 + (v & 63);
                     float sv[64];
-                    tmem_ld64(tmem_addr(tm, j, kColS + half * 64), sv);
-                    if (v < a.Dv) {
+                    tmem_ld64(tmem_addr(tm, j, kColS + hb * 64), sv);
 #pragma unroll
-                        for (int x = 0; x < 64; ++x)
-                            hp[(half * 64 + x) * a.Dv] = sv[x] * ends_s[half * 64 + x];
+                    for (int x = 0; x < 64; ++x) hq[x * 64] = sv[x] * ends_s[hb * 64 + x];
+                } else {
+                    float *hp = a.hT + (size_t)bh * a.Dk * a.Dv + v;
+#pragma unroll 1
+                    for (int half = 0; half < a.Dk / 64; ++half) {
+                        float sv[64];
+                        tmem_ld64(tmem_addr(tm, j, kColS + half * 64), sv);
+                        if (v < a.Dv) {
+#pragma unroll
+                            for (int x = 0; x < 64; ++x)
+                                hp[(half * 64 + x) * a.Dv] = sv[x] * ends_s[half * 64 + x];
+                        }
                     }
                 }
             }
@@ -1262,7 +1342,7 @@ constexpr int kScanBatch = 4;
 __global__ void __launch_bounds__(kScanThreads)
 gla_tc_scan_kernel(const float *__restrict__ E, const float *__restrict__ gam,
                    const float *__restrict__ h0, float *__restrict__ sstart, int splits,
-                   int pieces, int Dk, int Dv) {
+                   int pieces, int Dk, int Dv, int paired) {
     pdl_launch_dependents();    // the output kernel may be scheduled now; it waits for us
     if (threadIdx.x == 0 && blockIdx.y == 0) TRACE_GLOB(2, 0);
     pdl_wait_prerequisites();   // the end states of the state kernel
@@ -1276,7 +1356,11 @@ gla_tc_scan_kernel(const float *__restrict__ E, const float *__restrict__ gam,
 #pragma unroll
     for (int i = 0; i < kScanPer; ++i) {
         const int e = e0 + i * kScanThreads, d = e / kD, v = e % kD;   // h0 is Dk x Dv
-        s[i] = (h0 && d < Dk && v < Dv) ? h0[bh * (size_t)Dk * Dv + (size_t)d * Dv + v] : 0.f;
+        if (paired)   // head pairs: the diagonal blocks are heads 2 bh and 2 bh + 1 (64 x 64)
+            s[i] = (h0 && (d >> 6) == (v >> 6))
+                       ? h0[(bh * 2 + (v >> 6)) * 4096 + (size_t)(d & 63) * 64 + (v & 63)] : 0.f;
+        else
+            s[i] = (h0 && d < Dk && v < Dv) ? h0[bh * (size_t)Dk * Dv + (size_t)d * Dv + v] : 0.f;
     }
     const float *Eb = E + bh * npc * kDD + e0;
     const float *gb = gam + bh * npc * kD;
@@ -1322,13 +1406,14 @@ cudaError_t set_attrs() {
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_attr_mu);
     if (g_attr_done[dev]) return cudaSuccess;
-    const void *outs[4] = {(const void *)gla_tc_out_kernel<false, false>,
+    const void *outs[5] = {(const void *)gla_tc_out_kernel<false, false>,
                            (const void *)gla_tc_out_kernel<true, false>,
                            (const void *)gla_tc_out_kernel<false, true>,
-                           (const void *)gla_tc_out_kernel<true, true>};
+                           (const void *)gla_tc_out_kernel<true, true>,
+                           (const void *)gla_tc_out_kernel<false, false, true>};
     const void *states[2] = {(const void *)gla_tc_state_kernel<false>,
                              (const void *)gla_tc_state_kernel<true>};
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 5; ++i) {
         e = cudaFuncSetAttribute(outs[i], cudaFuncAttributeMaxDynamicSharedMemorySize, om::ALLOC);
         if (e != cudaSuccess) return e;
         if (i < 2) {
@@ -1366,6 +1451,21 @@ int clamp_splits(const Problem &p, int splits) {
     return (int)std::min<int64_t>(s, kMaxSplits);
 }
 
+// Head pairs: bf16 I/O, per-key gates, head dims 64 x 64, an even number of heads and no
+// packed sequences run as H / 2 heads of dims 128 (gla_tc_out_kernel<.., kPair>).
+bool pair_heads(const Problem &p) {
+    return p.io == 0 && p.Dk == 64 && p.Dv == 64 && p.H % 2 == 0 && p.gate != 1 && !p.cu;
+}
+
+// The problem as the tensor-core kernels see it.
+Problem tc_view(const Problem &p) {
+    if (!pair_heads(p)) return p;
+    Problem q = p;
+    q.H = p.H / 2;
+    q.Dk = q.Dv = kD;
+    return q;
+}
+
 }  // namespace
 
 bool tc_supported(const Problem &p) {
@@ -1376,7 +1476,8 @@ bool tc_supported(const Problem &p) {
            p.B * p.H < (int64_t(1) << 24);
 }
 
-int tc_auto_splits(const Problem &p, int num_sms) {
+int tc_auto_splits(const Problem &pc, int num_sms) {
+    const Problem p = tc_view(pc);
     const int64_t nchunks = (p.T + kC - 1) / kC;
     const int64_t bh = p.B * p.H;
     if (nchunks <= 1 || bh <= 0) return 1;
@@ -1388,7 +1489,8 @@ int tc_auto_splits(const Problem &p, int num_sms) {
     return (int)std::min<int64_t>(s, kMaxSplits);
 }
 
-int tc_state_pieces(const Problem &p, int splits, int num_sms) {
+int tc_state_pieces(const Problem &pc, int splits, int num_sms) {
+    const Problem p = tc_view(pc);
     const int s = clamp_splits(p, splits);
     if (s <= 1) return 1;
     // Split each segment's state pass into consecutive pieces until its grid, like the output
@@ -1400,7 +1502,8 @@ int tc_state_pieces(const Problem &p, int splits, int num_sms) {
     return (int)std::max<int64_t>(1, std::min<int64_t>(k, kMaxPieces));
 }
 
-size_t tc_workspace_bytes(const Problem &p, int splits, int num_sms) {
+size_t tc_workspace_bytes(const Problem &pc, int splits, int num_sms) {
+    const Problem p = tc_view(pc);
     const int s = clamp_splits(p, splits);
     if (s <= 1) return 0;
     const size_t bh = (size_t)(p.B * p.H);
@@ -1409,12 +1512,14 @@ size_t tc_workspace_bytes(const Problem &p, int splits, int num_sms) {
     return bh * (size_t)(s - 1) * (k * ((size_t)kD * kD + kD) + (size_t)kD * kD) * sizeof(float);
 }
 
-cudaError_t launch_tc(const Problem &p, int splits, int num_sms, void *ws, size_t ws_bytes,
+cudaError_t launch_tc(const Problem &pc, int splits, int num_sms, void *ws, size_t ws_bytes,
                       unsigned int *dev_err, cudaStream_t stream) {
     // Fewer tokens than one chunk (for packed sequences: in all of them together): the exact
     // kernel (each output is a handful of products of bf16-rounded decayed operands here,
     // with nothing to average their rounding). T = 0 only writes hT = h0.
-    if (p.T < kC) return launch_exact(p, dev_err, stream);
+    if (pc.T < kC) return launch_exact(pc, dev_err, stream);
+    const bool paired = pair_heads(pc);
+    const Problem p = tc_view(pc);
     const int s = p.cu ? 1 : clamp_splits(p, splits);   // packed sequences are not split
     const int64_t mB = p.cu ? 1 : p.B;                   // batch extent of the tensor maps
     const bool scalar = p.gate == 1;
@@ -1475,7 +1580,7 @@ cudaError_t launch_tc(const Problem &p, int splits, int num_sms, void *ws, size_
         cfg.attrs = pdl;
         cfg.numAttrs = 1;
         e = cudaLaunchKernelEx(&cfg, gla_tc_scan_kernel, (const float *)E, (const float *)gam,
-                               p.h0, sstart, s, pieces, (int)p.Dk, (int)p.Dv);
+                               p.h0, sstart, s, pieces, (int)p.Dk, (int)p.Dv, paired ? 1 : 0);
         if (e != cudaSuccess) return e;
         count_launches(2);
     }
@@ -1496,12 +1601,15 @@ cudaError_t launch_tc(const Problem &p, int splits, int num_sms, void *ws, size_
         cfg.stream = stream;
         cfg.attrs = pdl;
         cfg.numAttrs = 1;
-        e = scalar
-                ? cudaLaunchKernelEx(&cfg, gla_tc_out_kernel<true, false>, mq, mk, mv, mg, oa)
-                : cudaLaunchKernelEx(&cfg, gla_tc_out_kernel<false, false>, mq, mk, mv, mg, oa);
+        e = scalar   ? cudaLaunchKernelEx(&cfg, gla_tc_out_kernel<true, false>, mq, mk, mv, mg, oa)
+            : paired ? cudaLaunchKernelEx(&cfg, gla_tc_out_kernel<false, false, true>, mq, mk, mv,
+                                          mg, oa)
+                     : cudaLaunchKernelEx(&cfg, gla_tc_out_kernel<false, false>, mq, mk, mv, mg, oa);
     } else {
         auto kern = p.cu ? (scalar ? gla_tc_out_kernel<true, true> : gla_tc_out_kernel<false, true>)
-                         : (scalar ? gla_tc_out_kernel<true, false> : gla_tc_out_kernel<false, false>);
+                    : scalar ? gla_tc_out_kernel<true, false>
+                    : paired ? gla_tc_out_kernel<false, false, true>
+                             : gla_tc_out_kernel<false, false>;
         kern<<<bh * s, kOutThreads, om::ALLOC, stream>>>(mq, mk, mv, mg, oa);
         e = cudaGetLastError();
     }

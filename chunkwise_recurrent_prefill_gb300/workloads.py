@@ -58,6 +58,9 @@ WORKLOADS = {
     # the scalar-per-head gate variant on the bench shape (one log-gate per token and head)
     "bf16_B1_H16_T16384_scalar": Workload("bf16_B1_H16_T16384_scalar", B=1, T=16384, H=16,
                                           seed=6, gate="scalar"),
+    # head dims 64 on the bench shape (heads run in pairs on the tensor cores)
+    "bf16_B1_H16_T16384_D64": Workload("bf16_B1_H16_T16384_D64", B=1, T=16384, H=16, Dk=64,
+                                       Dv=64, seed=7, with_h0=True, want_hT=True),
 }
 
 # The workload the throughput metric is quoted on (B=1, H=16, T=16K, D=128, bf16).

@@ -274,3 +274,51 @@ def test_tc_head_dim_64(Dk, Dv, splits, gate):
     o_ref, h_ref = _oracle_scalar(x) if gate == "scalar" else _oracle(x)
     assert_close(o.float().cpu().numpy(), o_ref, "bf16", f"o(D={Dk}x{Dv})")
     assert_close(hT.cpu().numpy(), h_ref, "bf16", f"hT(D={Dk}x{Dv})")
+
+
+def _d64_inputs(B, T, H, seed, with_h0=True):
+    from chunkwise_recurrent_prefill_gb300.workloads import make_inputs, small
+    return make_inputs(small("d64p", B=B, T=T, H=H, io="bf16", seed=seed, with_h0=with_h0, Dk=64,
+                             Dv=64), DEV)
+
+
+@pytest.mark.parametrize("B,T,H,splits", [(2, 700, 4, 1), (2, 700, 4, 3), (1, 1000, 2, 0),
+                                          (1, 64, 2, 1), (3, 321, 6, 0), (1, 4100, 8, 0)])
+def test_tc_head_pairs_d64(B, T, H, splits):
+    """Head dims 64 with an even number of heads: two heads run as one of dims 128 with a
+    block-diagonal state. Every element of o and hT (h0 given) against the oracle."""
+    x = _d64_inputs(B, T, H, seed=B * 31 + T + H)
+    o, hT = _run(x, seq_splits=splits)
+    o_ref, h_ref = _oracle(x)
+    assert_close(o.float().cpu().numpy(), o_ref, "bf16", f"o(pairs B={B} T={T} H={H})")
+    assert_close(hT.cpu().numpy(), h_ref, "bf16", f"hT(pairs B={B} T={T} H={H})")
+
+
+@pytest.mark.parametrize("kind", ["forget", "strong", "mixed", "renorm", "one_chunk_extreme",
+                                  "one_head_extreme", "big_values"])
+def test_tc_head_pairs_d64_extreme(kind):
+    """Extreme gates on head pairs: chunks flagged extreme compute each head's P on the exact
+    route from that head's own key dims; a chunk extreme in one head only flags the pair."""
+    x = _d64_inputs(1, 700, 4, seed=7)
+    if kind == "one_head_extreme":
+        x["g"][:, 64:128, 1] = -3.0   # head 1 (second of the first pair) only
+    else:
+        x = _extreme(x, kind)
+    o, hT = _run(x, seq_splits=2)
+    assert torch.isfinite(o.float()).all() and torch.isfinite(hT).all()
+    o_ref, h_ref = _oracle(x)
+    assert_close(o.float().cpu().numpy(), o_ref, "bf16", f"o[pairs {kind}]")
+    assert_close(hT.cpu().numpy(), h_ref, "bf16", f"hT[pairs {kind}]")
+
+
+def test_tc_head_pairs_d64_bench_shape():
+    """The D = 64 bench shape (B=1, H=16, T=16384, h0 and hT) in its launch configuration:
+    every output of every head against the C oracle."""
+    from chunkwise_recurrent_prefill_gb300.workloads import WORKLOADS, make_inputs
+    x = make_inputs(WORKLOADS["bf16_B1_H16_T16384_D64"], DEV)
+    o, hT = _run(x)
+    o_ref, h_ref = _oracle(x)
+    eo = assert_close(o.float().cpu().numpy(), o_ref, "bf16", "D64 o")
+    eh = assert_close(hT.cpu().numpy(), h_ref, "bf16", "D64 hT")
+    print(f"\nparity D64 bench shape: o max/mean rel {eo[0]:.3e}/{eo[1]:.3e}  "
+          f"hT max/mean rel {eh[0]:.3e}/{eh[1]:.3e}")
