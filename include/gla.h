@@ -23,8 +23,11 @@
  *     q, k, g_log : [B, T, H, Dk]
  *     v, o        : [B, T, H, Dv]
  *     h0, hT      : [B, H, Dk, Dv]   float32
- * Supported head dims: Dk, Dv in {64, 128} on both paths (the tensor-core kernels work at
- * 128 and pad a head dim of 64 with zeros). Any T >= 0 (a partial last chunk is handled).
+ * Supported head dims: Dk, Dv in {64, 128} on both paths. The tensor-core kernels work at
+ * 128: with Dk = Dv = 64, an even H, per-key gates and no packed sequences, heads 2p and
+ * 2p + 1 (adjacent, so one contiguous row of 128) run together as one head of 128 with a
+ * block-diagonal state; any other head dim of 64 is padded with zeros. Results are the same
+ * either way, within the stated tolerances. Any T >= 0 (a partial last chunk is handled).
  *
  * Ownership and memory: every tensor pointer is a DEVICE pointer owned by the caller
  * and must be 16-byte aligned. o and hT must not overlap any input. The library never
@@ -262,7 +265,10 @@ gla_status gla_fwd_noalloc(const void *q, const void *k, const void *v, const fl
  * to use the library's workspace of `stream` (one per stream and device, shared with
  * gla_fwd_ex calls on that stream; see gla_options.workspace).
  * A caller workspace smaller than needed, misaligned, or overlapping an argument returns
- * GLA_ERR_WORKSPACE. fp32 arithmetic on CUDA cores; deterministic (no atomics). Two
+ * GLA_ERR_WORKSPACE. Arithmetic: bf16 I/O with Dk = Dv = 128 runs on the tensor cores
+ * (bf16 products of the inputs and split-precision bf16 coefficients in the chunk-parallel
+ * part, tf32 products with an fp32 state in the serial part, fp32 accumulation throughout);
+ * every other case runs fp32 arithmetic on CUDA cores. Deterministic (no atomics). Two
  * kernels, stream-ordered on `stream`; no host synchronisation. T = 0 writes hT = h0 (or
  * zero) and launches nothing.
  */
