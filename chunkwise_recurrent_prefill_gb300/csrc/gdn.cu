@@ -26,6 +26,7 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <mutex>
 #include <type_traits>
 
@@ -603,6 +604,34 @@ constexpr float kRenormL2 = 60.f;
 enum { FULL = 0, EMPTY = 2, WGD = 4, WGF = 6, URDY = 8, FIN = 9 };
 }  // namespace gt
 
+// Sequence split of the tensor-core scan. The chunk map S1 = (e^(b_63) I - Kh^T W) S0 +
+// Kh^T Ut is affine in the state, so a segment of chunks maps its start state S to M S + E,
+// with E its end state from a zero start and M (Dk x Dk) its end state from the identity with
+// Ut = 0 (the value columns of the state are independent, so M is the same recurrence with
+// Dk columns). Segment 0 starts from h0, which is known: its outputs run in the first
+// launch (mode 1), and its end state is the start state of segment 1. Beside them, two CTAs
+// per segment compute E and M of segments 1 .. segs - 2. gdn_seg_scan_kernel then forms
+// S_start(s + 1) = M_s S_start(s) + E_s, and the second launch (mode 0) runs the outputs of
+// segments 1 .. segs - 1 from their start states. Segment 0 is half as long as the others:
+// a transition chunk costs about half an output chunk.
+struct ScanPlan {
+    int segs;          // segments per (batch, head); 1 = no split
+    int mode;          // 0: outputs of segments s0 .. segs - 1; 1: see above
+    int s0;            // first segment of a mode-0 launch
+    float *E;          // [BH][segs - 1][Dk][Dv] (entries 1 .. segs - 2 used)
+    float *M;          // [BH][segs - 1][Dk][Dk] (entries 1 .. segs - 2 used)
+    float *Ss;         // [BH][segs - 1][Dk][Dv]: start states of segments 1 .. segs - 1
+};
+
+// First chunk of segment s of a split into `segs` (s = segs gives n): segment 0 weighs 1,
+// every other segment 2.
+__device__ __host__ __forceinline__ int gdn_seg_bound(int s, int n, int segs) {
+    if (segs <= 1) return s == 0 ? 0 : n;
+    if (s <= 0) return 0;
+    if (s >= segs) return n;
+    return (int)((int64_t)n * (2 * s - 1) / (2 * segs - 1));
+}
+
 // tcgen05.mma kind::tf32 with A from TMEM: D (+)= A[tmem] * B[smem]
 __device__ __forceinline__ void mma_tf32_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                             uint32_t idesc, uint32_t accumulate) {
@@ -645,7 +674,7 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, uint64_
 
 __global__ void __launch_bounds__(gt::kThreadsTC, 1)
 gdn_tc_scan_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap tg,
-                   const __grid_constant__ CUtensorMap tkt, GdnArgs a, unsigned *err) {
+                   const __grid_constant__ CUtensorMap tkt, GdnArgs a, ScanPlan sp, unsigned *err) {
     using namespace gt;
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) &
@@ -653,11 +682,40 @@ gdn_tc_scan_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + BAR);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + TSLOT);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t bh = blockIdx.x;
+    // CTA -> (batch and head, segment, output or transition, and of a transition E or M)
+    const int64_t BH = a.nblk / a.nchunks;
+    bool trans = false;
+    int seg = 0, part = 0;   // part 1: the linear part M
+    int64_t bh = 0;
+    if (sp.mode == 0) {
+        const int nout = sp.segs - sp.s0;
+        seg = sp.s0 + (int)(blockIdx.x % nout);
+        bh = blockIdx.x / nout;
+    } else if ((int64_t)blockIdx.x < BH) {
+        bh = blockIdx.x;   // segment 0's outputs
+    } else {
+        const int64_t t = blockIdx.x - BH;
+        trans = true;
+        part = (int)(t & 1);
+        seg = 1 + (int)((t >> 1) % (sp.segs - 2));
+        bh = (t >> 1) / (sp.segs - 2);
+    }
     const int64_t bb = bh / a.H, h = bh % a.H;
-    const int n = a.nchunks;
-    const int64_t blk0 = bh * n;
+    const int cb = gdn_seg_bound(seg, a.nchunks, sp.segs);
+    const int ce = gdn_seg_bound(seg + 1, a.nchunks, sp.segs);
+    const int n = ce - cb;                     // chunks of this segment
+    const int64_t blk0 = bh * a.nchunks + cb;  // workspace index of its first chunk
     const SoA so(a.ws, a.nblk, kMaxD, kMaxD);
+    const bool lin = trans && part == 1;       // Ut = 0, no outputs
+    // start state: h0, a segment start state, zero (E) or the identity (M)
+    const float *init = trans ? nullptr
+                      : seg == 0 ? (a.h0 ? a.h0 + bh * kMaxD * kMaxD : nullptr)
+                                 : sp.Ss + (bh * (sp.segs - 1) + seg - 1) * kMaxD * kMaxD;
+    // final state: hT after the last segment; the start state of segment 1 after segment 0;
+    // E or M of a transition
+    float *fin = trans ? (part ? sp.M : sp.E) + (bh * (sp.segs - 1) + seg) * kMaxD * kMaxD
+               : seg == sp.segs - 1 ? (a.hT ? a.hT + bh * kMaxD * kMaxD : nullptr)
+               : seg == 0 ? sp.Ss + bh * (sp.segs - 1) * kMaxD * kMaxD : nullptr;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -688,7 +746,8 @@ gdn_tc_scan_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant
             uint32_t r[16];
 #pragma unroll
             for (int x = 0; x < 16; ++x)
-                r[x] = a.h0 ? __float_as_uint(a.h0[(bh * kMaxD + d0 + x) * kMaxD + v]) : 0u;
+                r[x] = lin ? (d0 + x == v ? 0x3f800000u : 0u)
+                           : init ? __float_as_uint(init[(d0 + x) * kMaxD + v]) : 0u;
             tc::tmem_st16(tc::tmem_addr(tm, j, kS + d0), r);
         }
         tc::tmem_wait_st();
@@ -705,28 +764,30 @@ gdn_tc_scan_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant
             // the fp32 Ut and Oi tiles the U and O warps read with plain loads: brought into L2
             // two chunks ahead, so their loads do not wait on DRAM
             constexpr uint32_t kTile = kC * kMaxD * sizeof(float);
+            // (a transition reads no Oi, and its linear part no Ut)
             for (int c = 0; c < 2 && c < n; ++c) {
-                prefetch_l2(so.U + (blk0 + c) * kC * kMaxD, kTile);
-                prefetch_l2(so.O + (blk0 + c) * kC * kMaxD, kTile);
+                if (!lin) prefetch_l2(so.U + (blk0 + c) * kC * kMaxD, kTile);
+                if (!trans) prefetch_l2(so.O + (blk0 + c) * kC * kMaxD, kTile);
             }
             for (int c = 0; c < n && ok; ++c) {
                 const int st = c % kStages;
                 if (c + 2 < n) {
-                    prefetch_l2(so.U + (blk0 + c + 2) * kC * kMaxD, kTile);
-                    prefetch_l2(so.O + (blk0 + c + 2) * kC * kMaxD, kTile);
+                    if (!lin) prefetch_l2(so.U + (blk0 + c + 2) * kC * kMaxD, kTile);
+                    if (!trans) prefetch_l2(so.O + (blk0 + c + 2) * kC * kMaxD, kTile);
                 }
                 if (c >= kStages && !tc::mbar_wait(&bars[EMPTY + st], ((c / kStages) - 1) & 1)) {
                     ok = false;
                     break;
                 }
                 uint64_t *fb = &bars[FULL + st];
-                tc::mbar_arrive_expect_tx(fb, STAGE);
+                // a transition multiplies by W only: no G slabs
+                tc::mbar_arrive_expect_tx(fb, trans ? STAGE - 4 * 8192 : STAGE);
                 uint8_t *base = sm + st * STAGE;
                 const int row = (int)((blk0 + c) * kC);
 #pragma unroll
                 for (int sl = 0; sl < 4; ++sl) {
                     tma_load_2d(base + WG + sl * WGSLAB, &tw, fb, 32 * sl, row);
-                    tma_load_2d(base + WG + sl * WGSLAB + 8192, &tg, fb, 32 * sl, row);
+                    if (!trans) tma_load_2d(base + WG + sl * WGSLAB + 8192, &tg, fb, 32 * sl, row);
                 }
                 const int krow = (int)((blk0 + c) * kMaxD);
 #pragma unroll
@@ -743,7 +804,8 @@ gdn_tc_scan_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant
         __syncwarp();
     } else if (warp == 1) {
         // ---- MMA issuer (converged warp, one elected lane issues)
-        const uint32_t idWG = idesc_tf32(128, 128), idUP = idesc_tf32(128, 128);
+        // a transition needs W S~ only: N = 64 (the W rows of each slab)
+        const uint32_t idWG = idesc_tf32(128, trans ? 64 : 128), idUP = idesc_tf32(128, 128);
         for (int c = 0; c < n; ++c) {
             const int st = c % kStages, wb = c & 1;
             bool w = tc::mbar_wait(&bars[FULL + st], (c / kStages) & 1);
@@ -787,7 +849,7 @@ gdn_tc_scan_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant
         auto load_ut = [&](int c) {
             const float *src = so.U + ((blk0 + c) * kC + t0) * kMaxD + v;
 #pragma unroll
-            for (int x = 0; x < 32; ++x) ut[x] = src[x * kMaxD];
+            for (int x = 0; x < 32; ++x) ut[x] = lin ? 0.f : src[x * kMaxD];
         };
         if (n > 0) load_ut(0);
         for (int c = 0; c < n; ++c) {
@@ -844,8 +906,9 @@ gdn_tc_scan_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant
             L = Ln;
             if (c + 1 < n) load_ut(c + 1);
         }
-        // final state hT = 2^L S~ (transposed back), once every update has completed
-        if (ok && a.hT) {
+        // final state 2^L S~ (transposed back: hT, or E / M of a transition), once every
+        // update has completed
+        if (ok && fin) {
             if (!tc::mbar_wait(&bars[FIN], 0)) {
                 ok = false;
             } else {
@@ -859,7 +922,7 @@ gdn_tc_scan_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant
                     tc::reg_fence(r);
 #pragma unroll
                     for (int x = 0; x < 16; ++x)
-                        a.hT[(bh * kMaxD + d0 + x) * kMaxD + v] = __uint_as_float(r[x]) * eL;
+                        fin[(d0 + x) * kMaxD + v] = __uint_as_float(r[x]) * eL;
                 }
             }
         }
@@ -874,14 +937,20 @@ gdn_tc_scan_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant
 #pragma unroll
             for (int x = 0; x < 32; ++x) oi[x] = src[x * kMaxD];
         };
-        if (n > 0) load_oi(0);
+        if (n > 0 && !trans) load_oi(0);
         for (int c = 0; c < n; ++c) {
             const float bsum = so.C[blk0 + c];
             const bool w = tc::mbar_wait(&bars[WGD + (c & 1)], (c >> 1) & 1);
             if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
             tc::tc_fence_after();
+            if (trans) {   // no outputs: only hand the accumulator back
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&bars[WGF + (c & 1)]);
+                continue;
+            }
             const float eL = ex2f(L);
-            const int64_t tb = (int64_t)c * kC;
+            const int64_t tb = (int64_t)(cb + c) * kC;
             const int vr = (int)(a.T - tb < kC ? a.T - tb : kC);
             __nv_bfloat16 *op = o + ((bb * a.T + tb) * a.H + h) * kMaxD + v;
             const int64_t rs = (int64_t)a.H * kMaxD;
@@ -1408,13 +1477,87 @@ gdn_tc_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     if (!ok) atomicOr(err, kDevErrTimeout);
 }
 
+// Start states of the segments of a split scan: S_start(1) is segment 0's end state, and
+// S_start(s + 1) = M_s S_start(s) + E_s for s = 1 .. segs - 2, in fp32. One CTA per (batch and
+// head, block of 16 value columns); thread (v, r) owns value column v of key rows r + 16 i,
+// i < 8, so each S element read from shared memory feeds eight products. Each M_s is first copied
+// into shared memory with coalesced loads (rows padded against bank conflicts).
+constexpr int kSegCols = 16;
+constexpr int kSegMStride = kMaxD + 4;
+constexpr size_t kSegSmem = (size_t)(kMaxD * kSegMStride + kMaxD * kSegCols) * sizeof(float);
+__global__ void __launch_bounds__(256) gdn_seg_scan_kernel(ScanPlan sp) {
+    extern __shared__ __align__(16) float segsm[];
+    float *Ms = segsm;                       // [128][kSegMStride]
+    float *S = segsm + kMaxD * kSegMStride;  // [128][kSegCols]
+    const int64_t bh = blockIdx.x;
+    const int c0 = blockIdx.y * kSegCols;
+    // key rows rb + 16 i: the two row groups of a warp sit in different banks
+    const int v = threadIdx.x & (kSegCols - 1), rb = threadIdx.x >> 4;
+    // S_start(1): the end state of segment 0, written by its output CTA
+    const float *s1 = sp.Ss + (size_t)bh * (sp.segs - 1) * kMaxD * kMaxD;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) S[(rb + 16 * i) * kSegCols + v] = s1[(size_t)(rb + 16 * i) * kMaxD + c0 + v];
+    for (int sg = 1; sg < sp.segs - 1; ++sg) {
+        const size_t o = (size_t)(bh * (sp.segs - 1) + sg) * kMaxD * kMaxD;
+        {   // M_s: 4096 float4, 16 per thread, all in flight together
+            const float4 *src = reinterpret_cast<const float4 *>(sp.M + o);
+            float4 r[16];
+#pragma unroll
+            for (int x = 0; x < 16; ++x) r[x] = src[threadIdx.x + 256 * x];
+#pragma unroll
+            for (int x = 0; x < 16; ++x) {
+                const int f = threadIdx.x + 256 * x, row = f >> 5, col = (f & 31) * 4;
+                *reinterpret_cast<float4 *>(Ms + row * kSegMStride + col) = r[x];
+            }
+        }
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = sp.E[o + (size_t)(rb + 16 * i) * kMaxD + c0 + v];
+        __syncthreads();   // M_s (and the previous step's S) in shared memory
+#pragma unroll 2
+        for (int e = 0; e < kMaxD; e += 4) {
+            const float s0 = S[e * kSegCols + v], s1v = S[(e + 1) * kSegCols + v];
+            const float s2 = S[(e + 2) * kSegCols + v], s3 = S[(e + 3) * kSegCols + v];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 m = *reinterpret_cast<const float4 *>(Ms + (rb + 16 * i) * kSegMStride + e);
+                acc[i] = fmaf(m.x, s0, fmaf(m.y, s1v, fmaf(m.z, s2, fmaf(m.w, s3, acc[i]))));
+            }
+        }
+        __syncthreads();   // every thread has read S and M_s
+        float *out = sp.Ss + o;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            S[(rb + 16 * i) * kSegCols + v] = acc[i];
+            out[(size_t)(rb + 16 * i) * kMaxD + c0 + v] = acc[i];
+        }
+    }
+}
+
+// Segments of the tensor-core scan: the most whose first launch (segment 0's outputs and two
+// transition CTAs per middle segment) still fits one wave of one-CTA-per-SM launches, with
+// segment 0 at least 4 chunks. Fewer than three segments gain nothing (segment 1 would wait
+// for all of segment 0), so the split is then off.
+int gdn_tc_segments(int64_t BH, int nchunks, int num_sms) {
+    int64_t s = (num_sms / BH - 1) / 2 + 2;
+    s = std::min<int64_t>(s, (nchunks / 4 + 1) / 2);
+    s = std::min<int64_t>(s, 16);
+    return s >= 3 ? (int)s : 1;
+}
+
+// Floats of the split scan's arrays (E, M, start states) behind the per-chunk workspace.
+int64_t gdn_seg_floats(int64_t BH, int segs) {
+    return segs > 1 ? 3 * BH * (segs - 1) * (int64_t)kMaxD * kMaxD : 0;
+}
+
 constexpr size_t kPrepSmem = (size_t)(2 * kMaxD * kPrepStride + 2 * kC * kC + 5 * kC) * sizeof(float);
 
 // Shared-memory opt-in of the tensor-core scan, once per device.
 std::mutex g_gdn_attr_mu;
 bool g_gdn_attr_done[64];
 
-cudaError_t launch_tc_scan(const GdnArgs &a, int64_t BH, unsigned *err, cudaStream_t s) {
+cudaError_t launch_tc_scan(const GdnArgs &a, int64_t BH, int num_sms, unsigned *err,
+                           cudaStream_t s) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -1424,6 +1567,9 @@ cudaError_t launch_tc_scan(const GdnArgs &a, int64_t BH, unsigned *err, cudaStre
         if (!g_gdn_attr_done[dev]) {
             e = cudaFuncSetAttribute(gdn_tc_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)gt::ALLOC);
+            if (e != cudaSuccess) return e;
+            e = cudaFuncSetAttribute(gdn_seg_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kSegSmem);
             if (e != cudaSuccess) return e;
             g_gdn_attr_done[dev] = true;
         }
@@ -1437,7 +1583,29 @@ cudaError_t launch_tc_scan(const GdnArgs &a, int64_t BH, unsigned *err, cudaStre
         !make_2d_map(&mk, so.Kt, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.nblk * kMaxD, kC, 32, 128,
                      CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidResourceHandle;   // a tensor map could not be encoded
-    gdn_tc_scan_kernel<<<(unsigned)BH, gt::kThreadsTC, gt::ALLOC, s>>>(mw, mg, mk, a, err);
+    const int segs = gdn_tc_segments(BH, a.nchunks, num_sms);
+    ScanPlan sp{segs, 0, 0, nullptr, nullptr, nullptr};
+    if (segs > 1) {
+        // the split's arrays follow the per-chunk workspace
+        float *seg = a.ws + a.nblk * WsLayout(kMaxD, kMaxD).total;
+        const int64_t per = BH * (segs - 1) * (int64_t)kMaxD * kMaxD;
+        sp.E = seg;
+        sp.M = seg + per;
+        sp.Ss = seg + 2 * per;
+        sp.mode = 1;
+        gdn_tc_scan_kernel<<<(unsigned)(BH + BH * (segs - 2) * 2), gt::kThreadsTC, gt::ALLOC, s>>>(
+            mw, mg, mk, a, sp, err);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        gdn_seg_scan_kernel<<<dim3((unsigned)BH, kMaxD / kSegCols), 256, kSegSmem, s>>>(sp);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        count_launches(2);
+        sp.mode = 0;
+        sp.s0 = 1;
+    }
+    gdn_tc_scan_kernel<<<(unsigned)(BH * (segs - sp.s0)), gt::kThreadsTC, gt::ALLOC, s>>>(
+        mw, mg, mk, a, sp, err);
     return cudaGetLastError();
 }
 
@@ -1486,7 +1654,7 @@ cudaError_t launch_typed(const GdnArgs &a, int64_t BH, int num_sms, unsigned *er
     if (tc) {
         cudaError_t e = launch_tc_prep(a, BH / a.H, err, s);
         if (e != cudaSuccess) return e;
-        e = launch_tc_scan(a, BH, err, s);
+        e = launch_tc_scan(a, BH, num_sms, err, s);
         if (e == cudaSuccess) count_launches(2);
         return e;
     }
@@ -1522,9 +1690,14 @@ bool gdn_supported(int64_t Dk, int64_t Dv) {
     return Dk >= 4 && Dk <= kMaxD && Dk % 4 == 0 && Dv >= 16 && Dv <= kMaxD && Dv % 16 == 0;
 }
 
-size_t gdn_workspace_bytes(int64_t B, int64_t T, int64_t H, int64_t Dk, int64_t Dv) {
+size_t gdn_workspace_bytes(int64_t B, int64_t T, int64_t H, int64_t Dk, int64_t Dv, int num_sms) {
     const int64_t nchunks = (T + kC - 1) / kC;
-    return (size_t)(B * H * nchunks) * (size_t)WsLayout((int)Dk, (int)Dv).total * sizeof(float);
+    // head dims 128 may take the tensor-core scan, whose split adds its segment arrays
+    const int64_t seg = (Dk == kMaxD && Dv == kMaxD)
+                            ? gdn_seg_floats(B * H, gdn_tc_segments(B * H, (int)nchunks, num_sms))
+                            : 0;
+    return ((size_t)(B * H * nchunks) * (size_t)WsLayout((int)Dk, (int)Dv).total + (size_t)seg) *
+           sizeof(float);
 }
 
 cudaError_t launch_gdn(const GdnProblem &p, void *ws, int num_sms, unsigned *err,

@@ -428,7 +428,9 @@ size_t gdn_fwd_workspace_size(int64_t B, int64_t T, int64_t H, int64_t Dk, int64
     Sizes sz;
     if (validate_shape(B, T, H, Dk, Dv, GLA_IO_BF16, &sz) != GLA_OK) return 0;
     if (!gla::gdn_supported(Dk, Dv) || sz.nqk == 0) return 0;
-    return gla::gdn_workspace_bytes(B, T, H, Dk, Dv);
+    DeviceState *st = nullptr;
+    const int sms = current_device(&st) == GLA_OK ? st->num_sms : 152;
+    return gla::gdn_workspace_bytes(B, T, H, Dk, Dv, sms);
 }
 
 gla_status gdn_fwd(const void *q, const void *k, const void *v, const float *g_log,
@@ -454,7 +456,12 @@ gla_status gdn_fwd(const void *q, const void *k, const void *v, const float *g_l
             return GLA_ERR_ALIAS;
     }
     if (overlap(o, bv, hT, bs)) return GLA_ERR_ALIAS;
-    const size_t need = empty ? 0 : gla::gdn_workspace_bytes(B, T, H, Dk, Dv);
+    // the size the caller got from gdn_fwd_workspace_size on this device (the device itself is
+    // checked below, after the caller's arguments)
+    DeviceState *st = nullptr;
+    const gla_status dev_rc = current_device(&st);
+    const int sms = dev_rc == GLA_OK ? st->num_sms : 152;
+    const size_t need = empty ? 0 : gla::gdn_workspace_bytes(B, T, H, Dk, Dv, sms);
     if (workspace) {
         if (misaligned(workspace) || workspace_bytes < need) return GLA_ERR_WORKSPACE;
         for (int i = 0; i < 6; ++i)
@@ -462,9 +469,7 @@ gla_status gdn_fwd(const void *q, const void *k, const void *v, const float *g_l
         if (overlap(workspace, need, o, bv) || overlap(workspace, need, hT, bs))
             return GLA_ERR_WORKSPACE;
     }
-    DeviceState *st = nullptr;
-    rc = current_device(&st);
-    if (rc != GLA_OK) return rc;
+    if (dev_rc != GLA_OK) return dev_rc;
     if (empty) {
         // no tokens: the final state is the initial one (zero without h0)
         if (T == 0 && B * H > 0 && hT) {

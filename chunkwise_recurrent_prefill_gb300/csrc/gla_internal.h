@@ -81,7 +81,8 @@ struct GdnProblem {
     int io;
 };
 bool gdn_supported(int64_t Dk, int64_t Dv);
-size_t gdn_workspace_bytes(int64_t B, int64_t T, int64_t H, int64_t Dk, int64_t Dv);
+// Workspace of gdn_fwd on a device with num_sms SMs (the tensor-core scan's split depends on it).
+size_t gdn_workspace_bytes(int64_t B, int64_t T, int64_t H, int64_t Dk, int64_t Dv, int num_sms);
 cudaError_t launch_gdn(const GdnProblem &p, void *ws, int num_sms, unsigned int *dev_err,
                        cudaStream_t s);
 

@@ -261,7 +261,9 @@ gla_status gla_fwd_noalloc(const void *q, const void *k, const void *v, const fl
  * Dims: Dk a multiple of 4 in [4, 128], Dv a multiple of 16 in [16, 128]
  * (GLA_ERR_UNSUPPORTED_DIM otherwise). Pointers are device pointers, 16-byte aligned
  * (GLA_ERR_MISALIGNED); o and hT must not overlap an input or each other (GLA_ERR_ALIAS).
- * Workspace: gdn_fwd_workspace_size() bytes of device memory, 16-byte aligned; pass NULL
+ * Workspace: gdn_fwd_workspace_size() bytes of device memory (the size depends on the
+ * current device: with few (batch, head) pairs the tensor-core scan splits the sequence over
+ * its SMs and keeps the segments' transitions there), 16-byte aligned; pass NULL
  * to use the library's workspace of `stream` (one per stream and device, shared with
  * gla_fwd_ex calls on that stream; see gla_options.workspace).
  * A caller workspace smaller than needed, misaligned, or overlapping an argument returns

@@ -44,8 +44,12 @@ def _inputs(B, T, H, io, seed, h0=False, Dk=128, Dv=128):
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])
 @pytest.mark.parametrize("B,T,H,h0", [(1, 64, 2, False), (1, 200, 3, True), (2, 129, 2, True),
-                                      (1, 1, 2, True), (1, 63, 1, False), (2, 700, 4, True)])
+                                      (1, 1, 2, True), (1, 63, 1, False), (2, 700, 4, True),
+                                      (1, 1700, 1, True), (1, 2048, 2, True), (2, 1500, 1, False)])
 def test_small_cases(io, B, T, H, h0):
+    """bf16 at head dims 128 runs the tensor-core kernels; with few heads and enough chunks
+    their scan splits the sequence (T=1700, H=1: 3 segments, the last ending in a ragged
+    chunk; T=2048, H=2: 4 segments; B=2, T=1500: 3 segments per sequence, no h0)."""
     x = _inputs(B, T, H, io, seed=T * 7 + B + H, h0=h0)
     o, hT = _run(x)
     o_ref, h_ref = _oracle(x)
@@ -174,7 +178,7 @@ def test_degenerate_gates(io):
     """Full forgetting (g = -1e4: every in-chunk decay underflows to 0, and the masked
     exponentials above the diagonal overflow, which must never reach a product) and no
     writes (beta = 0: the state only decays), against the oracle."""
-    x = _inputs(1, 200, 2, io, seed=31, h0=True)
+    x = _inputs(1, 1600, 2, io, seed=31, h0=True)   # bf16: a 3-segment split scan
     xf = {**x, "g": torch.full_like(x["g"], -1e4)}
     o, hT = _run(xf)
     assert torch.isfinite(o.float()).all() and torch.isfinite(hT).all()
