@@ -1493,27 +1493,34 @@ __global__ void __launch_bounds__(256) gdn_seg_scan_kernel(ScanPlan sp) {
     const int c0 = blockIdx.y * kSegCols;
     // key rows rb + 16 i: the two row groups of a warp sit in different banks
     const int v = threadIdx.x & (kSegCols - 1), rb = threadIdx.x >> 4;
+    const size_t step = (size_t)kMaxD * kMaxD;
+    const size_t base = (size_t)bh * (sp.segs - 1) * step;
     // S_start(1): the end state of segment 0, written by its output CTA
-    const float *s1 = sp.Ss + (size_t)bh * (sp.segs - 1) * kMaxD * kMaxD;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) S[(rb + 16 * i) * kSegCols + v] = s1[(size_t)(rb + 16 * i) * kMaxD + c0 + v];
+    for (int i = 0; i < 8; ++i)
+        S[(rb + 16 * i) * kSegCols + v] = sp.Ss[base + (size_t)(rb + 16 * i) * kMaxD + c0 + v];
+    // M_s and E_s of the next step are loaded while the current step computes
+    float4 mr[16];
+    float er[8];
+    auto load_step = [&](int sg) {
+        const float4 *src = reinterpret_cast<const float4 *>(sp.M + base + sg * step);
+#pragma unroll
+        for (int x = 0; x < 16; ++x) mr[x] = src[threadIdx.x + 256 * x];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) er[i] = sp.E[base + sg * step + (size_t)(rb + 16 * i) * kMaxD + c0 + v];
+    };
+    if (sp.segs > 2) load_step(1);
     for (int sg = 1; sg < sp.segs - 1; ++sg) {
-        const size_t o = (size_t)(bh * (sp.segs - 1) + sg) * kMaxD * kMaxD;
-        {   // M_s: 4096 float4, 16 per thread, all in flight together
-            const float4 *src = reinterpret_cast<const float4 *>(sp.M + o);
-            float4 r[16];
 #pragma unroll
-            for (int x = 0; x < 16; ++x) r[x] = src[threadIdx.x + 256 * x];
-#pragma unroll
-            for (int x = 0; x < 16; ++x) {
-                const int f = threadIdx.x + 256 * x, row = f >> 5, col = (f & 31) * 4;
-                *reinterpret_cast<float4 *>(Ms + row * kSegMStride + col) = r[x];
-            }
+        for (int x = 0; x < 16; ++x) {   // M_s into shared memory (4096 float4, coalesced)
+            const int f = threadIdx.x + 256 * x, row = f >> 5, col = (f & 31) * 4;
+            *reinterpret_cast<float4 *>(Ms + row * kSegMStride + col) = mr[x];
         }
         float acc[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = sp.E[o + (size_t)(rb + 16 * i) * kMaxD + c0 + v];
+        for (int i = 0; i < 8; ++i) acc[i] = er[i];
         __syncthreads();   // M_s (and the previous step's S) in shared memory
+        if (sg + 1 < sp.segs - 1) load_step(sg + 1);
 #pragma unroll 2
         for (int e = 0; e < kMaxD; e += 4) {
             const float s0 = S[e * kSegCols + v], s1v = S[(e + 1) * kSegCols + v];
@@ -1525,7 +1532,7 @@ __global__ void __launch_bounds__(256) gdn_seg_scan_kernel(ScanPlan sp) {
             }
         }
         __syncthreads();   // every thread has read S and M_s
-        float *out = sp.Ss + o;
+        float *out = sp.Ss + base + sg * step;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             S[(rb + 16 * i) * kSegCols + v] = acc[i];
