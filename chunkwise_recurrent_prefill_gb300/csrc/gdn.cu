@@ -62,6 +62,13 @@ __device__ __forceinline__ float4 ld4<__nv_bfloat16>(const __nv_bfloat16 *p) {
     return make_float4(lo.x, lo.y, hi.x, hi.y);
 }
 
+// x -> (hi, lo) bf16 pairs with hi = bf16(x), lo = bf16(x - hi), two elements per word
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+    hi = tc::pack_bf16(x0, x1);
+    const float2 f = tc::unpack_bf16(hi);
+    lo = tc::pack_bf16(x0 - f.x, x1 - f.y);
+}
+
 // Workspace of one (batch, head, chunk), in floats (every offset a multiple of 4):
 //   Wt [Dk][64]  W transposed                    Ut [64][Dv] the solved values
 //   Gt [Dk][64]  (Qh - P W) transposed, Qh = scale exp(b_i) q_i
@@ -85,17 +92,20 @@ struct WsLayout {
 
 // Workspace of the tensor-core scan (bf16 I/O, Dk = Dv = 128): one array per quantity, so
 // that each is a plain 2-D tensor the scan can tile with TMA. For chunk blk = bh * nchunks + c:
-//   W [blk][64][Dk]    G [blk][64][Dk]    Kt [blk][Dk][64] (Kh transposed)
-//   U [blk][64][Dv]    O [blk][64][Dv]    C [blk] (b_63, the chunk's summed log-gate)
+//   W [blk][64][Dk]    G [blk][64][Dk]    U [blk][64][Dv]    O [blk][64][Dv]
+//   EK [blk][64] (e^(b_63 - b_j), the decay from token j to the chunk's end)
+//   C [blk] (b_63, the chunk's summed log-gate)
+// (the scan takes k itself, in bf16, for the state update). It fits in the per-chunk layout
+// above, which sizes the workspace of both routes.
 struct SoA {
-    float *W, *G, *Kt, *U, *O, *C;
+    float *W, *G, *U, *O, *EK, *C;
     __host__ __device__ SoA(float *ws, int64_t nblk, int Dk, int Dv) {
         W = ws;
         G = W + nblk * kC * Dk;
-        Kt = G + nblk * kC * Dk;
-        U = Kt + nblk * Dk * kC;
+        U = G + nblk * kC * Dk;
         O = U + nblk * kC * Dv;
-        C = O + nblk * kC * Dv;
+        EK = O + nblk * kC * Dv;
+        C = EK + nblk * kC;
     }
 };
 
@@ -577,10 +587,11 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_scan_kernel(GdnArgs a) {
 // Serial part on the tensor cores (bf16 I/O, Dk = Dv = 128): one CTA per (batch, head), the
 // fp32 state kept in TMEM across all chunks, transposed (lane = value column v, column = key
 // row d) and decay-normalised: S = 2^L S~ with one scalar L per head (the gate is one per
-// token). Per chunk c, with the prep's W, G, Kh, Ut, Oi and b_63:
+// token). Per chunk c, with the prep's W, G, Ut, Oi, e^(b_63 - b_j) and b_63, and k:
 //   [W S | G S]^T = S~^T [W | G]^T 2^L    one MMA chain, A = S~^T straight from TMEM (tf32)
 //   U = Ut - 2^L (W S~),  O = Oi + 2^L (G S~)                      (CUDA cores, fp32)
-//   S~ += (2^-L' U)^T Kh,  L' = L + b_63 log2(e)      A = the scaled U^T, from TMEM (tf32)
+//   S~ += sum_j (2^-L' e^(b_63 - b_j) U_j)^T k_j,  L' = L + b_63 log2(e):  A = the scaled U^T
+//   from TMEM as a bf16 hi / lo pair (about 16 significant bits), B = k exact in bf16
 // The state is rescaled (S~ <- 2^L' S~, L' <- 0) when |L'| passes kRenormL2, before the
 // update that would use it; a full-forgetting chunk (b_63 very negative) so zeroes S~.
 // tf32 operands (10-bit mantissa) keep the fp32 state's accuracy far inside the bf16 output
@@ -589,8 +600,9 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_scan_kernel(GdnArgs a) {
 namespace gt {
 constexpr int kStages = 2;
 // stage: four [W | G] slabs (dk 32 s .. 32 s + 31: W rows then G rows, 128 rows x 128 B,
-// 128B-swizzled, one swizzle atom per 8 rows) and two Kh^T boxes (tokens 32 s .., 128 rows)
-constexpr uint32_t WG = 0, WGSLAB = 16384, KT = 65536, KTBOX = 16384, STAGE = 98304;
+// 128B-swizzled, one swizzle atom per 8 rows), the chunk's k (bf16, two 128B-swizzled
+// [64 tokens x 64 dk] boxes) and its 64 decay factors e^(b_63 - b_j)
+constexpr uint32_t WG = 0, WGSLAB = 16384, KB = 65536, EKO = 81920, STAGE = 82944;
 constexpr uint32_t BAR = kStages * STAGE;
 constexpr uint32_t NBAR = 12;
 constexpr uint32_t TSLOT = BAR + NBAR * 8;
@@ -598,7 +610,8 @@ constexpr uint32_t ALLOC = TSLOT + 16 + 1024;
 // TMEM columns
 constexpr uint32_t kS = 0;       // S~^T, 128 columns
 constexpr uint32_t kWG = 128;    // [W S~ | G S~]^T, 2 x 128 columns (double buffered)
-constexpr uint32_t kU = 384;     // scaled U^T (A operand of the update), 64 columns
+constexpr uint32_t kU = 384;     // scaled U^T as bf16 hi (32 columns) and lo (32 columns):
+                                 // the A operand of the update
 constexpr int kThreadsTC = 18 * 32;   // producer, MMA issuer, 8 U warps, 8 O warps
 constexpr float kRenormL2 = 60.f;
 enum { FULL = 0, EMPTY = 2, WGD = 4, WGF = 6, URDY = 8, FIN = 9 };
@@ -674,7 +687,8 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, uint64_
 
 __global__ void __launch_bounds__(gt::kThreadsTC, 1)
 gdn_tc_scan_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap tg,
-                   const __grid_constant__ CUtensorMap tkt, GdnArgs a, ScanPlan sp, unsigned *err) {
+                   const __grid_constant__ CUtensorMap tk4, const __grid_constant__ CUtensorMap tek,
+                   GdnArgs a, ScanPlan sp, unsigned *err) {
     using namespace gt;
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) &
@@ -731,7 +745,8 @@ gdn_tc_scan_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant
     if (warp == 0 && lane == 0) {
         tc::tma_prefetch_desc(&tw);
         tc::tma_prefetch_desc(&tg);
-        tc::tma_prefetch_desc(&tkt);
+        tc::tma_prefetch_desc(&tk4);
+        tc::tma_prefetch_desc(&tek);
     }
     if (warp == 1) tc::tmem_alloc(tslot, 512);
     tc::tc_fence_before();
@@ -758,7 +773,7 @@ gdn_tc_scan_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant
     bool ok = true;
 
     if (warp == 0) {
-        // ---- TMA producer: [W | G] slabs and Kh^T boxes of each chunk
+        // ---- TMA producer: [W | G] slabs, k and the decay factors of each chunk
         if (lane == 0) {
             int issued = 0;
             // the fp32 Ut and Oi tiles the U and O warps read with plain loads: brought into L2
@@ -781,7 +796,7 @@ gdn_tc_scan_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant
                 }
                 uint64_t *fb = &bars[FULL + st];
                 // a transition multiplies by W only: no G slabs
-                tc::mbar_arrive_expect_tx(fb, trans ? STAGE - 4 * 8192 : STAGE);
+                tc::mbar_arrive_expect_tx(fb, (trans ? 32768u : 65536u) + 16384u + 256u);
                 uint8_t *base = sm + st * STAGE;
                 const int row = (int)((blk0 + c) * kC);
 #pragma unroll
@@ -789,10 +804,11 @@ gdn_tc_scan_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant
                     tma_load_2d(base + WG + sl * WGSLAB, &tw, fb, 32 * sl, row);
                     if (!trans) tma_load_2d(base + WG + sl * WGSLAB + 8192, &tg, fb, 32 * sl, row);
                 }
-                const int krow = (int)((blk0 + c) * kMaxD);
-#pragma unroll
-                for (int bx = 0; bx < 2; ++bx)
-                    tma_load_2d(base + KT + bx * KTBOX, &tkt, fb, 32 * bx, krow);
+                // k of the chunk (rows past the sequence end read as zero) and its decay factors
+                const int tk = (int)((int64_t)(cb + c) * kC);
+                tc::tma_load_4d(base + KB, &tk4, fb, 0, (int)h, tk, (int)bb);
+                tc::tma_load_4d(base + KB + 8192, &tk4, fb, 64, (int)h, tk, (int)bb);
+                tma_load_2d(base + EKO, &tek, fb, 0, (int)(blk0 + c));
                 ++issued;
             }
             // no bulk copy may still be landing when the CTA exits
@@ -805,7 +821,8 @@ gdn_tc_scan_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant
     } else if (warp == 1) {
         // ---- MMA issuer (converged warp, one elected lane issues)
         // a transition needs W S~ only: N = 64 (the W rows of each slab)
-        const uint32_t idWG = idesc_tf32(128, trans ? 64 : 128), idUP = idesc_tf32(128, 128);
+        const uint32_t idWG = idesc_tf32(128, trans ? 64 : 128);
+        const uint32_t idUP = tc::idesc_bf16(128, 128, 0, 1);   // A from TMEM, k MN-major
         for (int c = 0; c < n; ++c) {
             const int st = c % kStages, wb = c & 1;
             bool w = tc::mbar_wait(&bars[FULL + st], (c / kStages) & 1);
@@ -827,12 +844,13 @@ gdn_tc_scan_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant
             if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
             tc::tc_fence_after();
             if (tc::elect_one()) {
-                // S~^T += (scaled U)^T Kh: K = 64 tokens in 8 steps of 8
+                // S~^T += (scaled U)^T k: K = 64 tokens in 4 steps of 16, U hi then U lo
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_tf32_ts(tm + kS, tm + kU + kk * 8,
-                                tc::smem_desc(base + KT + (kk >> 2) * KTBOX + (kk & 3) * 32, 16, 1024),
-                                idUP, 1);
+                for (int hl = 0; hl < 2; ++hl)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc::mma_ts(tm + kS, tm + kU + hl * 32 + kk * 8,
+                                   tc::smem_desc(base + KB + kk * 2048, 8192, 1024), idUP, 1);
                 tc::mma_commit(&bars[EMPTY + st]);   // the stage's last reader
             }
             __syncwarp();
@@ -891,14 +909,19 @@ gdn_tc_scan_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant
                 Ln = 0.f;
             }
             const float su = ex2f(-Ln);
-            uint32_t u0[16], u1[16];
+            // decay factors of the chunk's tokens, in its stage (live until the update completes;
+            // the stage's barrier has completed, and cannot move on before this chunk's update)
+            if (!tc::mbar_wait(&bars[FULL + c % kStages], (c / kStages) & 1)) ok = false;
+            const float *eks = reinterpret_cast<const float *>(sm + (c % kStages) * STAGE + EKO) + t0;
+            uint32_t uh[16], ul[16];   // tokens t0 .. t0 + 31 in pairs: bf16 hi and lo
 #pragma unroll
             for (int x = 0; x < 16; ++x) {
-                u0[x] = __float_as_uint((ut[x] - eL * acc[x]) * su);
-                u1[x] = __float_as_uint((ut[16 + x] - eL * acc[16 + x]) * su);
+                const float a0 = (ut[2 * x] - eL * acc[2 * x]) * su * eks[2 * x];
+                const float a1 = (ut[2 * x + 1] - eL * acc[2 * x + 1]) * su * eks[2 * x + 1];
+                split2(a0, a1, uh[x], ul[x]);
             }
-            tc::tmem_st16(tc::tmem_addr(tm, j, kU + t0), u0);
-            tc::tmem_st16(tc::tmem_addr(tm, j, kU + t0 + 16), u1);
+            tc::tmem_st16(tc::tmem_addr(tm, j, kU + half * 16), uh);
+            tc::tmem_st16(tc::tmem_addr(tm, j, kU + 32 + half * 16), ul);
             tc::tmem_wait_st();
             tc::tc_fence_before();
             __syncwarp();
@@ -1049,12 +1072,6 @@ __device__ __forceinline__ void tmem_ld64f(uint32_t taddr, float (&out)[64]) {
     }
 }
 
-// x -> (hi, lo) bf16 pairs with hi = bf16(x), lo = bf16(x - hi), two elements per word
-__device__ __forceinline__ void split2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
-    hi = tc::pack_bf16(x0, x1);
-    const float2 f = tc::unpack_bf16(hi);
-    lo = tc::pack_bf16(x0 - f.x, x1 - f.y);
-}
 
 // Row `row` of a 64-column bf16 operand tile pair (hi at `hi`, lo at `lo`, 128B-swizzled):
 // the 64 values x[0..63] scaled by f.
@@ -1312,19 +1329,10 @@ gdn_tc_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 #pragma unroll
             for (int j = 0; j < kC; ++j) w[j] = j >= tid ? Ts[j * kAStride + tid] : 0.f;
         }
-    } else {
-        // Kh^T [d][j] = e^(b_63 - b_j) k_j[d], straight to global memory: each warp store is
-        // 32 tokens of one key row (128 bytes)
-        const bool wl = tc::mbar_wait(&bars[LOAD], 0);
-        ok &= wl;
-        float *kt = so.Kt + blk * kMaxD * kC;
-#pragma unroll 8
-        for (int it = 0; it < 64; ++it) {
-            const int rh = (warp - 4) * 64 + it, d = rh >> 1, j = (rh & 1) * 32 + lane;
-            const __nv_bfloat16 kv = *reinterpret_cast<const __nv_bfloat16 *>(
-                sm + KQ + (d >> 6) * 16384 + tc::sw128_offset(j, d & 63));
-            kt[d * kC + j] = ek[j] * __bfloat162float(kv);
-        }
+    } else if (warp == 4) {
+        // the decay factors e^(b_63 - b_j) of the chunk's tokens, for the scan's state update
+        so.EK[blk * kC + lane] = ek[lane];
+        so.EK[blk * kC + 32 + lane] = ek[32 + lane];
     }
     __syncthreads();   // A and T are dead from here
     if (tid < kC) {
@@ -1582,13 +1590,15 @@ cudaError_t launch_tc_scan(const GdnArgs &a, int64_t BH, int num_sms, unsigned *
         }
     }
     const SoA so(a.ws, a.nblk, kMaxD, kMaxD);
-    CUtensorMap mw, mg, mk;
+    CUtensorMap mw, mg, mk, me;
     if (!make_2d_map(&mw, so.W, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.nblk * kC, kMaxD, 32, 64,
                      CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_2d_map(&mg, so.G, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.nblk * kC, kMaxD, 32, 64,
                      CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_2d_map(&mk, so.Kt, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.nblk * kMaxD, kC, 32, 128,
-                     CU_TENSOR_MAP_SWIZZLE_128B))
+        !make_bthd_map(&mk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH / a.H, a.T, a.H, kMaxD,
+                       64, kC, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_2d_map(&me, so.EK, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.nblk, kC, kC, 1,
+                     CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidResourceHandle;   // a tensor map could not be encoded
     const int segs = gdn_tc_segments(BH, a.nchunks, num_sms);
     ScanPlan sp{segs, 0, 0, nullptr, nullptr, nullptr};
@@ -1601,7 +1611,7 @@ cudaError_t launch_tc_scan(const GdnArgs &a, int64_t BH, int num_sms, unsigned *
         sp.Ss = seg + 2 * per;
         sp.mode = 1;
         gdn_tc_scan_kernel<<<(unsigned)(BH + BH * (segs - 2) * 2), gt::kThreadsTC, gt::ALLOC, s>>>(
-            mw, mg, mk, a, sp, err);
+            mw, mg, mk, me, a, sp, err);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         gdn_seg_scan_kernel<<<dim3((unsigned)BH, kMaxD / kSegCols), 256, kSegSmem, s>>>(sp);
@@ -1612,7 +1622,7 @@ cudaError_t launch_tc_scan(const GdnArgs &a, int64_t BH, int num_sms, unsigned *
         sp.s0 = 1;
     }
     gdn_tc_scan_kernel<<<(unsigned)(BH * (segs - sp.s0)), gt::kThreadsTC, gt::ALLOC, s>>>(
-        mw, mg, mk, a, sp, err);
+        mw, mg, mk, me, a, sp, err);
     return cudaGetLastError();
 }
 
