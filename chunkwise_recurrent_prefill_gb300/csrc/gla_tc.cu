@@ -144,8 +144,10 @@ constexpr uint32_t NBAR = 26;
 constexpr uint32_t TSLOT = BAR + NBAR * 8;
 constexpr uint32_t ALLOC = TSLOT + 16 + 1024;
 static_assert(ALLOC <= 232448, "output kernel shared memory");
-static_assert(NQS * QSTAGE + 512 <= P, "scalar-gate stages and factors fit below the P tile");
 constexpr uint32_t FAC = NQS * QSTAGE;  // [64] float2 per-token factors (scalar gate)
+constexpr int NQF = 8;                  // scalar gate: ring of the output's per-token factors
+constexpr uint32_t QFR = FAC + 512;     // [NQF][64] f32
+static_assert(QFR + NQF * 256 <= P, "scalar-gate stages and factors fit below the P tile");
 }  // namespace om
 
 // mbarrier indices of the output kernel
@@ -619,6 +621,13 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             const int64_t t0 = tbase + (int64_t)(cb + c) * kC;
             const int64_t left = tend - t0;
             const int vr = left < kC ? (int)left : kC;   // rows of the sequence
+            if (kScalar) {
+                // a scalar gate's q is not scaled in place: O = f_t (S~^T q^T + V^T P'^T) with
+                // f_t = scale 2^(b_t + L) (1 in an extreme chunk, whose q is scaled)
+                const float *qf = reinterpret_cast<const float *>(sm + QFR) + (c & (NQF - 1)) * kC;
+#pragma unroll
+                for (int x = 0; x < kC; ++x) ov[x] *= qf[x];
+            }
             if (v < a.Dv) {
                 __nv_bfloat16 *op = a.o + ((((int64_t)bmap * a.T + t0) * a.H + h) * a.Dv) + v;
                 if (vr == kC) {
@@ -952,12 +961,20 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     if (q == pt) offt = Bt;
                     Bt = q == 0 ? tq : Bt + tq;
                 }
+                // the output's factor of this token, for the epilogue: q stays raw in a normal
+                // chunk (its factor applies to O), and is scaled in place in an extreme one. The
+                // ring slot of chunk c was last read by the epilogue of chunk c - NQF, which ended
+                // before the stage of chunk c - NQF + NQ could arrive.
+                float *qfr = reinterpret_cast<float *>(sm + QFR) + (c & (NQF - 1)) * kC;
                 if (!ext) {
                     const float eq = offt + Lq0 + lsc, ek = -(offt + Lq0);
-                    fac[gt] = make_float2(ex2(rt + eq), ex2(ek - rt));
+                    const float fq = ex2(rt + eq);
+                    fac[gt] = make_float2(fq, ex2(ek - rt));
+                    qfr[gt] = fq;
                 } else {
                     const float bt = offt + rt;
                     fac[gt] = make_float2(sc * ex2(bt), ex2(B0 - bt));
+                    qfr[gt] = 1.f;
                 }
             }
             w = mbar_wait(&bars[QFULL + qs], par(c / NQ));
@@ -984,7 +1001,8 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             // block costs one shared-memory round trip
             if (!ext) {
                 // Q' = scale q 2^(b + L), K' = k 2^-(b + L) with b = off + r: the per-chunk
-                // constants (offset, L, log2 scale) are folded into two exponent biases
+                // constants (offset, L, log2 scale) are folded into two exponent biases. With a
+                // scalar gate only k is scaled here (see the epilogue).
                 const float eq0 = off0 + Lq0 + lsc, eq1 = off1 + Lq1 + lsc;
                 const float ek0 = -(off0 + Lq0), ek1 = -(off1 + Lq1);
 #pragma unroll 1
@@ -995,18 +1013,19 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     for (int x = 0; x < kGateBlock; ++x) {
                         const uint32_t off = (uint32_t)(tb + t0) * 128u + swz[x];
                         gv[x] = gpair(t0 + x);
-                        qv[x] = *reinterpret_cast<const uint32_t *>(qt + off);
+                        if (!kScalar) qv[x] = *reinterpret_cast<const uint32_t *>(qt + off);
                         kv[x] = *reinterpret_cast<const uint32_t *>(kt + off);
                     }
 #pragma unroll
                     for (int x = 0; x < kGateBlock; ++x) {
-                        const float2 qf = unpack_bf16(qv[x]), kf = unpack_bf16(kv[x]);
+                        const float2 kf = unpack_bf16(kv[x]);
                         if (kScalar) {
-                            // one gate for every key dimension: the token's precomputed factors
-                            const float2 f = fac[tb + t0 + x];
-                            qv[x] = pack_bf16(qf.x * f.x, qf.y * f.x);
-                            kv[x] = pack_bf16(kf.x * f.y, kf.y * f.y);
+                            // one gate for every key dimension: the token's precomputed factor
+                            // (q stays raw: its factor multiplies the output in the epilogue)
+                            const float fk = fac[tb + t0 + x].y;
+                            kv[x] = pack_bf16(kf.x * fk, kf.y * fk);
                         } else {
+                            const float2 qf = unpack_bf16(qv[x]);
                             r0 = fmaf(gv[x].x, kLog2e, r0);
                             r1 = fmaf(gv[x].y, kLog2e, r1);
                             qv[x] = pack_bf16(qf.x * ex2(r0 + eq0), qf.y * ex2(r1 + eq1));
@@ -1016,7 +1035,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
 #pragma unroll
                     for (int x = 0; x < kGateBlock; ++x) {
                         const uint32_t off = (uint32_t)(tb + t0) * 128u + swz[x];
-                        *reinterpret_cast<uint32_t *>(qt + off) = qv[x];
+                        if (!kScalar) *reinterpret_cast<uint32_t *>(qt + off) = qv[x];
                         *reinterpret_cast<uint32_t *>(kt + off) = kv[x];
                     }
                 }
