@@ -46,10 +46,10 @@ def test_noalloc_host_checks():
     assert str(16 * 8 * PER_SEGMENT_HEAD) in detail and str(MAX_SCRATCH) in detail
 
 
-def _inputs(B, T, H, seed, with_h0=True):
+def _inputs(B, T, H, seed, with_h0=True, D=128):
     from chunkwise_recurrent_prefill_gb300.workloads import make_inputs, small
-    return make_inputs(small("noalloc", B=B, T=T, H=H, io="bf16", seed=seed, with_h0=with_h0),
-                       torch.device("cuda:0"))
+    return make_inputs(small("noalloc", B=B, T=T, H=H, io="bf16", seed=seed, with_h0=with_h0,
+                             Dk=D, Dv=D), torch.device("cuda:0"))
 
 
 def _oracle(x):
@@ -133,3 +133,15 @@ def test_noalloc_auto_split_one_head_long_sequence():
                          seq_splits=128)
     torch.cuda.synchronize()
     assert torch.equal(o, o128) and torch.equal(hT, h128)
+
+
+@pytest.mark.gpu
+def test_noalloc_head_pairs_d64():
+    """Head dims 64 with an even head count run as head pairs of dims 128: the split and its
+    scratch are those of the pair view. Here gla_fwd cuts each of the 8 pairs into 19 segments
+    (18.9 MB of scratch), so the automatic split of gla_fwd_noalloc is capped to fit the
+    array; the results still match the oracle and gla_fwd."""
+    from chunkwise_recurrent_prefill_gb300.gla import workspace_size
+    _lib()
+    assert workspace_size(1, 4096, 16, Dk=64, Dv=64) == 8 * 18 * 131584 > MAX_SCRATCH
+    _compare(_inputs(1, 4096, 16, seed=45, D=64), seq_splits=0)
