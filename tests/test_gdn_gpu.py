@@ -132,6 +132,14 @@ def test_caller_workspace_and_determinism():
         gdn_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], x["h0"],
                 workspace=ws[: need - 16])
     assert e.value.status == 9                                   # GLA_ERR_WORKSPACE
+    # a split scan (2 heads of 2048 tokens: 4 segments) keeps its segment arrays in the
+    # caller's workspace too: the reported size holds them, and the results are identical
+    x = _inputs(1, 2048, 2, "bf16", seed=22, h0=True)
+    o1, h1 = _run(x)
+    need = gdn_workspace_size(1, 2048, 2, 128, 128)
+    ws = torch.full((need,), 255, dtype=torch.uint8, device=DEV)   # stale contents must not matter
+    o3, h3 = _run(x, workspace=ws)
+    assert torch.equal(o1, o3) and torch.equal(h1, h3)
 
 
 def test_empty_and_no_state():
