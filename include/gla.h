@@ -35,6 +35,10 @@
  *
  * Execution: every call is asynchronous and ordered on `stream` (NULL = the legacy
  * default stream). No call synchronises the host, except gla_last_device_status().
+ * Calls may be captured into a CUDA graph (stream capture) once their scratch exists: pass a
+ * caller workspace, or make one call on the capturing stream first (the library's own
+ * workspace is allocated with cudaMalloc, which cannot happen during capture). A replay
+ * reads whatever the captured buffers then hold.
  *
  * Errors: every entry point returns a gla_status and never aborts, traps or throws.
  * Argument errors are detected on the host before any launch; nothing is written then.
