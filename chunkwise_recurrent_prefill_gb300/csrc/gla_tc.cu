@@ -147,7 +147,8 @@ static_assert(ALLOC <= 232448, "output kernel shared memory");
 constexpr uint32_t FAC = NQS * QSTAGE;  // [64] float2 per-token factors (scalar gate)
 constexpr int NQF = 8;                  // scalar gate: ring of the output's per-token factors
 constexpr uint32_t QFR = FAC + 512;     // [NQF][64] f32
-static_assert(QFR + NQF * 256 <= P, "scalar-gate stages and factors fit below the P tile");
+constexpr uint32_t RTOK = QFR + NQF * 256;  // [64] f32 running log2-gate sums within the ranges
+static_assert(RTOK + 256 <= P, "scalar-gate stages and factors fit below the P tile");
 }  // namespace om
 
 // mbarrier indices of the output kernel
@@ -159,14 +160,20 @@ enum {
 };
 static_assert(FIN < (int)om::NBAR, "output kernel barrier map");
 
-constexpr int kGateWarps = 6;          // warps 10..15 (4 warps with kGatePart 32 measured
+constexpr int kGateWarps = 6;          // warps 10..15 (4 warps with 32-token ranges measured
                                        // 3-5% slower at B*H = 64 and 256, equal at 16)
 constexpr int kOutThreads = (10 + kGateWarps) * 32;   // at most 4 warps per SM
                                                        // sub-partition: 128 registers
 constexpr int kGateThreads = kGateWarps * 32;
 constexpr int kGateParts = kGateThreads / 64;   // token ranges (one thread per key pair each)
-constexpr int kGatePart = 24;          // tokens per range (the last range takes the rest)
-static_assert(kGatePart * (kGateParts - 1) < 64 && kGatePart * kGateParts >= 64,
+// Token ranges [0, 24), [24, 56), [56, 64). Warp w runs on sub-partition w % 4: ranges 0 and 2
+// share sub-partitions 2 and 3 (warps 10, 14 and 11, 15), range 1 has 0 and 1 (warps 12, 13),
+// so every sub-partition scales 32 tokens of a chunk (equal ranges of 24, 24, 16 left 40 on
+// two of them).
+__host__ __device__ constexpr int gate_range_begin(int part) {
+    return part == 0 ? 0 : part == 1 ? 24 : part == 2 ? 56 : 64;
+}
+static_assert(kGateParts == 3 && gate_range_begin(kGateParts) == 64,
               "gate token ranges must cover the chunk");
 constexpr int kStateThreads = 320;     // 10 warps
 
@@ -841,20 +848,21 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     } else {
         // ------------------------------------------------------------ gate warps
         // Thread (part, dp) owns the key-dimension pair d = 2 dp, 2 dp + 1 over one of the
-        // kGateParts token ranges of a chunk (kGatePart tokens each). Pass 1 sums the range's
+        // kGateParts token ranges of a chunk (gate_range_begin). Pass 1 sums the range's
         // log2-gates and records the range of the running sums; the ranges exchange totals,
         // and the warps agree on the chunk's flags (extreme, renormalise). Pass 2 recomputes
         // the running sums while scaling q and k in place, two dimensions per 32-bit access.
         const int gt = (warp - 10) * 32 + lane;             // 0 .. kGateThreads - 1
         const int dp = gt & 63, part = gt >> 6;
-        const int tb = part * kGatePart;                    // first token of the range
-        const int tl = min(kGatePart, kC - tb);             // tokens in the range
+        const int tb = gate_range_begin(part);              // first token of the range
+        const int tl = gate_range_begin(part + 1) - tb;     // tokens in the range
         const int d = 2 * dp;
         const uint32_t boxo = (uint32_t)(d >> 6) * 8192;
         const uint32_t col = (uint32_t)(d & 63);
         // byte offsets of this thread's column within each row of an 8-row swizzle atom
         // (blocks start on multiples of 8 rows, so row % 8 is the index within the block)
-        static_assert(kGateBlock % 8 == 0 && kGatePart % kGateBlock == 0,
+        static_assert(kGateBlock % 8 == 0 && gate_range_begin(1) % kGateBlock == 0 &&
+                          gate_range_begin(2) % kGateBlock == 0,
                       "gate blocks must cover whole swizzle atoms");
         uint32_t swz[kGateBlock];
 #pragma unroll
@@ -867,6 +875,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         // of each chunk they are published in gsc[c & 1] (two buffers: no thread is ever more
         // than one chunk behind another, the loop has several barriers per chunk)
         float *gsc = reinterpret_cast<float *>(sm + GSC);
+        float *rtok = reinterpret_cast<float *>(sm + RTOK);
         auto fetch_scalar = [&](int c) -> float {
             const int64_t t = tbase + (int64_t)(cb + c) * kC + gt;
             return t < tend ? __ldg(a.g + ((int64_t)bmap * a.T + t) * a.H + h) : 0.f;
@@ -903,7 +912,8 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 }
                 return *reinterpret_cast<const float2 *>(grow + t * kD);
             };
-            float r0 = 0.f, r1 = 0.f;
+            const float2 l2e = make_float2(kLog2e, kLog2e);
+            float2 rs = make_float2(0.f, 0.f);                   // running sums of the pair
             float lo0 = 0.f, hi0 = 0.f, lo1 = 0.f, hi1 = 0.f;   // range of the running sums
 #pragma unroll 1
             for (int t0 = 0; t0 < tl; t0 += kGateBlock) {
@@ -912,14 +922,17 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 for (int x = 0; x < kGateBlock; ++x) gv[x] = gpair(t0 + x);
 #pragma unroll
                 for (int x = 0; x < kGateBlock; ++x) {
-                    r0 = fmaf(gv[x].x, kLog2e, r0);
-                    r1 = fmaf(gv[x].y, kLog2e, r1);
-                    lo0 = fminf(lo0, r0); hi0 = fmaxf(hi0, r0);
-                    lo1 = fminf(lo1, r1); hi1 = fmaxf(hi1, r1);
+                    rs = fma2(gv[x], l2e, rs);
+                    lo0 = fminf(lo0, rs.x); hi0 = fmaxf(hi0, rs.x);
+                    lo1 = fminf(lo1, rs.y); hi1 = fmaxf(hi1, rs.y);
+                    // scalar gate: every key pair forms the same sums; the first pair of each
+                    // range publishes them for the per-token factors below
+                    if (kScalar && dp == 0) rtok[tb + t0 + x] = rs.x;
                 }
             }
-            *reinterpret_cast<float2 *>(xch + part * kD + d) = make_float2(r0, r1);
-            named_bar_sync(1, kGateThreads);
+            *reinterpret_cast<float2 *>(xch + part * kD + d) = rs;
+            // the exchange barrier also ORs the renormalisation test of the state so far
+            const bool renL = named_bar_or(1, kGateThreads, fabsf(L0) > kRenorm2 || fabsf(L1) > kRenorm2);
             // b = off + (running sum within the range), with off the left-to-right sum of the
             // earlier ranges' totals; the chunk total is formed by the same additions, so that
             // b of the last token equals it exactly
@@ -935,8 +948,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             const float mx = fmaxf(fmaxf(fabsf(off0 + lo0), fabsf(off0 + hi0)),
                                    fmaxf(fabsf(off1 + lo1), fabsf(off1 + hi1)));
             const bool ext = named_bar_or(1, kGateThreads, mx > kExtreme2);
-            const bool ren =
-                named_bar_or(1, kGateThreads, fabsf(L0) > kRenorm2 || fabsf(L1) > kRenorm2) || ext;
+            const bool ren = renL || ext;
             if (gt == 0) TRACE_OUT(17, c);
             const float Lc0 = L0, Lc1 = L1;                     // before this chunk
             const float Lq0 = ren ? 0.f : L0, Lq1 = ren ? 0.f : L1;   // used by this chunk
@@ -944,16 +956,14 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             L1 = ext ? 0.f : Lq1 + B1;
             if (gt == 0) TRACE_OUT(18, c);
             // scalar gate: the factors are the same in every key dimension, so the 64 token
-            // threads compute them once per chunk (two ex2 each) for pass 2 to multiply by; the
-            // running sum and the range offset are formed exactly as the key-pair threads form
-            // them, so the numbers are the same. The barrier after the stage wait below
-            // publishes them.
+            // threads compute them once per chunk (two ex2 each) for pass 2 to multiply by, from
+            // the running sums pass 1 published and the range offset formed as the key-pair
+            // threads form it (so the numbers are the same). The barrier after the stage wait
+            // below publishes them.
             float2 *fac = reinterpret_cast<float2 *>(sm + FAC);
             if (kScalar && gt < kC) {
-                const int pt = gt / kGatePart, tbt = pt * kGatePart;
-                const float *gc = gsc + (c & 1) * kC;
-                float rt = 0.f;
-                for (int u = tbt; u <= gt; ++u) rt = fmaf(gc[u], kLog2e, rt);
+                const int pt = (gt >= gate_range_begin(1)) + (gt >= gate_range_begin(2));
+                const float rt = rtok[gt];
                 float Bt = 0.f, offt = 0.f;
 #pragma unroll
                 for (int q = 0; q < kGateParts; ++q) {
@@ -995,16 +1005,17 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 for (int t = max(vr - tb, 0); t < tl; ++t)
                     *reinterpret_cast<uint32_t *>(kt + sw128_offset((uint32_t)(tb + t), col)) = 0u;
             }
-            r0 = 0.f;
-            r1 = 0.f;
+            float r0 = 0.f, r1 = 0.f;
+            rs = make_float2(0.f, 0.f);
             // blocks of kGateBlock tokens: all loads of a block are issued before its stores, so a
             // block costs one shared-memory round trip
             if (!ext) {
                 // Q' = scale q 2^(b + L), K' = k 2^-(b + L) with b = off + r: the per-chunk
                 // constants (offset, L, log2 scale) are folded into two exponent biases. With a
                 // scalar gate only k is scaled here (see the epilogue).
-                const float eq0 = off0 + Lq0 + lsc, eq1 = off1 + Lq1 + lsc;
-                const float ek0 = -(off0 + Lq0), ek1 = -(off1 + Lq1);
+                const float2 eq = make_float2(off0 + Lq0 + lsc, off1 + Lq1 + lsc);
+                const float2 ek = make_float2(-(off0 + Lq0), -(off1 + Lq1));
+                const float2 neg1 = make_float2(-1.f, -1.f);
 #pragma unroll 1
                 for (int t0 = 0; t0 < tl; t0 += kGateBlock) {
                     float2 gv[kGateBlock];
@@ -1025,11 +1036,14 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                             const float fk = fac[tb + t0 + x].y;
                             kv[x] = pack_bf16(kf.x * fk, kf.y * fk);
                         } else {
-                            const float2 qf = unpack_bf16(qv[x]);
-                            r0 = fmaf(gv[x].x, kLog2e, r0);
-                            r1 = fmaf(gv[x].y, kLog2e, r1);
-                            qv[x] = pack_bf16(qf.x * ex2(r0 + eq0), qf.y * ex2(r1 + eq1));
-                            kv[x] = pack_bf16(kf.x * ex2(ek0 - r0), kf.y * ex2(ek1 - r1));
+                            // the pair's two lanes in packed fp32 instructions (ek - r as the exact
+                            // fma(r, -1, ek))
+                            rs = fma2(gv[x], l2e, rs);
+                            const float2 aq = add2(rs, eq), ak = fma2(rs, neg1, ek);
+                            const float2 pq = mul2(unpack_bf16(qv[x]), make_float2(ex2(aq.x), ex2(aq.y)));
+                            const float2 pk = mul2(kf, make_float2(ex2(ak.x), ex2(ak.y)));
+                            qv[x] = pack_bf16(pq.x, pq.y);
+                            kv[x] = pack_bf16(pk.x, pk.y);
                         }
                     }
 #pragma unroll
