@@ -118,8 +118,10 @@ constexpr uint32_t kColO2 = 448;
 
 // Shared-memory map of the output kernel (bytes from a 1024-aligned base).
 //   q/k/v ring (3 stages): raw tiles as 128B-swizzled [64 x 64] bf16 boxes, two per tile;
-//     the gate warps rewrite q -> Q' and k -> K' (or K^ in an extreme chunk) in place; the
-//     stage is released once the chunk's O MMAs (its last readers) have completed.
+//     the gate warps rewrite q -> Q' and k -> K' (or K^ in an extreme chunk) in place. With
+//     head pairs, once the chunk's P and U MMAs (the readers of K') have completed, the two
+//     heads' masked bf16 P tiles are written over K' (one box each). The stage is released
+//     once the chunk's O MMAs (its last readers) have completed.
 //   g ring (2 slots): the chunk's log-gates, [64 tokens][128] f32, loaded by TMA and
 //     released as soon as the gate warps have scaled the chunk.
 namespace om {
@@ -131,7 +133,7 @@ constexpr int NR = 4;                   // per-chunk ring of scales and flags (w
                                         // gates of c, read before O(c) completes)
 constexpr uint32_t Q = 0, K = 16384, V = 32768, QSTAGE = 49152;
 constexpr uint32_t G = NQ * QSTAGE, GSLOT = 32768;
-constexpr uint32_t P = G + NG * GSLOT;  // [64 x 64] bf16 P tile (128B swizzle)
+constexpr uint32_t P = G + NG * GSLOT;  // [64 x 64] bf16 P tile, 128B swizzle (not head pairs)
 constexpr uint32_t GAM = P + 8192;      // [NR][128] f32 exp(L_c): renormalisation scale
 constexpr uint32_t GAM2 = GAM + NR * 512; // [NR][128] f32 exp(Bc) (extreme chunks)
 constexpr uint32_t ENDS = GAM2 + NR * 512; // [128] f32 exp(L) after the latest chunk
@@ -140,7 +142,7 @@ constexpr uint32_t XCH = XF + 64;       // [<=4][128] f32 token-range totals of 
 constexpr uint32_t GSC = XCH + 2048;    // [2][64] f32 scalar gates of two chunks (scalar mode)
 constexpr uint32_t SCR = GSC + 512;     // [4][64] f32 exact-path scratch
 constexpr uint32_t BAR = SCR + 1024;    // mbarriers
-constexpr uint32_t NBAR = 26;
+constexpr uint32_t NBAR = 27;
 constexpr uint32_t TSLOT = BAR + NBAR * 8;
 constexpr uint32_t ALLOC = TSLOT + 16 + 1024;
 static_assert(ALLOC <= 232448, "output kernel shared memory");
@@ -152,13 +154,17 @@ static_assert(RTOK + 256 <= P, "scalar-gate stages and factors fit below the P t
 }  // namespace om
 
 // mbarrier indices of the output kernel
-// (q/k/v rings of up to 4 stages: 4 with a scalar gate, whose log-gate ring is unused)
+// (q/k/v rings of up to 4 stages: 4 with a scalar gate, whose log-gate ring is unused).
+// With head pairs, whose P tiles live in the stages, the state warps may write P(c + 1) before
+// O(c) is issued, so PBF (P tiles of chunk c written) alternates between two barriers, and
+// snapshot(c) may reuse bf16 snapshot buffer c % 2 only once O(c - 2) has read it (SBFREE,
+// two barriers): no barrier is ever two phases ahead of its waiter. A single head uses PBF
+// alone (its P conversion waits for the previous chunk's O).
 enum {
-    QFULL = 0, QEMPTY = 4, GFULL = 8, GEMPTY = 10, GDONE = 12, PFULL = 16, PFREE = 17, PBF = 18,
-    SREADY = 19, UDONE = 20, OFULL = 21, OFREE = 22, FIN = 23,
-    OAFULL = 24, PBF2 = 25,   // head pairs: first head's O^T done; second head's P tile written
+    QFULL = 0, QEMPTY = 4, GFULL = 8, GEMPTY = 10, GDONE = 12, PFULL = 16, PFREE = 17,
+    SREADY = 18, UDONE = 19, OFULL = 20, OFREE = 21, FIN = 22, PBF = 23, SBFREE = 25,
 };
-static_assert(FIN < (int)om::NBAR, "output kernel barrier map");
+static_assert(SBFREE + 2 <= (int)om::NBAR, "output kernel barrier map");
 
 constexpr int kGateWarps = 6;          // warps 10..15 (4 warps with 32-token ranges measured
                                        // 3-5% slower at B*H = 64 and 256, equal at 16)
@@ -315,8 +321,9 @@ __device__ __forceinline__ uint32_t par(int use) { return (uint32_t)use & 1u; }
 // pair is block diagonal; its off-diagonal blocks collect cross-head products that are never
 // read: the bf16 snapshot (the only operand read from the state) zeroes them, and hT
 // writes the diagonal blocks. P and the intra term are per head: P of the second head
-// accumulates apart, the P tile is filled twice, and the second head's O^T (its lanes are
-// value columns 64..127) accumulates in a second column block.
+// accumulates apart, each head's P tile fills one of the two boxes of the chunk's K' region,
+// and the second head's O^T (its lanes are value columns 64..127) accumulates in a second
+// column block.
 template <bool kScalar, bool kPacked, bool kPair = false>
 __global__ void __launch_bounds__(kOutThreads, 1)
 gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -324,6 +331,11 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                   const OutArgs a) {
     using namespace om;
     constexpr int NQ = kScalar ? NQS : om::NQ;   // q/k/v stages of this instance
+    // P tiles in the stage (head pairs: two per chunk, no wait for the previous chunk's O);
+    // otherwise one P tile, rewritten once the previous chunk's O MMAs have completed (that
+    // order measured 3-5 % faster for a single head, whose state warps would otherwise wait
+    // for the chunk's own state update)
+    constexpr bool kStageP = kPair;
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = align1024(smraw);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + BAR);
@@ -380,14 +392,15 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         }
         mbar_init(&bars[PFULL], 1);
         mbar_init(&bars[PFREE], 4);
-        mbar_init(&bars[PBF], 4);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars[PBF + i], 4);
+            mbar_init(&bars[SBFREE + i], 1);
+        }
         mbar_init(&bars[SREADY], 4);
         mbar_init(&bars[UDONE], 1);
         mbar_init(&bars[OFULL], 1);
         mbar_init(&bars[OFREE], 4);
         mbar_init(&bars[FIN], 1);
-        mbar_init(&bars[OAFULL], 1);
-        mbar_init(&bars[PBF2], 4);
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -475,7 +488,8 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         // Three MMA groups per chunk c, each issued back to back once its inputs are ready:
         //   U(c): snapshot of S~_c taken            -> S~ += K'^T V                (4 steps)
         //   P(c): gates of c done, P(c-1) read      -> P1 (d 0..63), P2 (d 64..127) (2 x 4)
-        //   O(c): P tile of c written, O(c-1) read  -> Oi = V^T P^T (4), Os = S~^T Q'^T (8)
+        //   O(c): P tile of c written, O(c-1) read  -> Os = S~^T Q'^T (8), Oi = V^T P^T (4)
+        //         (head pairs: the same for the second head into its own column block)
         // MMAs that accumulate into TMEM run at their latency, one after another, so the
         // order only decides who waits: U first (the state chain), then P, then O.
         // The whole warp runs the loop converged: every lane polls, lane 0's view of each
@@ -486,10 +500,9 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             const uint32_t idOi = idesc_bf16(128, 64, 1, 0);
             const uint32_t idOs = idesc_bf16(128, 64, 0, 0);
             int np = 0, nu = 0, no = 0;
-            int nb = kPair ? 0 : n;   // head pairs: second-head O groups issued
             uint32_t idle = 0;
             uint64_t t_idle = 0;
-            while (no < n || nb < n) {
+            while (no < n) {
                 bool prog = false;
                 const bool rU = __shfl_sync(0xffffffffu, nu < np && mbar_test(&bars[SREADY], par(nu)), 0);
                 if (rU) {
@@ -532,56 +545,39 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     prog = true;
                 }
                 const bool rO = __shfl_sync(
-                    0xffffffffu, no < nu && mbar_test(&bars[PBF], par(no)) &&
+                    0xffffffffu, no < nu &&
+                                     mbar_test(&bars[PBF + (kStageP ? no & 1 : 0)],
+                                               kStageP ? par(no >> 1) : par(no)) &&
                                      (no == 0 || mbar_test(&bars[OFREE], par(no - 1))), 0);
                 if (rO) {
                     tc_fence_after();
                     if (lane == 0) TRACE_OUT(6, no);
                     const uint32_t base = smem_u32(sm + (no % NQ) * QSTAGE);
-                    const uint32_t pbase = smem_u32(sm + P);
+                    const uint32_t pbase = kStageP ? base + K : smem_u32(sm + P);
                     if (elect_one()) {
-                        // one accumulator: the inter term S~^T Q'^T, then the intra term V^T P^T
+                        // one accumulator per head: the inter term S~^T Q'^T, then the intra term
+                        // V^T P^T with the head's P tile
 #pragma unroll
-                        for (int kk = 0; kk < 8; ++kk)
-                            mma_ts(tm + kColO, tm + kColSB + (no & 1) * 64 + kk * 8,
-                                   smem_desc(base + Q + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
-                                   idOs, kk > 0);
+                        for (int hp = 0; hp < (kPair ? 2 : 1); ++hp) {
+                            const uint32_t dst = hp ? kColO2 : kColO;
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            mma_ss(tm + kColO, smem_desc(base + V + kk * 2048, 8192, 1024),
-                                   smem_desc(pbase + kk * 32, 16, 1024), idOi, 1);
+                            for (int kk = 0; kk < 8; ++kk)
+                                mma_ts(tm + dst, tm + kColSB + (no & 1) * 64 + kk * 8,
+                                       smem_desc(base + Q + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
+                                       idOs, kk > 0);
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk)
+                                mma_ss(tm + dst, smem_desc(base + V + kk * 2048, 8192, 1024),
+                                       smem_desc(pbase + hp * 8192 + kk * 32, 16, 1024), idOi, 1);
+                        }
                         // U(no) and P(no) were issued before O(no)
-                        mma_commit(&bars[kPair ? OAFULL : OFULL]);
+                        mma_commit(&bars[OFULL]);
+                        if (kStageP) mma_commit(&bars[SBFREE + (no & 1)]);
                     }
                     __syncwarp();
                     if (lane == 0) TRACE_OUT(7, no);
                     ++no;
                     prog = true;
-                }
-                if (kPair) {
-                    // second head of the pair: its P tile replaced the first head's once the
-                    // first head's O^T had completed; lanes 64..127 of this block are its O^T
-                    const bool rB = __shfl_sync(0xffffffffu, nb < no && mbar_test(&bars[PBF2], par(nb)), 0);
-                    if (rB) {
-                        tc_fence_after();
-                        const uint32_t base = smem_u32(sm + (nb % NQ) * QSTAGE);
-                        const uint32_t pbase = smem_u32(sm + P);
-                        if (elect_one()) {
-#pragma unroll
-                            for (int kk = 0; kk < 8; ++kk)
-                                mma_ts(tm + kColO2, tm + kColSB + (nb & 1) * 64 + kk * 8,
-                                       smem_desc(base + Q + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
-                                       idOs, kk > 0);
-#pragma unroll
-                            for (int kk = 0; kk < 4; ++kk)
-                                mma_ss(tm + kColO2, smem_desc(base + V + kk * 2048, 8192, 1024),
-                                       smem_desc(pbase + kk * 32, 16, 1024), idOi, 1);
-                            mma_commit(&bars[OFULL]);
-                        }
-                        __syncwarp();
-                        ++nb;
-                        prog = true;
-                    }
                 }
                 if (prog) {
                     idle = 0;
@@ -693,8 +689,12 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         tmem_wait_st();
         for (int c = 0; c < n; ++c) {
             // ---- snapshot of S~_c
+            // (the snapshot buffer c % 2 is free once O(c - 2) has completed: without P tiles
+            // in the stages, the P conversion of c - 1 below waited for it)
             bool w = (c == 0 || mbar_wait(&bars[UDONE], par(c - 1))) &&
-                     mbar_wait(&bars[GDONE + c % NQ], par(c / NQ));
+                     mbar_wait(&bars[GDONE + c % NQ], par(c / NQ)) &&
+                     (!kStageP || c < 2 ||
+                      mbar_wait(&bars[SBFREE + (c & 1)], par((c >> 1) - 1)));
             if (named_bar_or(3, 128, !w)) { ok = false; break; }
             if (v == 0) TRACE_OUT(8, c);
             tc_fence_after();
@@ -739,23 +739,19 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[SREADY]);
             if (v == 0) TRACE_OUT(9, c);
-            // ---- P(c) -> masked bf16 P tile (the tile is free once O(c-1) completed)
-            w = mbar_wait(&bars[PFULL], par(c)) && (c == 0 || mbar_wait(&bars[OFULL], par(c - 1)));
+            // ---- P(c) -> masked bf16 P tile: over K' of chunk c's stage once its readers (the P
+            // and U MMAs of c) have completed, or in the P tile once O(c - 1) has read it
+            w = mbar_wait(&bars[PFULL], par(c)) &&
+                (kStageP ? mbar_wait(&bars[UDONE], par(c))
+                         : (c == 0 || mbar_wait(&bars[OFULL], par(c - 1))));
             if (named_bar_or(3, 128, !w)) { ok = false; break; }
             if (v == 0) TRACE_OUT(10, c);
             tc_fence_after();
             float prow[64];
             const int i = 16 * j + lane;        // P row held by this lane (lane < 16)
-            // head pairs fill the P tile twice: the second head's P once the first head's
-            // O^T (the tile's reader) has completed
-            bool pok = true;
+            // head pairs: one P tile per head, in the two boxes of the K' region
 #pragma unroll 1
             for (int ph = 0; ph < (kPair ? 2 : 1); ++ph) {
-                if (ph == 1) {
-                    w = mbar_wait(&bars[OAFULL], par(c));
-                    if (named_bar_or(3, 128, !w)) { pok = false; break; }
-                    tc_fence_after();
-                }
                 if (!ext) {
                     tmem_ld64(tmem_addr(tm, j, ph ? kColP2 : kColP), prow);
                 } else {
@@ -795,7 +791,7 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     if (lane == 0) mbar_arrive(&bars[PFREE]);
                 }
                 if (lane < 16) {
-                    uint8_t *pt = sm + P;
+                    uint8_t *pt = kStageP ? sm + (c % NQ) * QSTAGE + K + ph * 8192 : sm + P;
 #pragma unroll
                     for (int cc = 0; cc < 8; ++cc) {
                         uint32_t wv[4];
@@ -809,11 +805,10 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                             make_uint4(wv[0], wv[1], wv[2], wv[3]);
                     }
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[ph ? PBF2 : PBF]);
             }
-            if (!pok) { ok = false; break; }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[PBF + (kStageP ? c & 1 : 0)]);
             if (v == 0) TRACE_OUT(11, c);
         }
         if (ok && !bad_seq && a.hT && seg == a.splits - 1) {
