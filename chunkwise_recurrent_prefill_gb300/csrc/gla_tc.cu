@@ -747,62 +747,99 @@ gla_tc_out_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             if (named_bar_or(3, 128, !w)) { ok = false; break; }
             if (v == 0) TRACE_OUT(10, c);
             tc_fence_after();
-            float prow[64];
-            const int i = 16 * j + lane;        // P row held by this lane (lane < 16)
             // head pairs: one P tile per head, in the two boxes of the K' region
 #pragma unroll 1
             for (int ph = 0; ph < (kPair ? 2 : 1); ++ph) {
-                if (!ext) {
-                    tmem_ld64(tmem_addr(tm, j, ph ? kColP2 : kColP), prow);
-                } else {
-                    // exact route: P_ij = scale sum_d q_id k_jd exp(b_id - b_jd), j <= i
+                uint8_t *pt = kStageP ? sm + (c % NQ) * QSTAGE + K + ph * 8192 : sm + P;
+                if (!kScalar && !ext) {
+                    // the warp's 16 P rows (lanes 0..15 of its quarter) spread over all 32
+                    // threads: rows ia = 16 j + lane / 4 and ia + 8, column pairs 8 k + 2 (lane % 4)
+                    // (with a scalar gate this measured 4 % slower than one row per lane < 16)
+                    uint32_t pr[32];
+                    {
+                        uint32_t r0[16], r1[16];
+                        const uint32_t ta = tmem_addr(tm, j, ph ? kColP2 : kColP);
+                        tmem_ld16x256b_x4(ta, r0);
+                        tmem_ld16x256b_x4(ta + 32, r1);
+                        tmem_wait_ld();
+                        reg_fence(r0);
+                        reg_fence(r1);
 #pragma unroll
-                    for (int x = 0; x < 64; ++x) prow[x] = 0.f;
-                    float *gcol = scr, *qcol = scr + 64, *kcol = scr + 128, *bcol = scr + 192;
-                    const int64_t t0 = tbase + (int64_t)(cb + c) * kC;
-                    const int dlo = kPair ? 64 * ph : 0, dhi = kPair ? dlo + 64 : a.Dk;
-                    for (int d = dlo; d < dhi; ++d) {   // padded key dims add nothing
-                        if (st_t < 64) {
-                            const int64_t t = t0 + st_t;
-                            const bool in = t < tend;
-                            const int64_t idx = (((int64_t)bmap * a.T + t) * a.H + h) * a.Dk + d;
-                            gcol[st_t] = in ? (kScalar ? a.g[idx / a.Dk] : a.g[idx]) : 0.f;
-                            qcol[st_t] = in ? __bfloat162float(a.q[idx]) : 0.f;
-                            kcol[st_t] = in ? __bfloat162float(a.k[idx]) : 0.f;
+                        for (int x = 0; x < 16; ++x) {
+                            pr[x] = r0[x];
+                            pr[16 + x] = r1[x];
                         }
-                        named_bar_sync(3, 128);
-                        if (st_t == 0) {
-                            float s = 0.f;
-                            for (int t = 0; t < 64; ++t) { s += gcol[t]; bcol[t] = s; }
-                        }
-                        named_bar_sync(3, 128);
-                        if (lane < 16) {
-                            const float qi = a.scale * qcol[i], bi = bcol[i];
-#pragma unroll
-                            for (int x = 0; x < 64; ++x)
-                                if (x <= i) prow[x] += qi * kcol[x] * ex2((bi - bcol[x]) * kLog2e);
-                        }
-                        named_bar_sync(3, 128);
                     }
-                }
-                if (!kPair || ph == 1) {   // every P accumulator of c has been read
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&bars[PFREE]);
-                }
-                if (lane < 16) {
-                    uint8_t *pt = kStageP ? sm + (c % NQ) * QSTAGE + K + ph * 8192 : sm + P;
+                    if (!kPair || ph == 1) {   // every P accumulator of c has been read
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&bars[PFREE]);
+                    }
+                    const int ia = 16 * j + (lane >> 2), ib = ia + 8, c0 = 2 * (lane & 3);
 #pragma unroll
-                    for (int cc = 0; cc < 8; ++cc) {
-                        uint32_t wv[4];
+                    for (int k8 = 0; k8 < 8; ++k8) {
+                        const int col = 8 * k8 + c0;
+                        const float *f = reinterpret_cast<const float *>(pr + 4 * k8);
+                        *reinterpret_cast<uint32_t *>(pt + sw128_offset(ia, col)) =
+                            pack_bf16(col <= ia ? f[0] : 0.f, col + 1 <= ia ? f[1] : 0.f);
+                        *reinterpret_cast<uint32_t *>(pt + sw128_offset(ib, col)) =
+                            pack_bf16(col <= ib ? f[2] : 0.f, col + 1 <= ib ? f[3] : 0.f);
+                    }
+                } else {
+                    // one P row per lane < 16: the accumulator, or in an extreme chunk the exact
+                    // route P_ij = scale sum_d q_id k_jd exp(b_id - b_jd), j <= i
+                    float prow[64];
+                    const int i = 16 * j + lane;
+                    if (!ext) {
+                        tmem_ld64(tmem_addr(tm, j, ph ? kColP2 : kColP), prow);
+                    } else {
 #pragma unroll
-                        for (int x = 0; x < 4; ++x) {
-                            const int col = cc * 8 + 2 * x;
-                            wv[x] = pack_bf16(col <= i ? prow[col] : 0.f,
-                                              col + 1 <= i ? prow[col + 1] : 0.f);
+                        for (int x = 0; x < 64; ++x) prow[x] = 0.f;
+                        float *gcol = scr, *qcol = scr + 64, *kcol = scr + 128, *bcol = scr + 192;
+                        const int64_t t0 = tbase + (int64_t)(cb + c) * kC;
+                        const int dlo = kPair ? 64 * ph : 0, dhi = kPair ? dlo + 64 : a.Dk;
+                        for (int d = dlo; d < dhi; ++d) {   // padded key dims add nothing
+                            if (st_t < 64) {
+                                const int64_t t = t0 + st_t;
+                                const bool in = t < tend;
+                                const int64_t idx = (((int64_t)bmap * a.T + t) * a.H + h) * a.Dk + d;
+                                gcol[st_t] = in ? (kScalar ? a.g[idx / a.Dk] : a.g[idx]) : 0.f;
+                                qcol[st_t] = in ? __bfloat162float(a.q[idx]) : 0.f;
+                                kcol[st_t] = in ? __bfloat162float(a.k[idx]) : 0.f;
+                            }
+                            named_bar_sync(3, 128);
+                            if (st_t == 0) {
+                                float s = 0.f;
+                                for (int t = 0; t < 64; ++t) { s += gcol[t]; bcol[t] = s; }
+                            }
+                            named_bar_sync(3, 128);
+                            if (lane < 16) {
+                                const float qi = a.scale * qcol[i], bi = bcol[i];
+#pragma unroll
+                                for (int x = 0; x < 64; ++x)
+                                    if (x <= i) prow[x] += qi * kcol[x] * ex2((bi - bcol[x]) * kLog2e);
+                            }
+                            named_bar_sync(3, 128);
                         }
-                        *reinterpret_cast<uint4 *>(pt + sw128_offset(i, cc * 8)) =
-                            make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                    }
+                    if (!kPair || ph == 1) {   // every P accumulator of c has been read
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&bars[PFREE]);
+                    }
+                    if (lane < 16) {
+#pragma unroll
+                        for (int cc = 0; cc < 8; ++cc) {
+                            uint32_t wv[4];
+#pragma unroll
+                            for (int x = 0; x < 4; ++x) {
+                                const int col = cc * 8 + 2 * x;
+                                wv[x] = pack_bf16(col <= i ? prow[col] : 0.f,
+                                                  col + 1 <= i ? prow[col + 1] : 0.f);
+                            }
+                            *reinterpret_cast<uint4 *>(pt + sw128_offset(i, cc * 8)) =
+                                make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                        }
                     }
                 }
             }

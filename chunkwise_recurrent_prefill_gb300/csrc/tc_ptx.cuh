@@ -353,6 +353,20 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
         : "memory");
 }
 
+// 16 lanes x 32 consecutive columns of this warp's lane quarter (shape 16x256b, 4 repeats;
+// the lane field of taddr is the quarter's first lane): thread t receives, for k = 0..3,
+// registers 4k..4k+3 = (lane t/4, column 8k + 2(t%4)), (lane t/4, that column + 1),
+// (lane t/4 + 8, column 8k + 2(t%4)), (lane t/4 + 8, that column + 1). No wait.
+__device__ __forceinline__ void tmem_ld16x256b_x4(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
 // TMEM address of lane quarter `quarter` (warp id % 4) at column `col`.
 __device__ __forceinline__ uint32_t tmem_addr(uint32_t base, uint32_t quarter, uint32_t col) {
     return base + ((quarter * 32u) << 16) + col;
