@@ -280,7 +280,7 @@ gla_status gla_fwd_ex(const void *q, const void *k, const void *v, const float *
     if (gate != GLA_GATE_KEY && gate != GLA_GATE_SCALAR) return GLA_ERR_BAD_OPTION;
     gla_status rc = validate(q, k, v, g_log, h0, o, hT, B, T, H, Dk, Dv, io, gate, &sz);
     if (rc != GLA_OK) return rc;
-    gla::Problem p{q, k, v, g_log, scale, h0, o, hT, B, T, H, Dk, Dv, io, gate};
+    gla::Problem p{q, k, v, g_log, scale, h0, o, hT, B, T, H, Dk, Dv, io, gate, nullptr, 0};
     const int path = resolve_path(opt, p);
     if (path != GLA_PATH_EXACT && path != GLA_PATH_TC) return GLA_ERR_BAD_OPTION;
     if (opt && opt->seq_splits < 0) return GLA_ERR_BAD_OPTION;
@@ -351,7 +351,7 @@ gla_status gla_fwd_varlen(const void *q, const void *k, const void *v, const flo
             return GLA_ERR_ALIAS;
     }
     if (overlap(o, bv, hT, bs)) return GLA_ERR_ALIAS;
-    gla::Problem p{q, k, v, g_log, scale, h0, o, hT, N, T, H, Dk, Dv, io, gate, cu_seqlens};
+    gla::Problem p{q, k, v, g_log, scale, h0, o, hT, N, T, H, Dk, Dv, io, gate, cu_seqlens, 0};
     const int path = resolve_path(opt, p);
     if (path != GLA_PATH_EXACT && path != GLA_PATH_TC) return GLA_ERR_BAD_OPTION;
     if (path == GLA_PATH_EXACT && !gla::exact_supported(Dk, Dv)) return GLA_ERR_UNSUPPORTED_DIM;

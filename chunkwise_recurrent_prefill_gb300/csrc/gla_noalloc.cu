@@ -58,7 +58,7 @@ extern "C" gla_status gla_fwd_noalloc(const void *q, const void *k, const void *
                                       int64_t Dv, int seq_splits, gla_stream_t stream) {
     if (seq_splits < 0) return GLA_ERR_BAD_OPTION;
     const size_t cap = GLA_NOALLOC_SCRATCH_BYTES;
-    gla_options opt{GLA_PATH_AUTO, seq_splits, nullptr, 0};
+    gla_options opt{GLA_PATH_AUTO, seq_splits, nullptr, 0, GLA_GATE_KEY};
     size_t need = gla_fwd_workspace_size(B, T, H, Dk, Dv, GLA_IO_BF16, &opt);
     if (need > cap) {
         if (seq_splits > 0) {
